@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of the PLX attention hot path on B300.
+
+One step = one pass of the whole hot path on HBM-resident synthetic inputs:
+  * plx_fwd on the prefill workload B=4, H=16, N=2048, d=128 (bf16, causal,
+    rho = W_R x), outputs o and lse in fp32 (bf16 storage of o would add
+    rounding beyond the parity tolerance on rows where |o| is far above its RMS);
+  * plx_decode on the decode workload B=64, H=16, d=128, bf16 KV cache with
+    every length 4096 (split-KV + LSE combine).
+The headline value is prefill TFLOP/s, counting 8*d flop per causal
+(query, key) pair (four GEMMs: QK^T, rho K^T, PV, (P o R)V).  Decode is
+reported beside it in GB/s of K/V read (sum of lengths * H * d * 2 tensors
+* 2 bytes, plus q, rho, out).  Kernel durations come from CUDA events on the
+launching stream; L2 is flushed (a 256 MiB write) before every timed launch,
+outside the events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --impl reference the fp64 CPU oracle is timed on the host cores on a
+bounded sample of the same prefill workload (it is the reference arm: this
+method has no runnable reference implementation).  Under torchrun (N > 1)
+every rank runs the same per-GPU workload (weak scaling, no data-path
+collective) and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "PLX prefill TFLOP/s and decode KV GB/s vs B300 roofline, 1 GPU"
+PREFILL = "prefill_b4_h16_n2048_d128"
+DECODE = "decode_b64_h16_ctx4096_d128"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def prefill_flops(B, H, N, d, plx=True):
+    pairs = B * H * N * (N + 1) / 2
+    return pairs * (8 if plx else 4) * d
+
+
+def decode_bytes(seqlens, H, d, plx=True):
+    kv = float(np.sum(seqlens)) * H * d * 2 * 2
+    small = len(seqlens) * H * d * 2 * (3 if plx else 2)      # q, (rho), out (bf16)
+    return kv + small
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def read_traffic():
+    """Per-launch DRAM bytes of the timed kernels from the committed ncu
+    summary (profiles/traffic.json), or None when absent/stale."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return {}
+    with open(path) as f:
+        return json.load(f)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_prefill_sample(cfg, budget_s=12.0, x=None):
+    """Time the fp64 oracle (streaming form, all host threads) on whole heads
+    of the prefill workload until ``budget_s`` has elapsed or every head is
+    done.  Returns (TFLOP/s, seconds, description, threads)."""
+    import oracle
+    import plx_inputs
+    if x is None:
+        x = plx_inputs.prefill(cfg["B"], cfg["H"], cfg["N"], cfg["d"], seed=cfg["seed"], dtype="bf16",
+                               rho=cfg["rho"], keys=cfg["keys"])
+    heads = [(b, h) for b in range(cfg["B"]) for h in range(cfg["H"])]
+    done, flops, t0 = 0, 0.0, time.perf_counter()
+    threads = oracle.n_threads()
+    while done < len(heads) and time.perf_counter() - t0 < budget_s:
+        batch = heads[done:done + 4]
+        oracle.prefill("stream", x.q, x.k, x.v, x.rho, x.scale, heads=batch, threads=threads)
+        done += len(batch)
+        flops += len(batch) * prefill_flops(1, 1, cfg["N"], cfg["d"])
+    dt = time.perf_counter() - t0
+    desc = f"{done} of {len(heads)} heads (all {cfg['N']} rows each) of the prefill workload, stream form"
+    return flops / dt / 1e12, dt, desc, threads
+
+
+def run_reference(args, world, rank):
+    import plx_inputs
+    if rank != 0:
+        return 0
+    cfg = plx_inputs.CONFIGS[PREFILL]
+    x = plx_inputs.prefill(cfg["B"], cfg["H"], cfg["N"], cfg["d"], seed=cfg["seed"], dtype="bf16",
+                           rho=cfg["rho"], keys=cfg["keys"])
+    per_step_budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_prefill_sample(cfg, budget_s=min(per_step_budget, 2.0), x=x)
+    vals, times, desc, threads = [], [], "", 1
+    for _ in range(args.steps):
+        v, dt, desc, threads = oracle_prefill_sample(cfg, budget_s=per_step_budget, x=x)
+        vals.append(v)
+        times.append(dt)
+    value = float(np.median(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * float(np.median(times)), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL, "B": cfg["B"], "H": cfg["H"], "N": cfg["N"], "d": cfg["d"],
+                   "causal": True, "rho": "W_R x"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU path
+def run_ours(args, world, rank, local):
+    import torch
+    import parameterized_local_linear_02_b300 as plx
+    import plx_inputs
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peaks = read_peaks()
+    do_pf = args.only in ("both", "prefill")
+    do_dec = args.only in ("both", "decode")
+    extras = not args.no_extras
+
+    pc = plx_inputs.CONFIGS[PREFILL]
+    dc = plx_inputs.CONFIGS[DECODE]
+    B, H, N, d = pc["B"], pc["H"], pc["N"], pc["d"]
+    Bd, Hd, S_cap = (args.decode_batch or dc["B"]), dc["H"], dc["S_cap"]
+    x = None
+    if do_pf:
+        x = plx_inputs.prefill(B, H, N, d, seed=pc["seed"], dtype="bf16", rho=pc["rho"], keys=pc["keys"])
+        t = x.device_tensors(dev)
+        out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    if do_dec:
+        dd = plx_inputs.decode_device(Bd, Hd, dc["d"], S_cap, seed=dc["seed"], seqlens=dc["seqlens"],
+                                      rho_std=dc["rho_std"], device=dev)
+        dout = torch.empty((Bd, Hd, dc["d"]), dtype=torch.bfloat16, device=dev)
+        dlse = torch.empty((Bd, Hd), dtype=torch.float32, device=dev)
+        splits = plx.plx_decode_num_splits(Bd, Hd, dc["d"], S_cap)
+        ws_bytes = plx.plx_decode_workspace_size(Bd, Hd, dc["d"], S_cap, splits)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def fwd(rho=True):
+        plx.plx_fwd(t["q"], t["k"], t["v"], t["rho"] if rho else None, out=out, lse=lse)
+
+    def dec(rho=True):
+        plx.plx_decode(dd["q"], dd["rho"] if rho else None, dd["k_cache"], dd["v_cache"], dd["seqlens"],
+                       num_splits=splits, workspace=ws, out=dout, lse=dlse)
+
+    launches_per_step = (1 if do_pf else 0) + ((2 if splits > 1 else 1) if do_dec else 0)
+
+    def timed(fn, k):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        return evs
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        if do_pf:
+            fwd()
+        if do_dec:
+            dec()
+    torch.cuda.synchronize()
+    if plx.plx_last_device_error() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # ---- timed region: K steps of (prefill, decode)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev_f, ev_d = [], []
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        if do_pf:
+            ev_f += timed(fwd, 1)
+        if do_dec:
+            ev_d += timed(dec, 1)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    wall_ms = t_start.elapsed_time(t_end)
+    status = plx.plx_last_device_error()
+    line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic"}
+    traffic = read_traffic()
+
+    if do_pf:
+        f_avg = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev_f])), world)
+        flops = prefill_flops(B, H, N, d)
+        value = world * flops / (f_avg * 1e-3) / 1e12
+        line.update({"value": value, "unit": "TFLOP/s"})
+        line["roofline"] = {
+            "bound": "tensor", "achieved": value / world, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": value / world / peaks["bf16_tflops"],
+            "traffic": traffic.get("plx_fwd", {}).get("bytes_per_launch"),
+            "peak_source": f"{peaks['source']} bf16 dense (burst)",
+            "frac_of_sustained": value / world / peaks["bf16_tflops_sustained"],
+            "kernel": "plx_fwd_tc_kernel<128,true>", "flop_per_launch": flops, "avg_launch_ms": f_avg}
+    if do_dec:
+        d_avg = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev_d])), world)
+        dbytes = decode_bytes(dd["seqlens_host"], Hd, dc["d"])
+        d_gbs = world * dbytes / (d_avg * 1e-3) / 1e9
+        droof = {"bound": "hbm", "achieved": d_gbs / world, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                 "frac": d_gbs / world / peaks["hbm_gbs"],
+                 "traffic": traffic.get("plx_decode", {}).get("bytes_per_launch"),
+                 "peak_source": f"{peaks['source']} HBM copy", "bytes_per_launch": dbytes,
+                 "avg_launch_ms": d_avg,
+                 "kernel": "plx_decode_split_kernel<128,true>" + (" + combine" if splits > 1 else "")}
+        line["decode"] = {"value": d_gbs, "unit": "GB/s", "ms": d_avg, "batch": Bd, "splits": splits,
+                          "tokens_per_s": world * Bd / (d_avg * 1e-3), "roofline": droof}
+        if not do_pf:
+            line.update({"value": d_gbs, "unit": "GB/s", "roofline": droof})
+    line["ms_per_step"] = (f_avg if do_pf else 0.0) + (d_avg if do_dec else 0.0)
+    line["config"] = {"workload": PREFILL if do_pf else DECODE, "B": B, "H": H, "N": N, "d": d, "causal": True,
+                      "rho": "W_R x", "out": "fp32 o + fp32 lse",
+                      "l2": "flushed (256 MiB write) before every launch"}
+    if do_dec:
+        line["config"].update({"decode_workload": DECODE, "decode_batch": Bd, "decode_splits": splits})
+
+    if extras:
+        sa = {}
+        if do_pf:
+            sa_f = timed(lambda: fwd(False), max(5, args.steps // 2))
+        if do_dec:
+            sa_d = timed(lambda: dec(False), max(5, args.steps // 2))
+        torch.cuda.synchronize()
+        if do_pf:
+            sa_f_ms = float(np.mean([a.elapsed_time(b) for a, b in sa_f]))
+            sa.update({"prefill_ms": sa_f_ms,
+                       "prefill_tflops_4d": prefill_flops(B, H, N, d, False) / sa_f_ms / 1e9,
+                       "plx_over_sa_time": f_avg / sa_f_ms})
+        if do_dec:
+            sa_d_ms = float(np.mean([a.elapsed_time(b) for a, b in sa_d]))
+            sa.update({"decode_ms": sa_d_ms,
+                       "decode_gbs": decode_bytes(dd["seqlens_host"], Hd, dc["d"], False) / sa_d_ms / 1e6})
+        line["softmax_attention_same_kernel"] = sa
+        if do_pf:
+            # end to end through the public API with host buffers
+            pin = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v", "rho")}
+            h_out = torch.empty((B, H, N, d), dtype=torch.float32).pin_memory()
+            h_lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+            d_in = {n: torch.empty_like(t[n]) for n in pin}
+            h2d = sum(v.numel() * v.element_size() for v in pin.values())
+            d2h = h_out.numel() * 4 + h_lse.numel() * 4
+
+            def e2e_step():
+                for n in pin:
+                    d_in[n].copy_(pin[n], non_blocking=True)
+                plx.plx_fwd(d_in["q"], d_in["k"], d_in["v"], d_in["rho"], out=out, lse=lse)
+                h_out.copy_(out, non_blocking=True)
+                h_lse.copy_(lse, non_blocking=True)
+
+            for _ in range(2):
+                e2e_step()
+            torch.cuda.synchronize()
+            e_steps = max(5, args.steps // 2)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(e_steps):
+                e2e_step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world)
+            line["e2e"] = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+                           "path": "pinned host q,k,v,rho -> device, plx_fwd, out+lse -> pinned host"}
+    line["gpu_launches"] = launches_per_step * args.steps
+    line["clocks"] = clocks
+    line["wall_ms_timed_region"] = wall_ms
+    line["device_status"] = status
+    if rank == 0 and world == 1 and do_pf and not args.no_cpu_baseline:
+        v, dt, desc, threads = oracle_prefill_sample(pc, budget_s=args.cpu_budget, x=x)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=("both", "prefill", "decode"), default="both",
+                    help="run one kernel only (profiling of a single kernel)")
+    ap.add_argument("--decode-batch", type=int, default=None,
+                    help="decode batch (default: the decode workload's 64); smaller for profiling")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the softmax-attention comparison and the end-to-end leg")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps, always
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

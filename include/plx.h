@@ -1,0 +1,158 @@
+/*
+ * plx.h -- C ABI of the Parallax (PLX) attention hot path on B300 (sm_103a).
+ *
+ * PLX is causal softmax attention with a covariance correction driven by a
+ * per-token probe ("Parallax: Parameterized Local Linear Attention for
+ * Language Modeling", arXiv:2605.29157; zhichai.net section 1.3 and
+ * gist.science "Meccanismo Principale"):
+ *
+ *   o_i = o_i^SA - Sigma_KV^(i) rho_i
+ *   o_i^SA = sum_{j<=i} w_ij v_j,  w_ij = softmax_{j<=i}(scale * q_i . k_j)
+ *   Sigma_KV^(i) = sum_{j<=i} w_ij (v_j - vbar_i)(k_j - kbar_i)^T   (d_v x d_k)
+ *   vbar_i = o_i^SA,  kbar_i = sum_j w_ij k_j
+ *
+ * The probe rho_i = W_R x_i is an input (its projection is computed before
+ * this call).  The boundary term eta_i is zero and there is no solve
+ * (gist.science, "Meccanismo Principale").  The kernels never form Sigma_KV:
+ * they stream K/V once and use
+ *
+ *   Sigma_KV rho = sum_j w_j (k_j . rho) v_j - vbar (kbar . rho),
+ *   so o = (1 + c) vbar - u,  c = sum_j w_j (k_j . rho),  u = sum_j w_j (k_j . rho) v_j,
+ *
+ * the FlashAttention-compatible streaming algorithm that reuses the K/V
+ * stream (gist.science, "Algoritmo Consapevole dell'Hardware").
+ *
+ * Conventions for every entry point:
+ *   - Tensors are row-major and contiguous: q, k, v, rho, out are [B][H][N][d]
+ *     (d fastest); the decode cache is [B][H][S_cap][d].
+ *   - All pointers are DEVICE pointers owned by the caller; the library keeps
+ *     no reference after the call returns and allocates no device memory
+ *     (the decode workspace is passed in).  The library holds one device
+ *     status word per GPU (a static __device__ variable).
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call is asynchronous on that stream and never synchronises,
+ *     except plx_last_device_error.
+ *   - Arguments are validated before any launch; on a failed check the call
+ *     returns a status and launches nothing.  A launch error maps to
+ *     PLX_ERR_CUDA.  No C++ exception crosses this boundary.
+ *   - Passing rho == NULL selects the softmax-attention instantiation of the
+ *     same kernel (the zero probe of the attention family, zhichai.net
+ *     section 2.1): it skips the probe GEMMs, so it is the baseline for
+ *     timing, and its output equals PLX with rho = 0.
+ *   - scale multiplies q.k only; rho.k is not scaled.  lse is the natural
+ *     log of sum_j exp(scale * q_i . k_j), fp32.
+ */
+#ifndef PLX_H
+#define PLX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PLX_OK = 0,
+    PLX_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad dtype */
+    PLX_ERR_UNSUPPORTED = 2, /* head dim or size this build has no kernel for */
+    PLX_ERR_MISALIGNED = 3,  /* pointer not 16-byte aligned (lse: 4-byte) */
+    PLX_ERR_CUDA = 4,        /* a CUDA call or kernel launch failed */
+    PLX_ERR_TIMEOUT = 5,     /* a device-side wait gave up (see plx_last_device_error) */
+    PLX_ERR_WORKSPACE = 6,   /* decode workspace missing or too small */
+    PLX_ERR_RANGE = 7        /* plx_fwd produced a non-finite output (see plx_last_device_error) */
+} plx_status;
+
+typedef enum { PLX_BF16 = 0, PLX_F32 = 1 } plx_dtype;
+
+/* Library version, e.g. 100 for 0.1.0. */
+int plx_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* plx_strerror(plx_status status);
+
+/*
+ * plx_fwd -- causal prefill / training forward, bf16 inputs, fp32 accumulate.
+ * Streaming algorithm of gist.science "Algoritmo Consapevole dell'Hardware":
+ * per K/V tile, S = scale Q K^T and R = rho K^T on the tensor cores, online
+ * softmax, then O += P V and U += (P o R) V, finally o = (1 + c) vbar - u.
+ *
+ *   q, k, v, rho : bf16 [B][H][N][d], 16-byte aligned; rho may be NULL (SA).
+ *   out          : [B][H][N][d] of out_dtype (PLX_BF16 or PLX_F32), 16-byte aligned.
+ *   lse          : fp32 [B][H][N], 4-byte aligned, or NULL.
+ *   B, H, N >= 1; d in {64, 128}.  scale >= 0 finite (usually 1/sqrt(d)).
+ * Numerics: S = QK^T and R = rho K^T take the bf16 inputs exactly with fp32
+ * accumulation; P, P o R and V enter the PV GEMMs as fp16 (V is re-encoded
+ * from bf16 in shared memory), with fp32 accumulation.  Supported range:
+ * |v| < 65504 and |rho . k| < 4094 (P o R stays inside fp16 because the
+ * lazily updated softmax keeps P <= 16).  Outside it the output may be
+ * non-finite; the kernel then sets a device flag that plx_last_device_error
+ * reports as PLX_ERR_RANGE.
+ * Errors: PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED (other d, or more than
+ * 2^31 - 1 work items), PLX_ERR_MISALIGNED, PLX_ERR_CUDA.
+ */
+plx_status plx_fwd(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
+                   int B, int H, int N, int d, float scale, plx_dtype out_dtype, void* stream);
+
+/*
+ * plx_fwd_f32 -- the same causal forward with fp32 inputs, fp32 arithmetic on
+ * the CUDA cores (the high-precision path; no tensor cores).
+ *
+ *   q, k, v, rho : fp32 [B][H][N][d], 16-byte aligned; rho may be NULL (SA).
+ *   out          : fp32 [B][H][N][d];  lse : fp32 [B][H][N] or NULL.
+ *   B, H, N >= 1; d a multiple of 32 in [32, 256].
+ * Errors: as plx_fwd.
+ */
+plx_status plx_fwd_f32(const float* q, const float* k, const float* v, const float* rho, float* out,
+                       float* lse, int B, int H, int N, int d, float scale, void* stream);
+
+/*
+ * plx_decode -- one query token per sequence against a bf16 KV cache
+ * (the streaming decode of gist.science "Algoritmo Consapevole
+ * dell'Hardware").  The cache already holds the current token at position
+ * seqlens[b]-1; the query attends to positions 0..seqlens[b]-1.  The cache
+ * of each (b, h) is split into num_splits ranges processed by separate
+ * thread blocks; their partial states (max, sum, sum of probe terms and the
+ * two weighted value sums) are merged with a log-sum-exp weighted combine.
+ *
+ *   q, rho            : bf16 [B][H][d], 16-byte aligned; rho may be NULL (SA).
+ *   k_cache, v_cache  : bf16 [B][H][S_cap][d], 16-byte aligned.
+ *   seqlens           : int32 [B] on the device.  A length <= 0 gives o = 0
+ *                       and lse = -inf; a length > S_cap is clamped to S_cap
+ *                       and flags PLX_ERR_INVALID_ARG in the device status word.
+ *   out               : [B][H][d] of out_dtype;  lse : fp32 [B][H] or NULL.
+ *   d in {64, 128};  S_cap >= 1.
+ *   num_splits        : 0 picks a split count for this GPU; else 1..1024.
+ *   workspace         : device scratch of at least
+ *                       plx_decode_workspace_size(B, H, d, S_cap, num_splits)
+ *                       bytes, 16-byte aligned (may be NULL when that size is 0).
+ *                       Its contents need no initialisation.
+ * Errors: PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_MISALIGNED,
+ * PLX_ERR_WORKSPACE, PLX_ERR_CUDA.
+ */
+plx_status plx_decode(const void* q, const void* rho, const void* k_cache, const void* v_cache,
+                      const int32_t* seqlens, void* out, float* lse, int B, int H, int d, int S_cap,
+                      float scale, int num_splits, void* workspace, size_t workspace_bytes,
+                      plx_dtype out_dtype, void* stream);
+
+/* The split count plx_decode uses for these sizes when num_splits == 0, on
+ * the current device (queries the SM count once per device). */
+int plx_decode_num_splits(int B, int H, int d, int S_cap);
+
+/* Workspace bytes plx_decode needs (0 when one split suffices). */
+size_t plx_decode_workspace_size(int B, int H, int d, int S_cap, int num_splits);
+
+/*
+ * plx_last_device_error -- synchronises `stream`, then reads and clears the
+ * current device's status word.  Returns PLX_ERR_TIMEOUT if a kernel gave up
+ * a bounded wait, PLX_ERR_INVALID_ARG if a decode length exceeded S_cap,
+ * PLX_ERR_RANGE if plx_fwd wrote a non-finite output, PLX_ERR_CUDA if
+ * synchronisation failed, else PLX_OK.
+ */
+plx_status plx_last_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PLX_H */

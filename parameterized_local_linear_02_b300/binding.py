@@ -1,0 +1,207 @@
+"""ctypes binding of libplx.so (argument marshalling only).
+
+Each function checks tensor dtypes, shapes, devices and contiguity, passes
+raw device pointers and the current torch CUDA stream to the C entry point
+of the same name (include/plx.h), and raises PlxError on a non-zero status.
+Outputs (and the decode workspace) are allocated with torch when the caller
+does not pass them.  Nothing here computes any part of the attention.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+PLX_BF16, PLX_F32 = 0, 1
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "misaligned", 4: "CUDA error", 7: "range",
+           5: "device-side wait timed out", 6: "workspace too small"}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class PlxError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {plx_strerror(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def library() -> ctypes.CDLL:
+    """Load libplx.so, building it first if it is missing or older than its
+    sources.  Raises if it cannot be built or loaded."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if _build.stale():
+            _build.build()
+        lib = ctypes.CDLL(_build.LIB)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.plx_version.restype = i
+        lib.plx_version.argtypes = []
+        lib.plx_strerror.restype = ctypes.c_char_p
+        lib.plx_strerror.argtypes = [i]
+        lib.plx_fwd.restype = i
+        lib.plx_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.plx_fwd_f32.restype = i
+        lib.plx_fwd_f32.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, vp]
+        lib.plx_decode.restype = i
+        lib.plx_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, i, vp]
+        lib.plx_decode_num_splits.restype = i
+        lib.plx_decode_num_splits.argtypes = [i, i, i, i]
+        lib.plx_decode_workspace_size.restype = sz
+        lib.plx_decode_workspace_size.argtypes = [i, i, i, i, i]
+        lib.plx_last_device_error.restype = i
+        lib.plx_last_device_error.argtypes = [vp]
+        _lib = lib
+        return lib
+
+
+def plx_version() -> int:
+    return library().plx_version()
+
+
+def plx_strerror(status: int) -> str:
+    try:
+        return library().plx_strerror(int(status)).decode()
+    except OSError:
+        return _STATUS.get(int(status), "unknown status")
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise PlxError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _out_code(dtype) -> int:
+    if dtype == torch.bfloat16:
+        return PLX_BF16
+    if dtype == torch.float32:
+        return PLX_F32
+    raise TypeError("out dtype must be torch.bfloat16 or torch.float32")
+
+
+def plx_fwd(q, k, v, rho=None, *, scale=None, out=None, lse=None, out_dtype=torch.bfloat16,
+            with_lse=True):
+    """Causal PLX forward, bf16 [B, H, N, d] inputs on the tensor cores.
+
+    ``rho=None`` runs the softmax-attention instantiation of the same kernel.
+    Returns ``(out, lse)``; ``lse`` is None when ``with_lse`` is False."""
+    B, H, N, d = q.shape
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v)) + ((("rho", rho),) if rho is not None else ()):
+        _need(t, name, torch.bfloat16, (B, H, N, d), dev)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=out_dtype, device=dev)
+    else:
+        _need(out, "out", out.dtype, (B, H, N, d), dev)
+    if lse is None and with_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, N), dev)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().plx_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(out), _ptr(lse), B, H, N, d,
+                           scale, _out_code(out.dtype), _stream(dev))
+    _check(st, "plx_fwd")
+    return out, lse
+
+
+def plx_fwd_f32(q, k, v, rho=None, *, scale=None, out=None, lse=None, with_lse=True):
+    """Causal PLX forward, fp32 [B, H, N, d] inputs, fp32 arithmetic."""
+    B, H, N, d = q.shape
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v)) + ((("rho", rho),) if rho is not None else ()):
+        _need(t, name, torch.float32, (B, H, N, d), dev)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    else:
+        _need(out, "out", torch.float32, (B, H, N, d), dev)
+    if lse is None and with_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, N), dev)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().plx_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(out), _ptr(lse), B, H, N, d,
+                               scale, _stream(dev))
+    _check(st, "plx_fwd_f32")
+    return out, lse
+
+
+def plx_decode_num_splits(B: int, H: int, d: int, S_cap: int) -> int:
+    return library().plx_decode_num_splits(B, H, d, S_cap)
+
+
+def plx_decode_workspace_size(B: int, H: int, d: int, S_cap: int, num_splits: int = 0) -> int:
+    return library().plx_decode_workspace_size(B, H, d, S_cap, num_splits)
+
+
+def plx_decode(q, rho, k_cache, v_cache, seqlens, *, scale=None, num_splits=0, workspace=None,
+               out=None, lse=None, out_dtype=torch.bfloat16, with_lse=True):
+    """One-token PLX decode over a bf16 [B, H, S_cap, d] KV cache.
+
+    ``q``, ``rho``: bf16 [B, H, d] (``rho=None``: softmax attention);
+    ``seqlens``: int32 [B] on the device.  Returns ``(out, lse)``."""
+    B, H, S_cap, d = k_cache.shape
+    dev = k_cache.device
+    _need(q, "q", torch.bfloat16, (B, H, d), dev)
+    if rho is not None:
+        _need(rho, "rho", torch.bfloat16, (B, H, d), dev)
+    _need(k_cache, "k_cache", torch.bfloat16, (B, H, S_cap, d), dev)
+    _need(v_cache, "v_cache", torch.bfloat16, (B, H, S_cap, d), dev)
+    _need(seqlens, "seqlens", torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty((B, H, d), dtype=out_dtype, device=dev)
+    else:
+        _need(out, "out", out.dtype, (B, H, d), dev)
+    if lse is None and with_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, (B, H), dev)
+    need = plx_decode_workspace_size(B, H, d, S_cap, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().plx_decode(_ptr(q), _ptr(rho), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
+                              _ptr(out), _ptr(lse), B, H, d, S_cap, scale, int(num_splits),
+                              _ptr(workspace), ws_bytes, _out_code(out.dtype), _stream(dev))
+    _check(st, "plx_decode")
+    return out, lse
+
+
+def plx_last_device_error(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device
+    status: 0 ok, 5 a device wait timed out, 1 a decode length exceeded the
+    cache capacity."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    return library().plx_last_device_error(_stream(dev))

@@ -1,0 +1,334 @@
+// plx.cu -- the C ABI of the PLX attention library (see include/plx.h).
+//
+// One translation unit: argument validation, launch configuration, TMA
+// tensor-map encoding and the device status word, around the kernels in
+// fwd_tc.cuh (tcgen05 prefill), fwd_f32.cuh (fp32 prefill) and decode.cuh
+// (split-KV decode + combine).  Every entry point validates its arguments
+// before launching anything and never lets a C++ exception escape.
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "plx.h"
+#include "decode.cuh"
+#include "fwd_f32.cuh"
+#include "fwd_tc.cuh"
+
+namespace {
+
+using plx::DecodeCfg;
+using plx::FwdTcCfg;
+
+constexpr int kMaxDevices = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+
+inline bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
+
+struct DeviceInfo {
+    int sm_count = 0;
+    int decode_blocks_per_sm[2] = {0, 0};   // d = 64, d = 128
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_tried = false;
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+// Per-device facts and one-time kernel attributes.  Returns nullptr on error.
+const DeviceInfo* device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_dev_ready[dev]) return &g_dev[dev];
+    DeviceInfo info;
+    if (cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+    cudaError_t e = cudaSuccess;
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, true>, FwdTcCfg<128, true>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, false>, FwdTcCfg<128, false>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, true>, FwdTcCfg<64, true>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, false>, FwdTcCfg<64, false>::SMEM);
+    e = e ? e : set_smem(plx::plx_decode_split_kernel<128, true>, DecodeCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_decode_split_kernel<128, false>, DecodeCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_decode_split_kernel<64, true>, DecodeCfg<64>::SMEM);
+    e = e ? e : set_smem(plx::plx_decode_split_kernel<64, false>, DecodeCfg<64>::SMEM);
+    if (e != cudaSuccess) return nullptr;
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, plx::plx_decode_split_kernel<64, true>,
+                                                      DecodeCfg<64>::THREADS, DecodeCfg<64>::SMEM) != cudaSuccess)
+        return nullptr;
+    info.decode_blocks_per_sm[0] = nb > 0 ? nb : 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, plx::plx_decode_split_kernel<128, true>,
+                                                      DecodeCfg<128>::THREADS, DecodeCfg<128>::SMEM) != cudaSuccess)
+        return nullptr;
+    info.decode_blocks_per_sm[1] = nb > 0 ? nb : 1;
+    g_dev[dev] = info;
+    g_dev_ready[dev] = true;
+    return &g_dev[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode_tried) {
+        g_encode_tried = true;
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return g_encode;
+}
+
+// 3-D bf16 tensor map over [BH][N][d] with a {64, box_rows, 1} box, 128B swizzle.
+bool make_map(CUtensorMap* map, const void* base, int d, int N, long long BH, int box_rows) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+plx_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
+}
+
+bool valid_scale(float scale) { return std::isfinite(scale) && scale >= 0.f; }
+
+template <int D, bool PLX>
+plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
+                         int N, long long BH, float scale, plx_dtype out_dtype, cudaStream_t stream,
+                         int sm_count) {
+    using Cfg = FwdTcCfg<D, PLX>;
+    const long long n_qt = (N + Cfg::BM - 1) / Cfg::BM;
+    const long long n_items = BH * n_qt;
+    if (n_items > INT_MAX || BH > INT_MAX) return PLX_ERR_UNSUPPORTED;
+    CUtensorMap mq, mr, mk, mv;
+    if (!make_map(&mq, q, D, N, BH, Cfg::BM) || !make_map(&mk, k, D, N, BH, Cfg::BN) ||
+        !make_map(&mv, v, D, N, BH, Cfg::BN))
+        return PLX_ERR_CUDA;
+    if (PLX) {
+        if (!make_map(&mr, rho, D, N, BH, Cfg::BM)) return PLX_ERR_CUDA;
+    } else {
+        mr = mq;
+    }
+    plx::FwdTcParams p;
+    p.out = out;
+    p.lse = lse;
+    p.N = N;
+    p.BH = static_cast<int>(BH);
+    p.n_qt = static_cast<int>(n_qt);
+    p.n_items = static_cast<int>(n_items);
+    p.scale_log2 = scale * kLog2e;
+    p.out_f32 = out_dtype == PLX_F32;
+    const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
+    plx::plx_fwd_tc_kernel<D, PLX><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, p);
+    return launch_status();
+}
+
+template <int DPL, bool PLX>
+void launch_f32(const plx::FwdF32Params& p, long long BH, cudaStream_t stream) {
+    dim3 grid((p.N + plx::F32_ROWS_PER_BLOCK - 1) / plx::F32_ROWS_PER_BLOCK, static_cast<unsigned>(BH));
+    plx::plx_fwd_f32_kernel<DPL, PLX><<<grid, plx::F32_WARPS * 32, 0, stream>>>(p);
+}
+
+template <bool PLX>
+bool dispatch_f32(const plx::FwdF32Params& p, int d, long long BH, cudaStream_t s) {
+    switch (d / 32) {
+        case 1: launch_f32<1, PLX>(p, BH, s); return true;
+        case 2: launch_f32<2, PLX>(p, BH, s); return true;
+        case 3: launch_f32<3, PLX>(p, BH, s); return true;
+        case 4: launch_f32<4, PLX>(p, BH, s); return true;
+        case 5: launch_f32<5, PLX>(p, BH, s); return true;
+        case 6: launch_f32<6, PLX>(p, BH, s); return true;
+        case 7: launch_f32<7, PLX>(p, BH, s); return true;
+        case 8: launch_f32<8, PLX>(p, BH, s); return true;
+        default: return false;
+    }
+}
+
+int decode_splits(const DeviceInfo& info, long long BH, int d, int S_cap) {
+    constexpr int T = 32;
+    const long long slots = static_cast<long long>(info.sm_count) * info.decode_blocks_per_sm[d == 128 ? 1 : 0];
+    const long long max_by_len = (static_cast<long long>(S_cap) + 8 * T - 1) / (8 * T);   // >= 8 tiles per split
+    long long want = (2 * slots + BH - 1) / BH;
+    if (want > max_by_len) want = max_by_len;
+    if (want > 1024) want = 1024;
+    if (want < 1) want = 1;
+    return static_cast<int>(want);
+}
+
+size_t decode_ws_bytes(long long BH, int d, int splits) {
+    if (splits <= 1) return 0;
+    return static_cast<size_t>(BH) * splits * (2 * d + 4) * sizeof(float);
+}
+
+template <int D, bool PLX>
+void launch_decode(const plx::DecodeParams& p, long long BH, cudaStream_t s) {
+    using Cfg = DecodeCfg<D>;
+    dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(p.splits));
+    plx::plx_decode_split_kernel<D, PLX><<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(p);
+    if (p.splits > 1) plx::plx_decode_combine_kernel<D, PLX><<<static_cast<unsigned>(BH), D, 0, s>>>(p);
+}
+
+}  // namespace
+
+extern "C" {
+
+int plx_version(void) { return 100; }
+
+const char* plx_strerror(plx_status status) {
+    switch (status) {
+        case PLX_OK: return "ok";
+        case PLX_ERR_INVALID_ARG: return "invalid argument";
+        case PLX_ERR_UNSUPPORTED: return "unsupported size or head dimension";
+        case PLX_ERR_MISALIGNED: return "misaligned pointer";
+        case PLX_ERR_CUDA: return "CUDA error";
+        case PLX_ERR_TIMEOUT: return "device-side wait timed out";
+        case PLX_ERR_WORKSPACE: return "decode workspace missing or too small";
+        case PLX_ERR_RANGE: return "non-finite output (inputs outside the supported range)";
+        default: return "unknown status";
+    }
+}
+
+plx_status plx_fwd(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse, int B,
+                   int H, int N, int d, float scale, plx_dtype out_dtype, void* stream) {
+    try {
+        if (!q || !k || !v || !out) return PLX_ERR_INVALID_ARG;
+        if (B < 1 || H < 1 || N < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
+        if (out_dtype != PLX_BF16 && out_dtype != PLX_F32) return PLX_ERR_INVALID_ARG;
+        if (d != 128 && d != 64) return PLX_ERR_UNSUPPORTED;
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+            (rho && !aligned(rho, 16)) || (lse && !aligned(lse, 4)))
+            return PLX_ERR_MISALIGNED;
+        const DeviceInfo* info = device_info();
+        if (!info) return PLX_ERR_CUDA;
+        const long long BH = static_cast<long long>(B) * H;
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        if (d == 128)
+            return rho ? launch_fwd_tc<128, true>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count)
+                       : launch_fwd_tc<128, false>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s,
+                                                   info->sm_count);
+        return rho ? launch_fwd_tc<64, true>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count)
+                   : launch_fwd_tc<64, false>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count);
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+plx_status plx_fwd_f32(const float* q, const float* k, const float* v, const float* rho, float* out, float* lse,
+                       int B, int H, int N, int d, float scale, void* stream) {
+    try {
+        if (!q || !k || !v || !out) return PLX_ERR_INVALID_ARG;
+        if (B < 1 || H < 1 || N < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
+        if (d < 32 || d > 256 || d % 32 != 0) return PLX_ERR_UNSUPPORTED;
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+            (rho && !aligned(rho, 16)) || (lse && !aligned(lse, 4)))
+            return PLX_ERR_MISALIGNED;
+        const long long BH = static_cast<long long>(B) * H;
+        if (BH > 65535) return PLX_ERR_UNSUPPORTED;
+        plx::FwdF32Params p{q, k, v, rho, out, lse, N, scale};
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        const bool ok = rho ? dispatch_f32<true>(p, d, BH, s) : dispatch_f32<false>(p, d, BH, s);
+        if (!ok) return PLX_ERR_UNSUPPORTED;
+        return launch_status();
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+int plx_decode_num_splits(int B, int H, int d, int S_cap) {
+    try {
+        if (B < 1 || H < 1 || S_cap < 1 || (d != 64 && d != 128)) return 0;
+        const DeviceInfo* info = device_info();
+        if (!info) return 0;
+        return decode_splits(*info, static_cast<long long>(B) * H, d, S_cap);
+    } catch (...) {
+        return 0;
+    }
+}
+
+size_t plx_decode_workspace_size(int B, int H, int d, int S_cap, int num_splits) {
+    if (B < 1 || H < 1 || S_cap < 1 || (d != 64 && d != 128) || num_splits < 0 || num_splits > 1024) return 0;
+    const int splits = num_splits > 0 ? num_splits : plx_decode_num_splits(B, H, d, S_cap);
+    return decode_ws_bytes(static_cast<long long>(B) * H, d, splits);
+}
+
+plx_status plx_decode(const void* q, const void* rho, const void* k_cache, const void* v_cache,
+                      const int32_t* seqlens, void* out, float* lse, int B, int H, int d, int S_cap, float scale,
+                      int num_splits, void* workspace, size_t workspace_bytes, plx_dtype out_dtype, void* stream) {
+    try {
+        if (!q || !k_cache || !v_cache || !seqlens || !out) return PLX_ERR_INVALID_ARG;
+        if (B < 1 || H < 1 || S_cap < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
+        if (num_splits < 0 || num_splits > 1024) return PLX_ERR_INVALID_ARG;
+        if (out_dtype != PLX_BF16 && out_dtype != PLX_F32) return PLX_ERR_INVALID_ARG;
+        if (d != 64 && d != 128) return PLX_ERR_UNSUPPORTED;
+        if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+            (rho && !aligned(rho, 16)) || !aligned(seqlens, 4) || (lse && !aligned(lse, 4)) ||
+            (workspace && !aligned(workspace, 16)))
+            return PLX_ERR_MISALIGNED;
+        const long long BH = static_cast<long long>(B) * H;
+        if (BH > INT_MAX) return PLX_ERR_UNSUPPORTED;
+        const DeviceInfo* info = device_info();
+        if (!info) return PLX_ERR_CUDA;
+        const int splits = num_splits > 0 ? num_splits : decode_splits(*info, BH, d, S_cap);
+        const size_t need = decode_ws_bytes(BH, d, splits);
+        if (need > 0 && (!workspace || workspace_bytes < need)) return PLX_ERR_WORKSPACE;
+        plx::DecodeParams p;
+        p.q = static_cast<const __nv_bfloat16*>(q);
+        p.rho = static_cast<const __nv_bfloat16*>(rho);
+        p.kc = static_cast<const __nv_bfloat16*>(k_cache);
+        p.vc = static_cast<const __nv_bfloat16*>(v_cache);
+        p.seqlens = seqlens;
+        p.out = out;
+        p.lse = lse;
+        p.ws = static_cast<float*>(workspace);
+        p.H = H;
+        p.S_cap = S_cap;
+        p.splits = splits;
+        p.scale_log2 = scale * kLog2e;
+        p.out_f32 = out_dtype == PLX_F32;
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        if (d == 128) {
+            if (rho) launch_decode<128, true>(p, BH, s);
+            else launch_decode<128, false>(p, BH, s);
+        } else {
+            if (rho) launch_decode<64, true>(p, BH, s);
+            else launch_decode<64, false>(p, BH, s);
+        }
+        return launch_status();
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+plx_status plx_last_device_error(void* stream) {
+    try {
+        if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return PLX_ERR_CUDA;
+        unsigned int v = 0, zero = 0;
+        if (cudaMemcpyFromSymbol(&v, plx::g_plx_status, sizeof(v)) != cudaSuccess) return PLX_ERR_CUDA;
+        if (v && cudaMemcpyToSymbol(plx::g_plx_status, &zero, sizeof(zero)) != cudaSuccess) return PLX_ERR_CUDA;
+        if (v & plx::PLX_DEV_ERR_TIMEOUT) return PLX_ERR_TIMEOUT;
+        if (v & plx::PLX_DEV_ERR_SEQLEN) return PLX_ERR_INVALID_ARG;
+        if (v & plx::PLX_DEV_ERR_NONFINITE) return PLX_ERR_RANGE;
+        return PLX_OK;
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+}  // extern "C"

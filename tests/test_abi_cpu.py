@@ -1,0 +1,98 @@
+"""The C ABI library loads on a host without a GPU and exports every entry
+point include/plx.h declares; argument validation runs before any device
+access (CPU only, no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import parameterized_local_linear_02_b300 as plx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(plx_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("plx_fwd", "plx_fwd_f32", "plx_decode", "plx_decode_workspace_size",
+                 "plx_decode_num_splits", "plx_strerror", "plx_last_device_error", "plx_version"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = plx.library()
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libplx.so does not export {name}"
+
+
+def test_version_and_strerror():
+    assert plx.plx_version() >= 100
+    assert plx.plx_strerror(0) == "ok"
+    assert "misaligned" in plx.plx_strerror(3)
+    assert plx.plx_strerror(99) == "unknown status"
+
+
+P16 = ctypes.c_void_p(0x10000)        # aligned fake device address (never dereferenced)
+P_ODD = ctypes.c_void_p(0x10008)      # 8-byte aligned only
+
+
+def test_fwd_rejects_bad_arguments_before_launch():
+    lib = plx.library()
+    f = lib.plx_fwd
+    # null required pointer
+    assert f(None, P16, P16, None, P16, None, 1, 1, 8, 128, 0.1, 0, None) == 1
+    # non-positive sizes, bad scale, bad dtype
+    assert f(P16, P16, P16, None, P16, None, 0, 1, 8, 128, 0.1, 0, None) == 1
+    assert f(P16, P16, P16, None, P16, None, 1, 1, 0, 128, 0.1, 0, None) == 1
+    assert f(P16, P16, P16, None, P16, None, 1, 1, 8, 128, -1.0, 0, None) == 1
+    assert f(P16, P16, P16, None, P16, None, 1, 1, 8, 128, float("nan"), 0, None) == 1
+    assert f(P16, P16, P16, None, P16, None, 1, 1, 8, 128, 0.1, 7, None) == 1
+    # head dims without a kernel
+    assert f(P16, P16, P16, None, P16, None, 1, 1, 8, 96, 0.1, 0, None) == 2
+    assert f(P16, P16, P16, None, P16, None, 1, 1, 8, 256, 0.1, 0, None) == 2
+    # misaligned pointers
+    assert f(P_ODD, P16, P16, None, P16, None, 1, 1, 8, 128, 0.1, 0, None) == 3
+    assert f(P16, P16, P16, P_ODD, P16, None, 1, 1, 8, 128, 0.1, 0, None) == 3
+
+
+def test_fwd_f32_rejects_bad_arguments_before_launch():
+    f = plx.library().plx_fwd_f32
+    assert f(None, P16, P16, None, P16, None, 1, 1, 8, 64, 0.1, None) == 1
+    assert f(P16, P16, P16, None, P16, None, 1, 1, 8, 48, 0.1, None) == 2
+    assert f(P16, P16, P16, None, P16, None, 1, 1, 8, 288, 0.1, None) == 2
+    assert f(P16, P16, P16, None, P_ODD, None, 1, 1, 8, 64, 0.1, None) == 3
+
+
+def test_decode_rejects_bad_arguments_before_launch():
+    f = plx.library().plx_decode
+    args = lambda **kw: [kw.get("q", P16), kw.get("rho", None), kw.get("kc", P16), kw.get("vc", P16),
+                         kw.get("sl", P16), kw.get("out", P16), None, kw.get("B", 2), 16,
+                         kw.get("d", 128), kw.get("S", 64), 0.1, kw.get("ns", 1), None, 0,
+                         kw.get("dt", 0), None]
+    assert f(*args(q=None)) == 1
+    assert f(*args(sl=None)) == 1
+    assert f(*args(B=0)) == 1
+    assert f(*args(ns=-1)) == 1
+    assert f(*args(ns=5000)) == 1
+    assert f(*args(dt=3)) == 1
+    assert f(*args(d=96)) == 2
+    assert f(*args(kc=P_ODD)) == 3
+
+
+def test_decode_workspace_size_arithmetic():
+    ws = plx.library().plx_decode_workspace_size
+    assert ws(2, 16, 128, 4096, 1) == 0                         # one split: no partials
+    assert ws(2, 16, 128, 4096, 4) == 2 * 16 * 4 * (2 * 128 + 4) * 4
+    assert ws(3, 8, 64, 100, 7) == 3 * 8 * 7 * (2 * 64 + 4) * 4
+    assert ws(2, 16, 96, 4096, 4) == 0                          # unsupported head dim
+    assert ws(2, 16, 128, 4096, 2000) == 0                      # out of range
