@@ -54,8 +54,8 @@ struct FwdTcCfg {
     static constexpr int OFF_K = OFF_R + (PLX ? Q_BYTES : 0);
     static constexpr int OFF_V = OFF_K + NSTAGE * KV_BYTES;
     static constexpr int OFF_BAR = OFF_V + NSTAGE * KV_BYTES;
-    // barriers: q_full, q_empty, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], p_full[2], pv_done, drain
-    static constexpr int NBARS = 2 + 2 * NSTAGE + 2 + 2 + 2;
+    // barriers: q_full, q_empty, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], p_full[2], pv_done[2], drain
+    static constexpr int NBARS = 2 + 2 * NSTAGE + 2 + 2 + 2 + 1;
     static constexpr int SMEM_USED = OFF_BAR + NBARS * 8 + 16;
     static constexpr int SMEM = SMEM_USED + 1024;  // slack for 1024-byte alignment
     // TMEM columns
@@ -113,8 +113,8 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
     uint64_t* kv_empty = kv_full + NSTAGE;
     uint64_t* s_full = kv_empty + NSTAGE;
     uint64_t* p_full = s_full + 2;
-    uint64_t* pv_done = p_full + 2;
-    uint64_t* drain = pv_done + 1;
+    uint64_t* pv_done = p_full + 2;      // one per S/R buffer: PV of tiles g with g % 2 == b
+    uint64_t* drain = pv_done + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -135,8 +135,8 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
             mbar_init(&p_full[b], 128);
+            mbar_init(&pv_done[b], 1);
         }
-        mbar_init(pv_done, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -218,7 +218,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                     if (PLX) mma_ts(tmem + Cfg::TM_U, tR + kk * 8, bdesc, ID_PV, acc);
                 }
                 mma_commit(&kv_empty[stage]);
-                mma_commit(pv_done);
+                mma_commit(&pv_done[b]);
                 ++g_pv;
                 return true;
             };
@@ -265,7 +265,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-        int g_sr = 0, g_pv = 0;
+        int g_sr = 0;
         // all waits and exits are warp-uniform: the tcgen05 loads/stores below are .sync.aligned
         auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity));
@@ -376,21 +376,23 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                     }
                     fence_proxy_async_smem();
                 }
-                if (j >= 1) {
-                    // PV of the previous tile is complete: O and U are stable
-                    if (!wait_warp(pv_done, g_pv & 1)) { ok = false; break; }
-                    ++g_pv;
+                if (rescale_warp) {
+                    // O and U must hold the previous tile's PV before they are
+                    // rescaled.  Only that PV can still be in flight: the S/R MMA
+                    // of this tile completed after the PV two tiles back, and the
+                    // next PV needs this tile's P.  So the wait on the previous
+                    // tile's buffer barrier is unambiguous, and no other tile waits.
+                    const int gp = g_sr - 1;
+                    if (!wait_warp(&pv_done[gp & 1], (gp >> 1) & 1)) { ok = false; break; }
                     tc_fence_after();
-                    if (rescale_warp) {
 #pragma unroll 1
-                        for (int cb = 0; cb < (PLX ? 2 * D : D); cb += 32) {
-                            uint32_t o32[32];
-                            tmem_ld32x32b_x32(lane_addr + Cfg::TM_O + cb, o32);
+                    for (int cb = 0; cb < (PLX ? 2 * D : D); cb += 32) {
+                        uint32_t o32[32];
+                        tmem_ld32x32b_x32(lane_addr + Cfg::TM_O + cb, o32);
 #pragma unroll
-                            for (int cc = 0; cc < 32; ++cc)
-                                o32[cc] = __float_as_uint(__uint_as_float(o32[cc]) * alpha);
-                            tmem_st32x32b_x32(lane_addr + Cfg::TM_O + cb, o32);
-                        }
+                        for (int cc = 0; cc < 32; ++cc)
+                            o32[cc] = __float_as_uint(__uint_as_float(o32[cc]) * alpha);
+                        tmem_st32x32b_x32(lane_addr + Cfg::TM_O + cb, o32);
                     }
                 }
                 tmem_st_wait();
@@ -398,9 +400,13 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 mbar_arrive(&p_full[b]);
             }
             if (!ok) { fail(); break; }
-            // ---- epilogue: wait for the last PV, then o = (1 + c) vbar - u
-            if (!wait_warp(pv_done, g_pv & 1)) { fail(); break; }
-            ++g_pv;
+            // ---- epilogue: wait for the last PV (by the same argument the one
+            // before it on this buffer's barrier is complete), then
+            // o = (1 + c) vbar - u
+            {
+                const int gl = g_sr - 1;
+                if (!wait_warp(&pv_done[gl & 1], (gl >> 1) & 1)) { fail(); break; }
+            }
             tc_fence_after();
             const float inv_l = 1.f / l;
             const float cc_ = C * inv_l;
