@@ -68,14 +68,30 @@ def read_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
+def kernel_source_hash():
+    """sha256 over the CUDA sources (file name + bytes, sorted by name)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "parameterized_local_linear_02_b300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def read_traffic():
     """Per-launch DRAM bytes of the timed kernels from the committed ncu
-    summary (profiles/traffic.json), or None when absent/stale."""
+    summary (profiles/traffic.json).  An entry taken from other kernel
+    sources than the ones built now is stale and dropped, so the caller
+    reports null for it."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return {}
     with open(path) as f:
-        return json.load(f)
+        data = json.load(f)
+    now = kernel_source_hash()
+    return {k: v for k, v in data.items() if isinstance(v, dict) and v.get("source_sha256") == now}
 
 
 class ClockSampler:
