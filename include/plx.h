@@ -143,6 +143,40 @@ int plx_decode_num_splits(int B, int H, int d, int S_cap);
 size_t plx_decode_workspace_size(int B, int H, int d, int S_cap, int num_splits);
 
 /*
+ * plx_decode_noalloc -- plx_decode for callers that cannot allocate device
+ * memory: code running where cudaMalloc is off limits (inside a host
+ * callback, under an allocator that owns all device memory, or in a process
+ * that must not grow its footprint after start-up) cannot provide the
+ * workspace that plx_decode asks for.  This entry point takes no workspace
+ * and allocates nothing; the split partials go to a scratch array that the
+ * library holds in static device memory, PLX_DECODE_NOALLOC_SCRATCH_BYTES
+ * (4 MiB) on every GPU that loads the library, until the process exits.
+ * The paper has no counterpart: this is an interface convenience only.
+ *
+ * Arguments, layouts, numerics and results are those of plx_decode, which
+ * it calls with the scratch array as the workspace.
+ *   num_splits : 0 picks plx_decode's split count, lowered if needed to the
+ *                largest count whose partials fit in the scratch
+ *                (B * H * splits * (2 d + 4) * 4 bytes); with more than one
+ *                split that needs B * H <= 4032 at d = 128.  An explicit
+ *                count whose partials do not fit is rejected with
+ *                PLX_ERR_UNSUPPORTED before anything is launched.
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress, once per device, with that device current); make
+ * that first call before any stream capture.  Every call on a device shares
+ * the one array, so calls that may overlap on the GPU (on different streams,
+ * or from several host threads) race with each other: order them on one
+ * stream.  The array keeps the previous call's partials; nothing in it needs
+ * to start at zero because every split writes its whole partial before the
+ * combine reads it.
+ * Errors: as plx_decode, and PLX_ERR_UNSUPPORTED for the case above.
+ */
+#define PLX_DECODE_NOALLOC_SCRATCH_BYTES (4u << 20)
+plx_status plx_decode_noalloc(const void* q, const void* rho, const void* k_cache, const void* v_cache,
+                              const int32_t* seqlens, void* out, float* lse, int B, int H, int d, int S_cap,
+                              float scale, int num_splits, plx_dtype out_dtype, void* stream);
+
+/*
  * plx_last_device_error -- synchronises `stream`, then reads and clears the
  * current device's status word.  Returns PLX_ERR_TIMEOUT if a kernel gave up
  * a bounded wait, PLX_ERR_INVALID_ARG if a decode length exceeded S_cap,

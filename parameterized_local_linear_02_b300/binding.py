@@ -60,6 +60,8 @@ def library() -> ctypes.CDLL:
         lib.plx_decode_num_splits.argtypes = [i, i, i, i]
         lib.plx_decode_workspace_size.restype = sz
         lib.plx_decode_workspace_size.argtypes = [i, i, i, i, i]
+        lib.plx_decode_noalloc.restype = i
+        lib.plx_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         lib.plx_last_device_error.restype = i
         lib.plx_last_device_error.argtypes = [vp]
         _lib = lib
@@ -196,6 +198,38 @@ def plx_decode(q, rho, k_cache, v_cache, seqlens, *, scale=None, num_splits=0, w
                               _ptr(out), _ptr(lse), B, H, d, S_cap, scale, int(num_splits),
                               _ptr(workspace), ws_bytes, _out_code(out.dtype), _stream(dev))
     _check(st, "plx_decode")
+    return out, lse
+
+
+def plx_decode_noalloc(q, rho, k_cache, v_cache, seqlens, *, scale=None, num_splits=0, out=None, lse=None,
+                       out_dtype=torch.bfloat16, with_lse=True):
+    """plx_decode through the entry point that takes no workspace: the split
+    partials use the library's static device scratch, so the C call
+    allocates nothing (for callers that cannot allocate device memory).
+    Calls that overlap on the GPU share that scratch and race; this binding
+    issues them on the current stream.  ``out`` and ``lse`` are allocated
+    here with torch when not passed.  Returns ``(out, lse)``."""
+    B, H, S_cap, d = k_cache.shape
+    dev = k_cache.device
+    _need(q, "q", torch.bfloat16, (B, H, d), dev)
+    if rho is not None:
+        _need(rho, "rho", torch.bfloat16, (B, H, d), dev)
+    _need(k_cache, "k_cache", torch.bfloat16, (B, H, S_cap, d), dev)
+    _need(v_cache, "v_cache", torch.bfloat16, (B, H, S_cap, d), dev)
+    _need(seqlens, "seqlens", torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty((B, H, d), dtype=out_dtype, device=dev)
+    else:
+        _need(out, "out", out.dtype, (B, H, d), dev)
+    if lse is None and with_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, (B, H), dev)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().plx_decode_noalloc(_ptr(q), _ptr(rho), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
+                                      _ptr(out), _ptr(lse), B, H, d, S_cap, scale, int(num_splits),
+                                      _out_code(out.dtype), _stream(dev))
+    _check(st, "plx_decode_noalloc")
     return out, lse
 
 

@@ -185,6 +185,33 @@ void launch_decode(const plx::DecodeParams& p, long long BH, cudaStream_t s) {
     if (p.splits > 1) plx::plx_decode_combine_kernel<D, PLX><<<static_cast<unsigned>(BH), D, 0, s>>>(p);
 }
 
+// Split partials of plx_decode_noalloc: static device memory, one array per
+// GPU that loads the library, shared by every call on that GPU.
+constexpr size_t kNoallocScratchBytes = PLX_DECODE_NOALLOC_SCRATCH_BYTES;
+static_assert(kNoallocScratchBytes % 256 == 0, "scratch size");
+float* g_noalloc_scratch[kMaxDevices] = {};
+
+}  // namespace
+
+static __device__ __align__(256) float plx_decode_scratch[kNoallocScratchBytes / sizeof(float)];
+
+namespace {
+
+// Device address of plx_decode_scratch on the current device, looked up once
+// per device (host code cannot take the array's address directly: its name
+// there is a host-side stand-in).  nullptr on a CUDA error.
+float* noalloc_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_noalloc_scratch[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, plx_decode_scratch) != cudaSuccess || !ptr) return nullptr;
+        g_noalloc_scratch[dev] = static_cast<float*>(ptr);
+    }
+    return g_noalloc_scratch[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -311,6 +338,38 @@ plx_status plx_decode(const void* q, const void* rho, const void* k_cache, const
             else launch_decode<64, false>(p, BH, s);
         }
         return launch_status();
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+// plx_decode without a workspace argument.  The split partials live in a
+// static device array of PLX_DECODE_NOALLOC_SCRATCH_BYTES per GPU; its device
+// address is looked up once per device and handed to plx_decode as the
+// workspace, so this path allocates nothing.
+plx_status plx_decode_noalloc(const void* q, const void* rho, const void* k_cache, const void* v_cache,
+                              const int32_t* seqlens, void* out, float* lse, int B, int H, int d, int S_cap,
+                              float scale, int num_splits, plx_dtype out_dtype, void* stream) {
+    try {
+        if (B < 1 || H < 1 || S_cap < 1 || num_splits < 0 || num_splits > 1024) return PLX_ERR_INVALID_ARG;
+        if (d != 64 && d != 128) return PLX_ERR_UNSUPPORTED;
+        const long long BH = static_cast<long long>(B) * H;
+        if (BH > INT_MAX) return PLX_ERR_UNSUPPORTED;
+        const size_t per_split = static_cast<size_t>(BH) * (2 * d + 4) * sizeof(float);   // one split's partials
+        int splits = num_splits;
+        if (splits == 0) {
+            const DeviceInfo* info = device_info();
+            if (!info) return PLX_ERR_CUDA;
+            splits = decode_splits(*info, BH, d, S_cap);
+            const size_t fit = kNoallocScratchBytes / per_split;
+            if (splits > 1 && static_cast<size_t>(splits) > fit) splits = fit >= 2 ? static_cast<int>(fit) : 1;
+        } else if (decode_ws_bytes(BH, d, splits) > kNoallocScratchBytes) {
+            return PLX_ERR_UNSUPPORTED;
+        }
+        float* scratch = noalloc_scratch();
+        if (!scratch) return PLX_ERR_CUDA;
+        return plx_decode(q, rho, k_cache, v_cache, seqlens, out, lse, B, H, d, S_cap, scale, splits, scratch,
+                          kNoallocScratchBytes, out_dtype, stream);
     } catch (...) {
         return PLX_ERR_CUDA;
     }
