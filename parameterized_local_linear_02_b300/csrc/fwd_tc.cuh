@@ -19,20 +19,25 @@
 //   Sigma_KV rho = sum_j w_j (k_j.rho) v_j - vbar (kbar.rho)
 // (zhichai.net section 1.3; gist.science "Meccanismo Principale").
 //
-// Roles (192 threads, one CTA per SM, persistent over work items):
-//   warp 0     TMA producer: Q and rho once per item, K/V through an
-//              NSTAGE ring.
-//   warp 1     TMEM owner and MMA issuer (one thread).  Issue order per item
-//              SR_0, SR_1, PV_0, SR_2, PV_1, ... so the tensor pipe computes
-//              S/R of tile j+1 while the softmax works on tile j.
-//   warps 2-5  softmax + epilogue, thread r owns query row r of the tile
-//              (TMEM lane quadrant = warp % 4).
-// TMEM (512 columns): S0 | R0 | S1 | R1 (64 each) | O (D) | U (D).  P and PR
-// are written back as bf16 over the first 32 columns of their S/R buffer.
-// The running max is refreshed lazily: O, U, l, C are rescaled only when a
-// row max grows by more than 2^4, so P <= 16 and P o R stays inside the fp16
-// range for |rho.k| < 4094.  A non-finite output sets PLX_DEV_ERR_NONFINITE.
-// Work items (b*h, query tile) run longest-first in a snake order over CTAs.
+// Roles (448 threads, one CTA per SM, persistent over work items):
+//   warp 0       TMA producer (one lane): Q and rho once per item, K/V
+//                through an NSTAGE ring.
+//   warp 1       TMEM owner and MMA issuer.  The whole warp runs the issue
+//                loop and one elected lane issues each tcgen05 instruction,
+//                so descriptors stay in warp-uniform registers.  Issue order
+//                per item SR_0, SR_1, PV_0, SR_2, PV_1, ... so the tensor
+//                pipe computes S/R of tile j+1 while the softmax works on j.
+//   warps 2-9    softmax + epilogue, two warps per TMEM lane quadrant
+//                (quadrant = warp % 4, so both sit on the same scheduler):
+//                thread r of the pair owns query row r of the quadrant, the
+//                first warp keys 0-31 of each tile and the second keys 32-63.
+//                The pair agrees on the row max through shared memory and a
+//                per-quadrant mbarrier (bounded waits), once per tile; the
+//                exponentials are taken against the warp's own max while that
+//                handshake is in flight and rescaled by one factor after it.
+//   warps 10-13  V re-encode (bf16 -> fp16, in place) of each K/V stage as
+//                soon as it lands, off the softmax's critical path; the PV
+//                GEMMs wait for it.
 #pragma once
 #include "status.cuh"
 
@@ -44,7 +49,12 @@ struct FwdTcCfg {
     static constexpr int BN = 64;                  // keys per K/V tile
     static constexpr int NP = D / 64;              // 64-column panels (128 B rows)
     static constexpr int NSTAGE = (D == 128) ? 4 : 6;
-    static constexpr int THREADS = 192;
+    static constexpr int SM_WARPS = 8;             // softmax warps: 2 per TMEM lane quadrant
+    static constexpr int SM_THREADS = SM_WARPS * 32;
+    static constexpr int CV_WARPS = 4;             // V re-encode warps
+    static constexpr int CV_THREADS = CV_WARPS * 32;
+    static constexpr int THREADS = 64 + SM_THREADS + CV_THREADS;
+    static constexpr int HALF = BN / 2;            // keys of a tile per softmax warp
     static constexpr int Q_PANEL = BM * 128;       // bytes per Q/rho panel
     static constexpr int KV_PANEL = BN * 128;      // bytes per K/V panel
     static constexpr int Q_BYTES = NP * Q_PANEL;
@@ -53,9 +63,14 @@ struct FwdTcCfg {
     static constexpr int OFF_R = OFF_Q + Q_BYTES;
     static constexpr int OFF_K = OFF_R + (PLX ? Q_BYTES : 0);
     static constexpr int OFF_V = OFF_K + NSTAGE * KV_BYTES;
-    static constexpr int OFF_BAR = OFF_V + NSTAGE * KV_BYTES;
-    // barriers: q_full, q_empty, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], p_full[2], pv_done[2], drain
-    static constexpr int NBARS = 2 + 2 * NSTAGE + 2 + 2 + 2 + 1;
+    // pair exchange: row max per tile [2 tile parities][2 halves][BM] floats,
+    // (l, C) per item [2 item parities][2 halves][BM] float2
+    static constexpr int OFF_XMAX = OFF_V + NSTAGE * KV_BYTES;
+    static constexpr int OFF_XLC = OFF_XMAX + 2 * 2 * BM * 4;
+    static constexpr int OFF_BAR = OFF_XLC + 2 * 2 * BM * 8;
+    // barriers: q_full, q_empty, kv_full[NSTAGE], kv_empty[NSTAGE], v_ready[NSTAGE], s_full[2],
+    // p_full[2], pv_done[2], drain, pair[4]
+    static constexpr int NBARS = 2 + 3 * NSTAGE + 2 + 2 + 2 + 1 + 4;
     static constexpr int SMEM_USED = OFF_BAR + NBARS * 8 + 16;
     static constexpr int SMEM = SMEM_USED + 1024;  // slack for 1024-byte alignment
     // TMEM columns
@@ -63,7 +78,9 @@ struct FwdTcCfg {
     static constexpr uint32_t TM_COLS = 512;
     static constexpr float RESCALE_THRESH = 4.0f;  // log2 units: P <= 16
     static_assert(D == 64 || D == 128, "tcgen05 forward supports d in {64, 128}");
+    static_assert(HALF == 32, "one 32x32b.x32 TMEM load per warp and tile");
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert((KV_BYTES / 16) % CV_THREADS == 0, "V re-encode splits evenly over its threads");
 };
 
 struct FwdTcParams {
@@ -94,28 +111,32 @@ __device__ __forceinline__ int snake_item(int r, int c, int G) {
 }
 
 template <int D, bool PLX>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(FwdTcCfg<D, PLX>::THREADS, 1)
 plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapR,
                   const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                   const FwdTcParams p) {
     using Cfg = FwdTcCfg<D, PLX>;
-    constexpr int BM = Cfg::BM, BN = Cfg::BN, NP = Cfg::NP, NSTAGE = Cfg::NSTAGE;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, NP = Cfg::NP, NSTAGE = Cfg::NSTAGE, HALF = Cfg::HALF;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem + Cfg::OFF_Q;
     uint8_t* sR = smem + Cfg::OFF_R;
     uint8_t* sK = smem + Cfg::OFF_K;
     uint8_t* sV = smem + Cfg::OFF_V;
+    float* xmax = reinterpret_cast<float*>(smem + Cfg::OFF_XMAX);
+    float2* xlc = reinterpret_cast<float2*>(smem + Cfg::OFF_XLC);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     uint64_t* q_full = bars;
     uint64_t* q_empty = bars + 1;
     uint64_t* kv_full = bars + 2;
     uint64_t* kv_empty = kv_full + NSTAGE;
-    uint64_t* s_full = kv_empty + NSTAGE;
+    uint64_t* v_ready = kv_empty + NSTAGE;   // V of the stage re-encoded to fp16
+    uint64_t* s_full = v_ready + NSTAGE;
     uint64_t* p_full = s_full + 2;
     uint64_t* pv_done = p_full + 2;      // one per S/R buffer: PV of tiles g with g % 2 == b
     uint64_t* drain = pv_done + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* pair_bar = drain + 1;      // one per TMEM lane quadrant: the two softmax warps on it
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pair_bar + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -131,13 +152,15 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
+            mbar_init(&v_ready[s], Cfg::CV_WARPS);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], 128);
+            mbar_init(&p_full[b], Cfg::SM_WARPS);     // one elected arrival per softmax warp
             mbar_init(&pv_done[b], 1);
         }
         mbar_init(drain, 1);
+        for (int qd = 0; qd < 4; ++qd) mbar_init(&pair_bar[qd], 2);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&mapQ);
@@ -195,80 +218,101 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             if (items > 0 && !mbar_wait(q_full, (items - 1) & 1)) fail();
         }
     } else if (warp == 1) {
-        // ===================================================== MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t ID_S = idesc_bf16_f32(128, BN, false, false);
-            constexpr uint32_t ID_PV = idesc_f16_f32(128, D, false, true);
-            const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sR), sKa = smem_u32(sK), sVa = smem_u32(sV);
-            int items = 0, kv_it = 0, g_sr = 0, g_pv = 0;
-            bool ok = true;
-            int pv_stage = 0;
-            auto issue_pv = [&](int jj, int stage) -> bool {
-                const int b = g_pv & 1;
-                if (!mbar_wait(&p_full[b], (g_pv >> 1) & 1)) return false;
+        // ===================================================== MMA issuer (whole warp)
+        constexpr uint32_t ID_S = idesc_bf16_f32(128, BN, false, false);
+        constexpr uint32_t ID_PV = idesc_f16_f32(128, D, false, true);
+        const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sR), sKa = smem_u32(sK), sVa = smem_u32(sV);
+        auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+        };
+        int items = 0, kv_it = 0, g_sr = 0, g_pv = 0;
+        bool ok = true;
+        int pv_kv = 0;                        // ring index of the tile whose PV is next
+        auto issue_pv = [&](int jj, int kvi) -> bool {
+            const int b = g_pv & 1;
+            const int stage = kvi % NSTAGE;
+            if (!wait_warp(&p_full[b], (g_pv >> 1) & 1)) return false;
+            if (!wait_warp(&v_ready[stage], (kvi / NSTAGE) & 1)) return false;
+            tc_fence_after();
+            const uint32_t tS = tmem + (b ? Cfg::TM_S1 : Cfg::TM_S0);
+            const uint32_t tR = tmem + (b ? Cfg::TM_R1 : Cfg::TM_R0);
+            const uint32_t vbase = sVa + stage * Cfg::KV_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+                const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, Cfg::KV_PANEL, 1024);
+                const uint32_t acc = (jj > 0 || kk > 0) ? 1u : 0u;
+                mma_ts_warp(tmem + Cfg::TM_O, tS + kk * 8, bdesc, ID_PV, acc);
+                if (PLX) mma_ts_warp(tmem + Cfg::TM_U, tR + kk * 8, bdesc, ID_PV, acc);
+            }
+            mma_commit_warp(&kv_empty[stage]);
+            mma_commit_warp(&pv_done[b]);
+            ++g_pv;
+            return true;
+        };
+        for (int r = 0; ok; ++r) {
+            const int u = snake_item(r, c, G);
+            // one read of the flag for the whole warp: every lane takes the same branch
+            if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            int bh, qt;
+            item_coords(u, p.BH, p.n_qt, bh, qt);
+            const int q0 = qt * BM;
+            const int n_kv = (min(p.N, q0 + BM) + BN - 1) / BN;
+            if (!wait_warp(q_full, items & 1)) { fail(); break; }
+            tc_fence_after();
+            for (int j = 0; j < n_kv; ++j, ++kv_it, ++g_sr) {
+                const int s = kv_it % NSTAGE;
+                if (!wait_warp(&kv_full[s], (kv_it / NSTAGE) & 1)) { ok = false; break; }
                 tc_fence_after();
+                const int b = g_sr & 1;
                 const uint32_t tS = tmem + (b ? Cfg::TM_S1 : Cfg::TM_S0);
                 const uint32_t tR = tmem + (b ? Cfg::TM_R1 : Cfg::TM_R0);
-                const uint32_t vbase = sVa + stage * Cfg::KV_BYTES;
+                const uint32_t kbase = sKa + s * Cfg::KV_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, Cfg::KV_PANEL, 1024);
-                    const uint32_t acc = (jj > 0 || kk > 0) ? 1u : 0u;
-                    mma_ts(tmem + Cfg::TM_O, tS + kk * 8, bdesc, ID_PV, acc);
-                    if (PLX) mma_ts(tmem + Cfg::TM_U, tR + kk * 8, bdesc, ID_PV, acc);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * Cfg::Q_PANEL + (kk & 3) * 32;
+                    const uint32_t koff = (kk >> 2) * Cfg::KV_PANEL + (kk & 3) * 32;
+                    const uint64_t bdesc = sdesc_sw128(kbase + koff, 16, 1024);
+                    mma_ss_warp(tS, sdesc_sw128(sQa + off, 16, 1024), bdesc, ID_S, kk > 0);
+                    if (PLX) mma_ss_warp(tR, sdesc_sw128(sRa + off, 16, 1024), bdesc, ID_S, kk > 0);
                 }
-                mma_commit(&kv_empty[stage]);
-                mma_commit(&pv_done[b]);
-                ++g_pv;
-                return true;
-            };
-            for (int r = 0; ok; ++r) {
-                const int u = snake_item(r, c, G);
-                if (u >= p.n_items || *abort_flag) break;
-                int bh, qt;
-                item_coords(u, p.BH, p.n_qt, bh, qt);
-                const int q0 = qt * BM;
-                const int n_kv = (min(p.N, q0 + BM) + BN - 1) / BN;
-                if (!mbar_wait(q_full, items & 1)) { fail(); break; }
-                tc_fence_after();
-                for (int j = 0; j < n_kv; ++j, ++kv_it, ++g_sr) {
-                    const int s = kv_it % NSTAGE;
-                    if (!mbar_wait(&kv_full[s], (kv_it / NSTAGE) & 1)) { ok = false; break; }
-                    tc_fence_after();
-                    const int b = g_sr & 1;
-                    const uint32_t tS = tmem + (b ? Cfg::TM_S1 : Cfg::TM_S0);
-                    const uint32_t tR = tmem + (b ? Cfg::TM_R1 : Cfg::TM_R0);
-                    const uint32_t kbase = sKa + s * Cfg::KV_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * Cfg::Q_PANEL + (kk & 3) * 32;
-                        const uint32_t koff = (kk >> 2) * Cfg::KV_PANEL + (kk & 3) * 32;
-                        const uint64_t bdesc = sdesc_sw128(kbase + koff, 16, 1024);
-                        mma_ss(tS, sdesc_sw128(sQa + off, 16, 1024), bdesc, ID_S, kk > 0);
-                        if (PLX) mma_ss(tR, sdesc_sw128(sRa + off, 16, 1024), bdesc, ID_S, kk > 0);
-                    }
-                    mma_commit(&s_full[b]);
-                    if (j == n_kv - 1) mma_commit(q_empty);
-                    if (j >= 1 && !issue_pv(j - 1, pv_stage)) { ok = false; break; }
-                    pv_stage = s;
-                }
-                if (!ok) { fail(); break; }
-                if (!issue_pv(n_kv - 1, pv_stage)) { fail(); break; }
-                ++items;
+                mma_commit_warp(&s_full[b]);
+                if (j == n_kv - 1) mma_commit_warp(q_empty);
+                if (j >= 1 && !issue_pv(j - 1, pv_kv)) { ok = false; break; }
+                pv_kv = kv_it;
             }
-            // drain: every MMA issued by this thread has finished before TMEM is freed
-            mma_commit(drain);
-            if (!mbar_wait(drain, 0)) fail();
+            if (!ok) { fail(); break; }
+            if (!issue_pv(n_kv - 1, pv_kv)) { fail(); break; }
+            ++items;
         }
-    } else {
-        // ===================================================== softmax + epilogue (warps 2..5)
-        const int quad = warp & 3;
-        const int row = quad * 32 + lane;
+        // drain: every MMA issued by this warp has finished before TMEM is freed
+        mma_commit_warp(drain);
+        if (!wait_warp(drain, 0)) fail();
+    } else if (warp < 2 + Cfg::SM_WARPS) {
+        // ===================================================== softmax + epilogue (warps 2..9)
+        const int sw = warp - 2;                // 0..7
+        const int quad = warp & 3;              // TMEM lane quadrant this warp may access
+        const int half = sw >> 2;               // 0: keys 0..31 of each tile, 1: keys 32..63
+        const int row = quad * 32 + lane;       // query row within the item
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-        int g_sr = 0;
+        const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+        uint64_t* pbar = &pair_bar[quad];
+        int g_sr = 0, n_pair = 0, items = 0;
         // all waits and exits are warp-uniform: the tcgen05 loads/stores below are .sync.aligned
         auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+        };
+        // The two warps of a quadrant meet here: each has finished its TMEM loads
+        // and shared-memory writes before the other passes pair_wait.
+        auto pair_arrive = [&]() {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pbar);
+        };
+        auto pair_wait = [&]() -> bool {
+            const bool ok = wait_warp(pbar, n_pair & 1);
+            ++n_pair;
+            tc_fence_after();
+            return ok;
         };
         for (int r = 0;; ++r) {
             const int u = snake_item(r, c, G);
@@ -286,22 +330,47 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 tc_fence_after();
                 const uint32_t tS = lane_addr + (b ? Cfg::TM_S1 : Cfg::TM_S0);
                 const uint32_t tR = lane_addr + (b ? Cfg::TM_R1 : Cfg::TM_R0);
-                uint32_t sraw[64];
-                tmem_ld32x32b_x64(tS, sraw);
-                float sc[64];
+                uint32_t sraw[HALF], rraw[HALF];
+                tmem_ld32x32b_x32_nowait(tS + half * HALF, sraw);
+                if constexpr (PLX) tmem_ld32x32b_x32_nowait(tR + half * HALF, rraw);
+                tmem_ld_wait(sraw);
+                if constexpr (PLX) tmem_ld_wait(rraw);
+                float sc[HALF];
 #pragma unroll
-                for (int cc = 0; cc < 64; ++cc) sc[cc] = __uint_as_float(sraw[cc]);
+                for (int cc = 0; cc < HALF; ++cc) sc[cc] = __uint_as_float(sraw[cc]);
                 // causal mask on tiles that reach past the first row of the item
                 const bool diag = (j + 1) * BN - 1 > q0;
-                const int kbase = j * BN;
+                const int kbase = j * BN + half * HALF;
                 if (diag) {
 #pragma unroll
-                    for (int cc = 0; cc < 64; ++cc)
+                    for (int cc = 0; cc < HALF; ++cc)
                         if (kbase + cc > i) sc[cc] = -INFINITY;
                 }
-                float mt = sc[0];
+                // row max over this warp's 32 keys: a tree of three-input maxes
+                float mx[11];
 #pragma unroll
-                for (int cc = 1; cc < 64; ++cc) mt = fmaxf(mt, sc[cc]);
+                for (int t = 0; t < 10; ++t) mx[t] = fmax3(sc[3 * t], sc[3 * t + 1], sc[3 * t + 2]);
+                mx[10] = fmaxf(sc[30], sc[31]);
+                const float mloc = fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                               fmax3(mx[6], mx[7], mx[8])),
+                                         fmaxf(mx[9], mx[10]));
+                // The other warp of the quadrant holds the other 32 keys of the row.
+                // Publish this warp's max, take the exponentials against it while
+                // the handshake completes, then rescale them to the common max.
+                float* xm = xmax + (b * 2) * BM;
+                xm[half * BM + row] = mloc;
+                pair_arrive();
+                const float mloc2 = mloc == -INFINITY ? 0.f : mloc * p.scale_log2;   // log2 units
+                const float2 nl2 = make_float2(-mloc2, -mloc2);
+                float pe[HALF];
+#pragma unroll
+                for (int cc = 0; cc < HALF; cc += 2) {
+                    const float2 x = ffma2(make_float2(sc[cc], sc[cc + 1]), sl2, nl2);
+                    pe[cc] = fast_exp2(x.x);
+                    pe[cc + 1] = fast_exp2(x.y);
+                }
+                if (!pair_wait()) { ok = false; break; }
+                const float mt = fmaxf(xm[row], xm[BM + row]);   // same operands, same order in both warps
                 // scaled row max of this tile, log2 units (-inf when every key is masked)
                 const float mt2 = mt == -INFINITY ? -INFINITY : mt * p.scale_log2;
                 float alpha = 1.f;
@@ -319,62 +388,47 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                         C *= alpha;
                     }
                 }
+                // P = 2^(scale S - m) = 2^(scale S - mloc2) * 2^(mloc2 - m); the factor
+                // is at most 2^4 (m is within 2^4 of the row max), and 0 when every
+                // key of this warp is masked.
+                const float f = mloc == -INFINITY ? 0.f : fast_exp2(mloc2 - m);
+                const float2 f2 = make_float2(f, f);
+#pragma unroll
+                for (int cc = 0; cc < HALF; cc += 2) {
+                    const float2 y = fmul2(make_float2(pe[cc], pe[cc + 1]), f2);
+                    pe[cc] = y.x;
+                    pe[cc + 1] = y.y;
+                }
+                if (diag) {
+#pragma unroll
+                    for (int cc = 0; cc < HALF; ++cc)
+                        if (kbase + cc > i) pe[cc] = 0.f;       // also covers scale == 0
+                }
                 // P and PR go to the tensor cores as fp16; l and C are summed from
                 // the same rounded values, so o = (1 + C/l) O/l - U/l is exactly
                 // PLX for the rounded weights (they sum to one) and the rounding
                 // errors cancel the way the exact terms do.
-                const float neg_m = -m;
-                uint32_t pk[32];
-                float lsum = 0.f;
-                float pe[64];
+                uint32_t pk[HALF / 2];
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int cc = 0; cc < 64; ++cc) {
-                    pe[cc] = fast_exp2(fmaf(sc[cc], p.scale_log2, neg_m));
-                    if (diag && kbase + cc > i) pe[cc] = 0.f;     // also covers scale == 0
-                }
-#pragma unroll
-                for (int cc = 0; cc < 32; ++cc) {
+                for (int cc = 0; cc < HALF / 2; ++cc) {
                     pk[cc] = pack_f16x2(pe[2 * cc], pe[2 * cc + 1]);
-                    float lo, hi;
-                    unpack_f16x2(pk[cc], lo, hi);
-                    lsum += lo + hi;
+                    ls[cc & 3] = add_f16x2(ls[cc & 3], pk[cc]);
                 }
-                l += lsum;
-                tmem_st32x32b_x32(tS, pk);
+                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                tmem_st32x32b_x16(tS + half * (HALF / 2), pk);
                 if constexpr (PLX) {
-                    uint32_t rraw[64];
-                    tmem_ld32x32b_x64(tR, rraw);
-                    float csum = 0.f;
+                    float cs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) {
-                        const float a0 = pe[2 * cc] * __uint_as_float(rraw[2 * cc]);
-                        const float a1 = pe[2 * cc + 1] * __uint_as_float(rraw[2 * cc + 1]);
-                        pk[cc] = pack_f16x2(a0, a1);
-                        float lo, hi;
-                        unpack_f16x2(pk[cc], lo, hi);
-                        csum += lo + hi;
+                    for (int cc = 0; cc < HALF / 2; ++cc) {
+                        const float2 a = fmul2(make_float2(pe[2 * cc], pe[2 * cc + 1]),
+                                               make_float2(__uint_as_float(rraw[2 * cc]),
+                                                           __uint_as_float(rraw[2 * cc + 1])));
+                        pk[cc] = pack_f16x2(a.x, a.y);
+                        cs[cc & 3] = add_f16x2(cs[cc & 3], pk[cc]);
                     }
-                    C += csum;
-                    tmem_st32x32b_x32(tR, pk);
-                }
-                {
-                    // re-encode this tile's V (bf16 -> fp16) in place for the PV GEMMs;
-                    // element-wise, so the 128-byte swizzle is unchanged.  The wait on
-                    // the stage's load barrier (already complete: the S/R MMA of this
-                    // tile waited on it) orders the TMA writes before these reads.
-                    const int stage = g_sr % NSTAGE;
-                    if (!wait_warp(&kv_full[stage], (g_sr / NSTAGE) & 1)) { ok = false; break; }
-                    uint4* vt = reinterpret_cast<uint4*>(sV + stage * Cfg::KV_BYTES);
-#pragma unroll
-                    for (int k = 0; k < Cfg::KV_BYTES / 16 / 128; ++k) {
-                        uint4 w = vt[row + 128 * k];
-                        w.x = bf16x2_to_f16x2(w.x);
-                        w.y = bf16x2_to_f16x2(w.y);
-                        w.z = bf16x2_to_f16x2(w.z);
-                        w.w = bf16x2_to_f16x2(w.w);
-                        vt[row + 128 * k] = w;
-                    }
-                    fence_proxy_async_smem();
+                    C += (cs[0] + cs[1]) + (cs[2] + cs[3]);
+                    tmem_st32x32b_x16(tR + half * (HALF / 2), pk);
                 }
                 if (rescale_warp) {
                     // O and U must hold the previous tile's PV before they are
@@ -382,11 +436,14 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                     // of this tile completed after the PV two tiles back, and the
                     // next PV needs this tile's P.  So the wait on the previous
                     // tile's buffer barrier is unambiguous, and no other tile waits.
+                    // Both warps of the quadrant take the same decision; each
+                    // rescales half of the accumulator columns.
                     const int gp = g_sr - 1;
                     if (!wait_warp(&pv_done[gp & 1], (gp >> 1) & 1)) { ok = false; break; }
                     tc_fence_after();
+                    constexpr int ACC = PLX ? 2 * D : D;
 #pragma unroll 1
-                    for (int cb = 0; cb < (PLX ? 2 * D : D); cb += 32) {
+                    for (int cb = half * (ACC / 2); cb < (half + 1) * (ACC / 2); cb += 32) {
                         uint32_t o32[32];
                         tmem_ld32x32b_x32(lane_addr + Cfg::TM_O + cb, o32);
 #pragma unroll
@@ -397,36 +454,47 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&p_full[b]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[b]);
             }
             if (!ok) { fail(); break; }
             // ---- epilogue: wait for the last PV (by the same argument the one
-            // before it on this buffer's barrier is complete), then
-            // o = (1 + c) vbar - u
+            // before it on this buffer's barrier is complete), combine the two
+            // warps' partial sums, then o = (1 + c) vbar - u on this warp's half
+            // of the columns
             {
                 const int gl = g_sr - 1;
                 if (!wait_warp(&pv_done[gl & 1], (gl >> 1) & 1)) { fail(); break; }
             }
             tc_fence_after();
-            const float inv_l = 1.f / l;
-            const float cc_ = C * inv_l;
+            float2* xe = xlc + ((items & 1) * 2) * BM;
+            xe[half * BM + row] = make_float2(l, C);
+            pair_arrive();
+            if (!pair_wait()) { fail(); break; }
+            const float2 e0 = xe[row], e1 = xe[BM + row];
+            const float l_all = e0.x + e1.x, C_all = e0.y + e1.y;
+            const float inv_l = 1.f / l_all;
+            const float cc_ = C_all * inv_l;
             const bool store = i < p.N;
             bool nonfinite_ok = true;
             const size_t orow = (static_cast<size_t>(bh) * p.N + (store ? i : 0)) * D;
 #pragma unroll 1
-            for (int cb = 0; cb < D; cb += 32) {
+            for (int cb = half * (D / 2); cb < (half + 1) * (D / 2); cb += 32) {
                 uint32_t o32[32];
-                tmem_ld32x32b_x32(lane_addr + Cfg::TM_O + cb, o32);
                 float o[32];
                 if constexpr (PLX) {
                     uint32_t u32[32];
-                    tmem_ld32x32b_x32(lane_addr + Cfg::TM_U + cb, u32);
+                    tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_O + cb, o32);
+                    tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_U + cb, u32);
+                    tmem_ld_wait(o32);
+                    tmem_ld_wait(u32);
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) {
                         const float vbar = __uint_as_float(o32[cc]) * inv_l;
                         o[cc] = fmaf(cc_, vbar, vbar) - __uint_as_float(u32[cc]) * inv_l;
                     }
                 } else {
+                    tmem_ld32x32b_x32(lane_addr + Cfg::TM_O + cb, o32);
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) o[cc] = __uint_as_float(o32[cc]) * inv_l;
                 }
@@ -449,10 +517,49 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                     }
                 }
             }
-            if (store && p.lse) p.lse[static_cast<size_t>(bh) * p.N + i] = (m + __log2f(l)) * 0.69314718055994531f;
+            if (store && half == 0 && p.lse)
+                p.lse[static_cast<size_t>(bh) * p.N + i] = (m + __log2f(l_all)) * 0.69314718055994531f;
             if (__any_sync(0xffffffffu, store && !nonfinite_ok) && lane == 0)
                 atomicOr(&g_plx_status, PLX_DEV_ERR_NONFINITE);
+            ++items;
             tc_fence_before();
+        }
+    } else if (warp >= 2 + Cfg::SM_WARPS) {
+        // ===================================================== V re-encode (warps 10..13)
+        // Each stage's V goes bf16 -> fp16 in place for the PV GEMMs as soon as
+        // it lands; element-wise, so the 128-byte swizzle is unchanged.
+        const int t = (warp - 2 - Cfg::SM_WARPS) * 32 + lane;
+        auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+        };
+        int kv_it = 0;
+        for (int r = 0;; ++r) {
+            const int u = snake_item(r, c, G);
+            if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            int bh, qt;
+            item_coords(u, p.BH, p.n_qt, bh, qt);
+            const int q0 = qt * BM;
+            const int n_kv = (min(p.N, q0 + BM) + BN - 1) / BN;
+            bool ok = true;
+            for (int j = 0; j < n_kv; ++j, ++kv_it) {
+                const int stage = kv_it % NSTAGE;
+                if (!wait_warp(&kv_full[stage], (kv_it / NSTAGE) & 1)) { ok = false; break; }
+                uint4* vt = reinterpret_cast<uint4*>(sV + stage * Cfg::KV_BYTES);
+#pragma unroll
+                for (int k = 0; k < Cfg::KV_BYTES / 16 / Cfg::CV_THREADS; ++k) {
+                    uint4 w = vt[t + Cfg::CV_THREADS * k];
+                    w.x = bf16x2_to_f16x2(w.x);
+                    w.y = bf16x2_to_f16x2(w.y);
+                    w.z = bf16x2_to_f16x2(w.z);
+                    w.w = bf16x2_to_f16x2(w.w);
+                    vt[t + Cfg::CV_THREADS * k] = w;
+                }
+                // the re-encoded V is read next by the tensor cores (async proxy)
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&v_ready[stage]);
+            }
+            if (!ok) { fail(); break; }
         }
     }
 
