@@ -19,7 +19,7 @@
 //   Sigma_KV rho = sum_j w_j (k_j.rho) v_j - vbar (kbar.rho)
 // (zhichai.net section 1.3; gist.science "Meccanismo Principale").
 //
-// Roles (448 threads, one CTA per SM, persistent over work items):
+// Roles (384 threads, one CTA per SM, persistent over work items):
 //   warp 0       TMA producer (one lane): Q and rho once per item, K/V
 //                through an NSTAGE ring.
 //   warp 1       TMEM owner and MMA issuer.  The whole warp runs the issue
@@ -35,7 +35,7 @@
 //                per-quadrant mbarrier (bounded waits), once per tile; the
 //                exponentials are taken against the warp's own max while that
 //                handshake is in flight and rescaled by one factor after it.
-//   warps 10-13  V re-encode (bf16 -> fp16, in place) of each K/V stage as
+//   warps 10-11  V re-encode (bf16 -> fp16, in place) of each K/V stage as
 //                soon as it lands, off the softmax's critical path; the PV
 //                GEMMs wait for it.
 #pragma once
@@ -51,7 +51,7 @@ struct FwdTcCfg {
     static constexpr int NSTAGE = (D == 128) ? 4 : 6;
     static constexpr int SM_WARPS = 8;             // softmax warps: 2 per TMEM lane quadrant
     static constexpr int SM_THREADS = SM_WARPS * 32;
-    static constexpr int CV_WARPS = 4;             // V re-encode warps
+    static constexpr int CV_WARPS = 2;             // V re-encode warps (schedulers 2 and 3)
     static constexpr int CV_THREADS = CV_WARPS * 32;
     static constexpr int THREADS = 64 + SM_THREADS + CV_THREADS;
     static constexpr int HALF = BN / 2;            // keys of a tile per softmax warp
@@ -355,20 +355,26 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                                                fmax3(mx[6], mx[7], mx[8])),
                                          fmaxf(mx[9], mx[10]));
                 // The other warp of the quadrant holds the other 32 keys of the row.
-                // Publish this warp's max, take the exponentials against it while
-                // the handshake completes, then rescale them to the common max.
+                // Publish this warp's max.  While the handshake completes, take the
+                // exponentials against the running max m of the earlier tiles: in the
+                // usual case this tile raises no row max of the warp by more than
+                // 2^4, m stays, and they are final.  The first tile of an item, and a
+                // tile that does raise a row max that far (a warp-uniform decision,
+                // the same in both warps), take them again against the new m.
                 float* xm = xmax + (b * 2) * BM;
                 xm[half * BM + row] = mloc;
                 pair_arrive();
-                const float mloc2 = mloc == -INFINITY ? 0.f : mloc * p.scale_log2;   // log2 units
-                const float2 nl2 = make_float2(-mloc2, -mloc2);
                 float pe[HALF];
+                auto exps = [&](float mref) {
+                    const float2 nm2 = make_float2(-mref, -mref);
 #pragma unroll
-                for (int cc = 0; cc < HALF; cc += 2) {
-                    const float2 x = ffma2(make_float2(sc[cc], sc[cc + 1]), sl2, nl2);
-                    pe[cc] = fast_exp2(x.x);
-                    pe[cc + 1] = fast_exp2(x.y);
-                }
+                    for (int cc = 0; cc < HALF; cc += 2) {
+                        const float2 x = ffma2(make_float2(sc[cc], sc[cc + 1]), sl2, nm2);
+                        pe[cc] = fast_exp2(x.x);
+                        pe[cc + 1] = fast_exp2(x.y);
+                    }
+                };
+                if (j > 0) exps(m);
                 if (!pair_wait()) { ok = false; break; }
                 const float mt = fmaxf(xm[row], xm[BM + row]);   // same operands, same order in both warps
                 // scaled row max of this tile, log2 units (-inf when every key is masked)
@@ -388,17 +394,8 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                         C *= alpha;
                     }
                 }
-                // P = 2^(scale S - m) = 2^(scale S - mloc2) * 2^(mloc2 - m); the factor
-                // is at most 2^4 (m is within 2^4 of the row max), and 0 when every
-                // key of this warp is masked.
-                const float f = mloc == -INFINITY ? 0.f : fast_exp2(mloc2 - m);
-                const float2 f2 = make_float2(f, f);
-#pragma unroll
-                for (int cc = 0; cc < HALF; cc += 2) {
-                    const float2 y = fmul2(make_float2(pe[cc], pe[cc + 1]), f2);
-                    pe[cc] = y.x;
-                    pe[cc + 1] = y.y;
-                }
+                // P = 2^(scale S - m) <= 2^4: every score of the tile is within 2^4 of m
+                if (j == 0 || rescale_warp) exps(m);
                 if (diag) {
 #pragma unroll
                     for (int cc = 0; cc < HALF; ++cc)
@@ -525,7 +522,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             tc_fence_before();
         }
     } else if (warp >= 2 + Cfg::SM_WARPS) {
-        // ===================================================== V re-encode (warps 10..13)
+        // ===================================================== V re-encode (warps 10..11, on schedulers 2 and 3: scheduler 1 carries the MMA warp)
         // Each stage's V goes bf16 -> fp16 in place for the PV GEMMs as soon as
         // it lands; element-wise, so the 128-byte swizzle is unchanged.
         const int t = (warp - 2 - Cfg::SM_WARPS) * 32 + lane;

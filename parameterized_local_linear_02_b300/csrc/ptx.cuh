@@ -56,15 +56,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Wait until the phase with the given parity has completed.  Bounded: returns
-// false after PLX_WAIT_TIMEOUT_NS of wall time or PLX_WAIT_MAX_POLLS polls.
+// The same test, but the thread may be suspended (issuing nothing) until the
+// phase completes or about ns nanoseconds have passed.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+constexpr uint32_t PLX_WAIT_SUSPEND_NS = 1000;
+// Wait until the phase with the given parity has completed.  Waiting threads
+// are suspended between polls, so they leave the issue slots to the warps that
+// work.  Bounded: returns false after PLX_WAIT_TIMEOUT_NS of wall time or
+// PLX_WAIT_MAX_POLLS polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t polls = 0; polls < PLX_WAIT_MAX_POLLS; polls += 32) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+    for (uint32_t polls = 0; polls < PLX_WAIT_MAX_POLLS; ++polls) {
+        if (mbar_try_wait_suspend(bar, parity, PLX_WAIT_SUSPEND_NS)) return true;
         if (globaltimer_ns() - t0 > PLX_WAIT_TIMEOUT_NS) return false;
     }
     return false;
@@ -103,6 +117,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         "%5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+// Prefetch one 3-D tile of a tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
