@@ -409,6 +409,87 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def run_decode_sweep(args, world, rank, local):
+    """Decode over a sweep of batch x context (per-sequence lengths drawn
+    uniformly from [ctx/2, ctx]), H=16, d=128, bf16 cache; cells whose K+V
+    cache would exceed the 180 GB cap are listed as not run.  Each cell times
+    PLX and the rho = NULL (softmax attention) instantiation of the same
+    kernels; L2 is flushed (256 MiB write) before every timed launch, outside
+    the events.  Prints one JSON line."""
+    import torch
+    import parameterized_local_linear_02_b300 as plx
+    import plx_inputs
+
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    cfg = plx_inputs.CONFIGS["decode_sweep"]
+    H, d = cfg["H"], cfg["d"]
+    cap = 180e9
+    peaks = read_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    cells = []
+    sampler = ClockSampler(local)
+    sampler.start()
+    for B in cfg["batches"]:
+        for ctx in cfg["contexts"]:
+            cache_bytes = 2 * B * H * ctx * d * 2
+            cell = {"batch": B, "context": ctx, "cache_gb": cache_bytes / 1e9}
+            if cache_bytes > cap:
+                cell["status"] = "does not fit (180 GB cap)"
+                cells.append(cell)
+                continue
+            seed = cfg["seed"] + 100 * B + ctx // 1024
+            t = plx_inputs.decode_device(B, H, d, ctx, seed=seed, seqlens="ragged", rho_std=cfg["rho_std"],
+                                         device=dev)
+            splits = plx.plx_decode_num_splits(B, H, d, ctx)
+            ws = torch.empty(max(plx.plx_decode_workspace_size(B, H, d, ctx, splits), 16), dtype=torch.uint8,
+                             device=dev)
+            out = torch.empty((B, H, d), dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+            res = {}
+            for name, rho in (("plx", t["rho"]), ("sa", None)):
+                def call():
+                    plx.plx_decode(t["q"], rho, t["k_cache"], t["v_cache"], t["seqlens"], num_splits=splits,
+                                   workspace=ws, out=out, lse=lse)
+                for _ in range(3):
+                    call()
+                ms = []
+                for _ in range(args.sweep_iters):
+                    flush.zero_()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    call()
+                    b.record(stream)
+                    torch.cuda.synchronize()
+                    ms.append(a.elapsed_time(b))
+                med = float(np.median(ms))
+                nbytes = decode_bytes(t["seqlens_host"], H, d, plx=(rho is not None))
+                res[name] = {"ms": med, "gbs": nbytes / (med * 1e-3) / 1e9,
+                             "frac_hbm": nbytes / (med * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                             "tokens_per_s": B / (med * 1e-3)}
+            cell.update({"splits": splits, "kv_bytes": float(decode_bytes(t["seqlens_host"], H, d)),
+                         "mean_len": float(np.mean(t["seqlens_host"])), "plx": res["plx"], "sa": res["sa"]})
+            status = plx.plx_last_device_error()
+            cell["device_status"] = status
+            cells.append(cell)
+            print(f"# B={B:4d} ctx={ctx:6d} splits={splits:4d} PLX {res['plx']['ms']:.4f} ms "
+                  f"{res['plx']['gbs']:7.1f} GB/s  SA {res['sa']['ms']:.4f} ms {res['sa']['gbs']:7.1f} GB/s",
+                  file=sys.stderr, flush=True)
+            del t, ws, out, lse
+            torch.cuda.empty_cache()
+    clocks = sampler.stop()
+    line = {"metric": "PLX decode KV GB/s over batch x context (ragged lengths), 1 GPU", "unit": "GB/s",
+            "higher_is_better": True, "n_gpus": 1, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "decode_sweep", "H": H, "d": d, "lengths": "U[ctx/2, ctx] per sequence",
+                       "l2": "flushed (256 MiB write) before every launch", "iters_per_cell": args.sweep_iters},
+            "peak_hbm_gbs": peaks["hbm_gbs"], "cells": cells, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -421,6 +502,9 @@ def main():
                     help="run one kernel only (profiling of a single kernel)")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="decode batch (default: the decode workload's 64); smaller for profiling")
+    ap.add_argument("--decode-sweep", action="store_true",
+                    help="time plx_decode over the batch x context sweep instead of the step")
+    ap.add_argument("--sweep-iters", type=int, default=10)
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the softmax-attention comparison and the end-to-end leg")
     args = ap.parse_args()
@@ -428,6 +512,8 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.decode_sweep:
+        return run_decode_sweep(args, world, rank, local)
     return run_ours(args, world, rank, local)
 
 

@@ -161,15 +161,32 @@ bool dispatch_f32(const plx::FwdF32Params& p, int d, long long BH, cudaStream_t 
     }
 }
 
+// Split count for plx_decode: each (b, h) row's cache range is cut into s equal
+// parts, one thread block each.  The blocks run in waves of `slots` (SMs x
+// resident blocks per SM), so the estimated time is
+//   ceil(BH s / slots) x (tiles per block + fixed cost per block)
+// plus the combine pass when s > 1; pick the s that minimises it, with at least
+// 8 tiles (256 cache rows) per block.
 int decode_splits(const DeviceInfo& info, long long BH, int d, int S_cap) {
     constexpr int T = 32;
     const long long slots = static_cast<long long>(info.sm_count) * info.decode_blocks_per_sm[d == 128 ? 1 : 0];
-    const long long max_by_len = (static_cast<long long>(S_cap) + 8 * T - 1) / (8 * T);   // >= 8 tiles per split
-    long long want = (2 * slots + BH - 1) / BH;
-    if (want > max_by_len) want = max_by_len;
-    if (want > 1024) want = 1024;
-    if (want < 1) want = 1;
-    return static_cast<int>(want);
+    const double tiles = static_cast<double>((static_cast<long long>(S_cap) + T - 1) / T);
+    long long smax = (static_cast<long long>(S_cap) + 8 * T - 1) / (8 * T);
+    if (smax > 1024) smax = 1024;
+    if (smax < 1) smax = 1;
+    constexpr double kBlockCost = 2.0;     // per-block setup and merge, in tile units
+    constexpr double kCombineCost = 4.0;   // the combine launch, in tile units
+    int best = 1;
+    double best_t = 0.0;
+    for (long long s = 1; s <= smax; ++s) {
+        const double waves = static_cast<double>((BH * s + slots - 1) / slots);
+        const double t = waves * (tiles / static_cast<double>(s) + kBlockCost) + (s > 1 ? kCombineCost : 0.0);
+        if (s == 1 || t < best_t) {
+            best_t = t;
+            best = static_cast<int>(s);
+        }
+    }
+    return best;
 }
 
 size_t decode_ws_bytes(long long BH, int d, int splits) {

@@ -132,3 +132,37 @@ def test_decode_full_size_b64_h16_ctx4096_sampled():
     assert_bf16(np.stack(got), np.stack(ref), "decode full size")
     assert_lse(lg, lr, LSE_BF16, "decode full size lse")
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("B,ctx", [(8, 32768), (1, 131072), (256, 2048)])
+def test_decode_sweep_cells_sampled(B, ctx):
+    """Cells of the decode sweep at full size: lengths drawn from [ctx/2, ctx],
+    the split count the library picks for this GPU; sampled heads vs the
+    oracle, every output finite."""
+    import torch
+    import parameterized_local_linear_02_b300 as plx
+    cfg = plx_inputs.CONFIGS["decode_sweep"]
+    t = plx_inputs.decode_device(B, cfg["H"], cfg["d"], ctx, seed=cfg["seed"] + B, seqlens="ragged",
+                                 rho_std=cfg["rho_std"])
+    out, lse = plx.plx_decode(t["q"], t["rho"], t["k_cache"], t["v_cache"], t["seqlens"],
+                              out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert plx.plx_last_device_error() == 0
+    rng = np.random.default_rng(B + ctx)
+    heads = sorted({(0, 0), (B - 1, cfg["H"] - 1)} |
+                   {(int(b), int(h)) for b, h in zip(rng.integers(0, B, 4), rng.integers(0, cfg["H"], 4))})
+    got, ref, lg, lr = [], [], [], []
+    for b, h in heads:
+        L = int(t["seqlens_host"][b])
+        f = lambda name: t[name][b, h].float().cpu().numpy()
+        kc = t["k_cache"][b, h, :L].float().cpu().numpy()
+        vc = t["v_cache"][b, h, :L].float().cpu().numpy()
+        o, l = oracle.query("stream", f("q"), f("rho"), kc, vc, 1 / np.sqrt(cfg["d"]))
+        got.append(out[b, h].cpu().numpy())
+        ref.append(o)
+        lg.append(float(lse[b, h]))
+        lr.append(l)
+    assert_f32(np.stack(got), np.stack(ref), f"decode sweep B={B} ctx={ctx}")
+    assert_lse(lg, lr, LSE_BF16, f"decode sweep B={B} ctx={ctx} lse")
+    assert torch.isfinite(out).all()
