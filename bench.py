@@ -159,13 +159,28 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The largest x over all ranks (the slowest rank's time); x itself at N=1.
+    Uses a host tensor under the gloo backend and a device tensor under NCCL."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def weak_scaling_value(units_per_rank, ms_per_rank, world):
+    """Whole-job throughput when every rank processes its own fixed share:
+    all ranks' units divided by the slowest rank's time (units per second)."""
+    slowest = max_over_ranks(ms_per_rank, world)
+    return world * units_per_rank / (slowest * 1e-3)
+
+
+def rank_seed(seed, rank):
+    """Seed of a rank's shard: ranks draw distinct inputs of the same shape."""
+    return seed + 1000003 * rank
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -245,12 +260,13 @@ def run_ours(args, world, rank, local):
     Bd, Hd, S_cap = (args.decode_batch or dc["B"]), dc["H"], dc["S_cap"]
     x = None
     if do_pf:
-        x = plx_inputs.prefill(B, H, N, d, seed=pc["seed"], dtype="bf16", rho=pc["rho"], keys=pc["keys"])
+        x = plx_inputs.prefill(B, H, N, d, seed=rank_seed(pc["seed"], rank), dtype="bf16", rho=pc["rho"],
+                               keys=pc["keys"])
         t = x.device_tensors(dev)
         out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     if do_dec:
-        dd = plx_inputs.decode_device(Bd, Hd, dc["d"], S_cap, seed=dc["seed"], seqlens=dc["seqlens"],
+        dd = plx_inputs.decode_device(Bd, Hd, dc["d"], S_cap, seed=rank_seed(dc["seed"], rank), seqlens=dc["seqlens"],
                                       rho_std=dc["rho_std"], device=dev)
         dout = torch.empty((Bd, Hd, dc["d"]), dtype=torch.bfloat16, device=dev)
         dlse = torch.empty((Bd, Hd), dtype=torch.float32, device=dev)
