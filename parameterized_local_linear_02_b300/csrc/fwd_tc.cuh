@@ -33,11 +33,15 @@
 //                first warp keys 0-31 of each tile and the second keys 32-63.
 //                The pair agrees on the row max through shared memory and a
 //                per-quadrant mbarrier (bounded waits), once per tile; the
-//                exponentials are taken against the warp's own max while that
-//                handshake is in flight and rescaled by one factor after it.
+//                exponentials are taken against the running max while that
+//                handshake is in flight (again only if a row max jumps).
 //   warps 10-11  V re-encode (bf16 -> fp16, in place) of each K/V stage as
 //                soon as it lands, off the softmax's critical path; the PV
 //                GEMMs wait for it.
+// TMEM (512 columns): S0 | R0 | S1 | R1 (64 each) | O (D) | U (D).  Each softmax
+// warp writes its fp16 P (and PR) over the first half of the S (and R) columns
+// it read itself: keys [32h, 32h + 32) of the tile go to columns [32h, 32h + 16).
+// So no warp writes columns its partner reads.
 #pragma once
 #include "status.cuh"
 
@@ -241,8 +245,10 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             for (int kk = 0; kk < BN / 16; ++kk) {
                 const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, Cfg::KV_PANEL, 1024);
                 const uint32_t acc = (jj > 0 || kk > 0) ? 1u : 0u;
-                mma_ts_warp(tmem + Cfg::TM_O, tS + kk * 8, bdesc, ID_PV, acc);
-                if (PLX) mma_ts_warp(tmem + Cfg::TM_U, tR + kk * 8, bdesc, ID_PV, acc);
+                // keys [32h, 32h + 32) of the tile sit, as fp16 pairs, in columns [32h, 32h + 16)
+                const uint32_t acol = (kk >> 1) * 32 + (kk & 1) * 8;
+                mma_ts_warp(tmem + Cfg::TM_O, tS + acol, bdesc, ID_PV, acc);
+                if (PLX) mma_ts_warp(tmem + Cfg::TM_U, tR + acol, bdesc, ID_PV, acc);
             }
             mma_commit_warp(&kv_empty[stage]);
             mma_commit_warp(&pv_done[b]);
@@ -330,11 +336,11 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 tc_fence_after();
                 const uint32_t tS = lane_addr + (b ? Cfg::TM_S1 : Cfg::TM_S0);
                 const uint32_t tR = lane_addr + (b ? Cfg::TM_R1 : Cfg::TM_R0);
+                // S now; R is loaded after the max is published, so its TMEM
+                // latency hides under the exponentials
                 uint32_t sraw[HALF], rraw[HALF];
                 tmem_ld32x32b_x32_nowait(tS + half * HALF, sraw);
-                if constexpr (PLX) tmem_ld32x32b_x32_nowait(tR + half * HALF, rraw);
                 tmem_ld_wait(sraw);
-                if constexpr (PLX) tmem_ld_wait(rraw);
                 float sc[HALF];
 #pragma unroll
                 for (int cc = 0; cc < HALF; ++cc) sc[cc] = __uint_as_float(sraw[cc]);
@@ -364,6 +370,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 float* xm = xmax + (b * 2) * BM;
                 xm[half * BM + row] = mloc;
                 pair_arrive();
+                if constexpr (PLX) tmem_ld32x32b_x32_nowait(tR + half * HALF, rraw);
                 float pe[HALF];
                 auto exps = [&](float mref) {
                     const float2 nm2 = make_float2(-mref, -mref);
@@ -413,8 +420,9 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                     ls[cc & 3] = add_f16x2(ls[cc & 3], pk[cc]);
                 }
                 l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                tmem_st32x32b_x16(tS + half * (HALF / 2), pk);
+                tmem_st32x32b_x16(tS + half * HALF, pk);
                 if constexpr (PLX) {
+                    tmem_ld_wait(rraw);
                     float cs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int cc = 0; cc < HALF / 2; ++cc) {
@@ -425,7 +433,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                         cs[cc & 3] = add_f16x2(cs[cc & 3], pk[cc]);
                     }
                     C += (cs[0] + cs[1]) + (cs[2] + cs[3]);
-                    tmem_st32x32b_x16(tR + half * (HALF / 2), pk);
+                    tmem_st32x32b_x16(tR + half * HALF, pk);
                 }
                 if (rescale_warp) {
                     // O and U must hold the previous tile's PV before they are
