@@ -206,6 +206,27 @@ def oracle_prefill_sample(cfg, budget_s=12.0, x=None):
     return flops / dt / 1e12, dt, desc, threads
 
 
+def oracle_decode_sample(budget_s=5.0):
+    """Time the fp64 oracle (streaming form, all host threads) on host-drawn
+    (b, h) rows of the decode workload's shape (context 4096, d=128) until
+    ``budget_s`` has elapsed.  Returns (GB/s of K/V processed, seconds,
+    description, threads)."""
+    import oracle
+    import plx_inputs
+    dc = plx_inputs.CONFIGS[DECODE]
+    H, d, S = dc["H"], dc["d"], dc["S_cap"]
+    x = plx_inputs.decode(1, H, d, S, seed=dc["seed"], seqlens="full", rho_std=dc["rho_std"])
+    threads = oracle.n_threads()
+    done, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        oracle.decode("stream", x.q, x.rho, x.k_cache, x.v_cache, x.seqlens, x.scale, threads=threads)
+        done += H
+    dt = time.perf_counter() - t0
+    gbs = done * S * d * 2 * 2 / dt / 1e9
+    desc = f"{done} (b, h) rows of length {S} (one batch row of the decode workload, repeated), stream form"
+    return gbs, dt, desc, threads
+
+
 def run_reference(args, world, rank):
     import plx_inputs
     if rank != 0:
@@ -417,6 +438,10 @@ def run_ours(args, world, rank, local):
         v, dt, desc, threads = oracle_prefill_sample(pc, budget_s=args.cpu_budget, x=x)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                 "sample": desc, "seconds": dt}
+        if do_dec:
+            gbs, ddt, ddesc, dthreads = oracle_decode_sample(min(5.0, args.cpu_budget))
+            line["cpu_baseline"]["decode"] = {"value": gbs, "unit": "GB/s", "cores": dthreads, "kind": "oracle",
+                                              "sample": ddesc, "seconds": ddt}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
