@@ -531,6 +531,74 @@ def run_decode_sweep(args, world, rank, local):
     return 0
 
 
+def run_backward_bench(args, world, rank, local):
+    """plx_bwd_f32 on the prefill workload's shape (B=4, H=16, N=2048, d=128),
+    fp32 inputs (the bf16-rounded values widened), the forward's o and lse
+    from plx_fwd_f32 (not timed).  TFLOP/s counts 14 d flop per causal pair:
+    S, R and dO V^T recomputed once (3 x 2d), dq, drho (2 x 2d), dk (4d),
+    dv (2d).  The kernels run on the CUDA cores, so the roofline is the fp32
+    FMA rate: SMs x 128 lanes x 2 flop x the maximum SM clock.  Prints one
+    JSON line."""
+    import torch
+    import parameterized_local_linear_02_b300 as plx
+    import plx_inputs
+
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    pc = plx_inputs.CONFIGS[PREFILL]
+    B, H, N, d = pc["B"], pc["H"], pc["N"], pc["d"]
+    x = plx_inputs.prefill(B, H, N, d, seed=pc["seed"], dtype="bf16", rho=pc["rho"], keys=pc["keys"])
+    t = {n: torch.from_numpy(np.ascontiguousarray(getattr(x, n), np.float32)).to(dev) for n in ("q", "k", "v", "rho")}
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    dout = torch.randn((B, H, N, d), generator=g, device=dev)
+    out, lse = plx.plx_fwd_f32(t["q"], t["k"], t["v"], t["rho"], scale=x.scale)
+    grads = tuple(torch.empty((B, H, N, d), dtype=torch.float32, device=dev) for _ in range(4))
+    ws = torch.empty(plx.plx_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        plx.plx_bwd_f32(t["q"], t["k"], t["v"], t["rho"], out, lse, dout, scale=x.scale, workspace=ws, grads=grads)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    ms = []
+    for _ in range(max(3, args.steps)):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    clocks = sampler.stop()
+    med = float(np.median(ms))
+    pairs = B * H * N * (N + 1) / 2
+    flops = pairs * 14 * d
+    props = torch.cuda.get_device_properties(dev)
+    sm_max = clocks.get("sm_max_mhz") or 2032.0
+    peak = props.multi_processor_count * 128 * 2 * sm_max * 1e6 / 1e12
+    value = flops / (med * 1e-3) / 1e12
+    line = {"metric": "PLX backward (dq, dk, dv, drho) TFLOP/s, fp32 on the CUDA cores, 1 GPU", "value": value,
+            "unit": "TFLOP/s", "n_gpus": 1, "steps": len(ms), "warmup": max(3, args.warmup), "ms_per_step": med,
+            "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": PREFILL, "B": B, "H": H, "N": N, "d": d, "causal": True, "rho": "W_R x",
+                       "inputs": "fp32 (bf16-rounded values)", "l2": "flushed (256 MiB write) before every launch"},
+            "roofline": {"bound": "alu", "achieved": value, "peak": peak, "unit": "TFLOP/s", "frac": value / peak,
+                         "peak_source": f"{props.multi_processor_count} SMs x 128 fp32 FMA/clk x 2 x {sm_max:.0f} MHz",
+                         "flop_per_launch": flops, "flop_per_pair": 14 * d,
+                         "implementation_flop_per_pair": 28 * d},
+            "gpu_launches": 3 * len(ms), "clocks": clocks, "device_status": plx.plx_last_device_error()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -546,6 +614,8 @@ def main():
     ap.add_argument("--decode-sweep", action="store_true",
                     help="time plx_decode over the batch x context sweep instead of the step")
     ap.add_argument("--sweep-iters", type=int, default=10)
+    ap.add_argument("--backward", action="store_true",
+                    help="time plx_bwd_f32 on the prefill workload's shape instead of the step")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the softmax-attention comparison and the end-to-end leg")
     args = ap.parse_args()
@@ -555,6 +625,8 @@ def main():
         return run_reference(args, world, rank)
     if args.decode_sweep:
         return run_decode_sweep(args, world, rank, local)
+    if args.backward:
+        return run_backward_bench(args, world, rank, local)
     return run_ours(args, world, rank, local)
 
 

@@ -107,6 +107,38 @@ plx_status plx_fwd_f32(const float* q, const float* k, const float* v, const flo
                        float* lse, int B, int H, int N, int d, float scale, void* stream);
 
 /*
+ * plx_bwd_f32 -- gradients of the causal PLX forward with respect to q, k, v
+ * and rho, fp32 inputs and arithmetic on the CUDA cores.  The pages define
+ * the forward only (zhichai.net section 1.3; gist.science "Meccanismo
+ * Principale"); this is that forward differentiated.  With dO = dL/do,
+ * G_ij = dO_i.v_j, a_i = dO_i.vbar_i and w_ij = exp(scale q_i.k_j - lse_i):
+ *   dL/ds_ij = w_ij ((1 + c_i - r_ij) G_ij + a_i r_ij - D_i),  D_i = dO_i.o_i + c_i a_i
+ *   dL/dr_ij = w_ij (a_i - G_ij),  dv_j = sum_i w_ij (1 + c_i - r_ij) dO_i
+ *   dq = scale dS K,  drho = dR K,  dk = scale dS^T Q + dR^T rho.
+ *
+ *   q, k, v, rho : fp32 [B][H][N][d], 16-byte aligned; rho may be NULL
+ *                  (softmax attention; drho is then ignored).
+ *   out, lse     : the forward's o (fp32 [B][H][N][d]) and lse (fp32 [B][H][N],
+ *                  natural log), e.g. from plx_fwd_f32.
+ *   dout         : dL/do, fp32 [B][H][N][d].
+ *   dq, dk, dv, drho : fp32 [B][H][N][d] outputs (written, not accumulated).
+ *   workspace    : device scratch of plx_bwd_workspace_size(B, H, N, d) bytes,
+ *                  16-byte aligned; no initialisation needed.
+ *   B, H, N >= 1, B*H <= 65535; d a multiple of 32 in [32, 256].
+ * Three launches on `stream`: a per-row pre-pass, a pass over query rows
+ * (dq, drho) and a pass over key rows (dk, dv); no atomics, deterministic.
+ * Errors: PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_MISALIGNED,
+ * PLX_ERR_WORKSPACE, PLX_ERR_CUDA.
+ */
+plx_status plx_bwd_f32(const float* q, const float* k, const float* v, const float* rho, const float* out,
+                       const float* lse, const float* dout, float* dq, float* dk, float* dv, float* drho,
+                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale,
+                       void* stream);
+
+/* Workspace bytes plx_bwd_f32 needs: B*H*N*16 (0 for invalid sizes). */
+size_t plx_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
  * plx_decode -- one query token per sequence against a bf16 KV cache
  * (the streaming decode of gist.science "Algoritmo Consapevole
  * dell'Hardware").  The cache already holds the current token at position

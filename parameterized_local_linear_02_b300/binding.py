@@ -60,6 +60,10 @@ def library() -> ctypes.CDLL:
         lib.plx_decode_num_splits.argtypes = [i, i, i, i]
         lib.plx_decode_workspace_size.restype = sz
         lib.plx_decode_workspace_size.argtypes = [i, i, i, i, i]
+        lib.plx_bwd_f32.restype = i
+        lib.plx_bwd_f32.argtypes = [vp] * 12 + [sz, i, i, i, i, f, vp]
+        lib.plx_bwd_workspace_size.restype = sz
+        lib.plx_bwd_workspace_size.argtypes = [i, i, i, i]
         lib.plx_decode_noalloc.restype = i
         lib.plx_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         lib.plx_last_device_error.restype = i
@@ -157,6 +161,39 @@ def plx_fwd_f32(q, k, v, rho=None, *, scale=None, out=None, lse=None, with_lse=T
                                scale, _stream(dev))
     _check(st, "plx_fwd_f32")
     return out, lse
+
+
+def plx_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return library().plx_bwd_workspace_size(B, H, N, d)
+
+
+def plx_bwd_f32(q, k, v, rho, out, lse, dout, *, scale=None, workspace=None, grads=None):
+    """Gradients (dq, dk, dv, drho) of the causal PLX forward, fp32 on the
+    CUDA cores.  ``out`` and ``lse`` are the forward's outputs; ``rho=None``
+    gives the softmax-attention gradients (drho is then None).  ``grads`` may
+    pass preallocated (dq, dk, dv, drho) tensors."""
+    B, H, N, d = q.shape
+    dev = q.device
+    names = (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout))
+    for name, t in names + ((("rho", rho),) if rho is not None else ()):
+        _need(t, name, torch.float32, (B, H, N, d), dev)
+    _need(lse, "lse", torch.float32, (B, H, N), dev)
+    if grads is None:
+        grads = tuple(torch.empty((B, H, N, d), dtype=torch.float32, device=dev) for _ in range(3)) + (
+            torch.empty((B, H, N, d), dtype=torch.float32, device=dev) if rho is not None else None,)
+    dq, dk, dv, drho = grads
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)) + ((("drho", drho),) if rho is not None else ()):
+        _need(t, name, torch.float32, (B, H, N, d), dev)
+    need = plx_bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().plx_bwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(out), _ptr(lse), _ptr(dout),
+                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(drho), _ptr(workspace), ws_bytes,
+                               B, H, N, d, scale, _stream(dev))
+    _check(st, "plx_bwd_f32")
+    return dq, dk, dv, drho
 
 
 def plx_decode_num_splits(B: int, H: int, d: int, S_cap: int) -> int:

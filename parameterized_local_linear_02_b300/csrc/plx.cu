@@ -2,8 +2,8 @@
 //
 // One translation unit: argument validation, launch configuration, TMA
 // tensor-map encoding and the device status word, around the kernels in
-// fwd_tc.cuh (tcgen05 prefill), fwd_f32.cuh (fp32 prefill) and decode.cuh
-// (split-KV decode + combine).  Every entry point validates its arguments
+// fwd_tc.cuh (tcgen05 prefill), fwd_f32.cuh (fp32 prefill), bwd_f32.cuh (fp32
+// backward) and decode.cuh (split-KV decode + combine).  Every entry point validates its arguments
 // before launching anything and never lets a C++ exception escape.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "plx.h"
+#include "bwd_f32.cuh"
 #include "decode.cuh"
 #include "fwd_f32.cuh"
 #include "fwd_tc.cuh"
@@ -161,6 +162,29 @@ bool dispatch_f32(const plx::FwdF32Params& p, int d, long long BH, cudaStream_t 
     }
 }
 
+template <int DPL, bool PLX>
+void launch_bwd(const plx::BwdF32Params& p, long long BH, cudaStream_t s) {
+    dim3 grid((p.N + plx::BWD_ROWS_PER_BLOCK - 1) / plx::BWD_ROWS_PER_BLOCK, static_cast<unsigned>(BH));
+    plx::plx_bwd_pre_kernel<DPL, PLX><<<grid, plx::BWD_WARPS * 32, 0, s>>>(p);
+    plx::plx_bwd_dq_kernel<DPL, PLX><<<grid, plx::BWD_WARPS * 32, 0, s>>>(p);
+    plx::plx_bwd_dkv_kernel<DPL, PLX><<<grid, plx::BWD_WARPS * 32, 0, s>>>(p);
+}
+
+template <bool PLX>
+bool dispatch_bwd(const plx::BwdF32Params& p, int d, long long BH, cudaStream_t s) {
+    switch (d / 32) {
+        case 1: launch_bwd<1, PLX>(p, BH, s); return true;
+        case 2: launch_bwd<2, PLX>(p, BH, s); return true;
+        case 3: launch_bwd<3, PLX>(p, BH, s); return true;
+        case 4: launch_bwd<4, PLX>(p, BH, s); return true;
+        case 5: launch_bwd<5, PLX>(p, BH, s); return true;
+        case 6: launch_bwd<6, PLX>(p, BH, s); return true;
+        case 7: launch_bwd<7, PLX>(p, BH, s); return true;
+        case 8: launch_bwd<8, PLX>(p, BH, s); return true;
+        default: return false;
+    }
+}
+
 // Split count for plx_decode: each (b, h) row's cache range is cut into s equal
 // parts, one thread block each.  The blocks run in waves of `slots` (SMs x
 // resident blocks per SM), so the estimated time is
@@ -288,6 +312,38 @@ plx_status plx_fwd_f32(const float* q, const float* k, const float* v, const flo
         plx::FwdF32Params p{q, k, v, rho, out, lse, N, scale};
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         const bool ok = rho ? dispatch_f32<true>(p, d, BH, s) : dispatch_f32<false>(p, d, BH, s);
+        if (!ok) return PLX_ERR_UNSUPPORTED;
+        return launch_status();
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+size_t plx_bwd_workspace_size(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || d < 32 || d > 256 || d % 32 != 0) return 0;
+    return static_cast<size_t>(B) * H * N * 4 * sizeof(float);
+}
+
+plx_status plx_bwd_f32(const float* q, const float* k, const float* v, const float* rho, const float* out,
+                       const float* lse, const float* dout, float* dq, float* dk, float* dv, float* drho,
+                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale,
+                       void* stream) {
+    try {
+        if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || (rho && !drho))
+            return PLX_ERR_INVALID_ARG;
+        if (B < 1 || H < 1 || N < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
+        if (d < 32 || d > 256 || d % 32 != 0) return PLX_ERR_UNSUPPORTED;
+        const void* ptrs16[] = {q, k, v, out, dout, dq, dk, dv, workspace};
+        for (const void* ptr : ptrs16)
+            if (ptr && !aligned(ptr, 16)) return PLX_ERR_MISALIGNED;
+        if ((rho && (!aligned(rho, 16) || !aligned(drho, 16))) || !aligned(lse, 4)) return PLX_ERR_MISALIGNED;
+        const long long BH = static_cast<long long>(B) * H;
+        if (BH > 65535) return PLX_ERR_UNSUPPORTED;
+        const size_t need = plx_bwd_workspace_size(B, H, N, d);
+        if (!workspace || workspace_bytes < need) return PLX_ERR_WORKSPACE;
+        plx::BwdF32Params p{q, k, v, rho, out, lse, dout, dq, dk, dv, drho, static_cast<float*>(workspace), N, scale};
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        const bool ok = rho ? dispatch_bwd<true>(p, d, BH, s) : dispatch_bwd<false>(p, d, BH, s);
         if (!ok) return PLX_ERR_UNSUPPORTED;
         return launch_status();
     } catch (...) {

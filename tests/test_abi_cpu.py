@@ -96,3 +96,24 @@ def test_decode_workspace_size_arithmetic():
     assert ws(3, 8, 64, 100, 7) == 3 * 8 * 7 * (2 * 64 + 4) * 4
     assert ws(2, 16, 96, 4096, 4) == 0                          # unsupported head dim
     assert ws(2, 16, 128, 4096, 2000) == 0                      # out of range
+
+
+def test_bwd_rejects_bad_arguments_before_launch():
+    lib = plx.library()
+    P, WS = P16, ctypes.c_void_p(0x20000)
+    args = [P] * 11
+    # head dim not a multiple of 32
+    assert lib.plx_bwd_f32(*args, WS, 1 << 20, 1, 1, 64, 48, 0.1, None) == 2
+    # workspace missing or too small
+    assert lib.plx_bwd_f32(*args, None, 0, 1, 1, 64, 64, 0.1, None) == 6
+    need = lib.plx_bwd_workspace_size(2, 3, 64, 64)
+    assert need == 2 * 3 * 64 * 16
+    assert lib.plx_bwd_f32(*args, WS, need - 16, 2, 3, 64, 64, 0.1, None) == 6
+    # misaligned gradient output
+    bad = args[:]
+    bad[8] = P_ODD
+    assert lib.plx_bwd_f32(*bad, WS, need, 2, 3, 64, 64, 0.1, None) == 3
+    # rho given without drho
+    bad = args[:]
+    bad[10] = None
+    assert lib.plx_bwd_f32(*bad, WS, need, 2, 3, 64, 64, 0.1, None) == 1
