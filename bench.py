@@ -383,6 +383,20 @@ def run_ours(args, world, rank, local):
     if do_dec:
         line["config"].update({"decode_workload": DECODE, "decode_batch": Bd, "decode_splits": splits})
 
+    if extras and do_pf:
+        # the same launches back to back, no L2 flush between them (sustained clocks)
+        bb_n = max(20, args.steps)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(bb_n):
+            fwd()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        bb_ms = e0.elapsed_time(e1) / bb_n
+        line["roofline"]["back_to_back"] = {"launches": bb_n, "avg_launch_ms": bb_ms,
+                                            "achieved": prefill_flops(B, H, N, d) / bb_ms / 1e9,
+                                            "frac_of_sustained": prefill_flops(B, H, N, d) / bb_ms / 1e9
+                                            / peaks["bf16_tflops_sustained"]}
     if extras:
         sa = {}
         if do_pf:
