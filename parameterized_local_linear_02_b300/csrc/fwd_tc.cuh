@@ -20,13 +20,17 @@
 // (zhichai.net section 1.3; gist.science "Meccanismo Principale").
 //
 // Roles (384 threads, one CTA per SM, persistent over work items):
-//   warp 0       TMA producer (one lane): Q and rho once per item, K/V
-//                through an NSTAGE ring.
+//   warp 0       TMA producer (one lane): Q and rho once per item (with an L2
+//                prefetch of the next item's tile a few K/V tiles ahead), K
+//                through a KSTAGE ring and V through an NSTAGE ring.  A K slot
+//                frees when its S/R GEMMs finish, a V slot when its PV GEMMs do.
 //   warp 1       TMEM owner and MMA issuer.  The whole warp runs the issue
 //                loop and one elected lane issues each tcgen05 instruction,
-//                so descriptors stay in warp-uniform registers.  Issue order
-//                per item SR_0, SR_1, PV_0, SR_2, PV_1, ... so the tensor
-//                pipe computes S/R of tile j+1 while the softmax works on j.
+//                so descriptors stay in warp-uniform registers.  The issue
+//                order runs across items without a break: SR_{g+1} before PV_g
+//                for the CTA's global tile index g, so the tensor pipe computes
+//                S/R of the next tile (of this item or the next) while the
+//                softmax works on the current one.
 //   warps 2-9    softmax + epilogue, two warps per TMEM lane quadrant
 //                (quadrant = warp % 4, so both sit on the same scheduler):
 //                thread r of the pair owns query row r of the quadrant, the
@@ -35,7 +39,13 @@
 //                per-quadrant mbarrier (bounded waits), once per tile; the
 //                exponentials are taken against the running max while that
 //                handshake is in flight (again only if a row max jumps).
-//   warps 10-11  V re-encode (bf16 -> fp16, in place) of each K/V stage as
+//                An item's epilogue runs inside the first tile of the CTA's
+//                next item, after that tile's P/PR are stored and before they
+//                are released to the PV GEMM (whose first MMA overwrites O/U):
+//                the item's last PV has long finished by then, and (l, C)
+//                ride on that tile's max handshake.  The output goes through
+//                a swizzled shared-memory chunk per warp and a TMA store.
+//   warps 10-11  V re-encode (bf16 -> fp16, in place) of each V stage as
 //                soon as it lands, off the softmax's critical path; the PV
 //                GEMMs wait for it.
 // TMEM (512 columns): S0 | R0 | S1 | R1 (64 each) | O (D) | U (D).  Each softmax
@@ -52,7 +62,8 @@ struct FwdTcCfg {
     static constexpr int BM = 128;                 // query rows per item
     static constexpr int BN = 64;                  // keys per K/V tile
     static constexpr int NP = D / 64;              // 64-column panels (128 B rows)
-    static constexpr int NSTAGE = (D == 128) ? 4 : 6;
+    static constexpr int NSTAGE = (D == 128) ? 4 : 6;   // V ring
+    static constexpr int KSTAGE = NSTAGE - 1;      // K ring: its slots free one PV earlier
     static constexpr int SM_WARPS = 8;             // softmax warps: 2 per TMEM lane quadrant
     static constexpr int SM_THREADS = SM_WARPS * 32;
     static constexpr int CV_WARPS = 2;             // V re-encode warps (schedulers 2 and 3)
@@ -63,18 +74,23 @@ struct FwdTcCfg {
     static constexpr int KV_PANEL = BN * 128;      // bytes per K/V panel
     static constexpr int Q_BYTES = NP * Q_PANEL;
     static constexpr int KV_BYTES = NP * KV_PANEL;
+    // output staging: per softmax warp two chunks of 32 rows x 64 bytes (16 fp32 or
+    // 32 bf16 columns), 64-byte swizzle, written to global memory by TMA stores
+    static constexpr int STG_ROW = 64;
+    static constexpr int STG_BYTES = 32 * STG_ROW;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_R = OFF_Q + Q_BYTES;
     static constexpr int OFF_K = OFF_R + (PLX ? Q_BYTES : 0);
-    static constexpr int OFF_V = OFF_K + NSTAGE * KV_BYTES;
+    static constexpr int OFF_V = OFF_K + KSTAGE * KV_BYTES;
+    static constexpr int OFF_STG = OFF_V + NSTAGE * KV_BYTES;
     // pair exchange: row max per tile [2 tile parities][2 halves][BM] floats,
     // (l, C) per item [2 item parities][2 halves][BM] float2
-    static constexpr int OFF_XMAX = OFF_V + NSTAGE * KV_BYTES;
+    static constexpr int OFF_XMAX = OFF_STG + SM_WARPS * 2 * STG_BYTES;
     static constexpr int OFF_XLC = OFF_XMAX + 2 * 2 * BM * 4;
     static constexpr int OFF_BAR = OFF_XLC + 2 * 2 * BM * 8;
-    // barriers: q_full, q_empty, kv_full[NSTAGE], kv_empty[NSTAGE], v_ready[NSTAGE], s_full[2],
-    // p_full[2], pv_done[2], drain, pair[4]
-    static constexpr int NBARS = 2 + 3 * NSTAGE + 2 + 2 + 2 + 1 + 4;
+    // barriers: q_full, q_empty, k_full[KSTAGE], k_empty[KSTAGE], v_full[NSTAGE], v_empty[NSTAGE],
+    // v_ready[NSTAGE], s_full[2], p_full[2], pv_done[2], drain, pair[4]
+    static constexpr int NBARS = 2 + 2 * KSTAGE + 3 * NSTAGE + 2 + 2 + 2 + 1 + 4;
     static constexpr int SMEM_USED = OFF_BAR + NBARS * 8 + 16;
     static constexpr int SMEM = SMEM_USED + 1024;  // slack for 1024-byte alignment
     // TMEM columns
@@ -83,12 +99,12 @@ struct FwdTcCfg {
     static constexpr float RESCALE_THRESH = 4.0f;  // log2 units: P <= 16
     static_assert(D == 64 || D == 128, "tcgen05 forward supports d in {64, 128}");
     static_assert(HALF == 32, "one 32x32b.x32 TMEM load per warp and tile");
+    static_assert(OFF_STG % 1024 == 0, "staging chunks start on the swizzle period");
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert((KV_BYTES / 16) % CV_THREADS == 0, "V re-encode splits evenly over its threads");
 };
 
 struct FwdTcParams {
-    void* out;
     float* lse;
     int N;
     int BH;
@@ -118,9 +134,10 @@ template <int D, bool PLX>
 __global__ void __launch_bounds__(FwdTcCfg<D, PLX>::THREADS, 1)
 plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapR,
                   const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
-                  const FwdTcParams p) {
+                  const __grid_constant__ CUtensorMap mapO, const FwdTcParams p) {
     using Cfg = FwdTcCfg<D, PLX>;
-    constexpr int BM = Cfg::BM, BN = Cfg::BN, NP = Cfg::NP, NSTAGE = Cfg::NSTAGE, HALF = Cfg::HALF;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, NP = Cfg::NP, NSTAGE = Cfg::NSTAGE, KSTAGE = Cfg::KSTAGE,
+                  HALF = Cfg::HALF;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem + Cfg::OFF_Q;
@@ -132,9 +149,11 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     uint64_t* q_full = bars;
     uint64_t* q_empty = bars + 1;
-    uint64_t* kv_full = bars + 2;
-    uint64_t* kv_empty = kv_full + NSTAGE;
-    uint64_t* v_ready = kv_empty + NSTAGE;   // V of the stage re-encoded to fp16
+    uint64_t* k_full = bars + 2;
+    uint64_t* k_empty = k_full + KSTAGE;
+    uint64_t* v_full = k_empty + KSTAGE;
+    uint64_t* v_empty = v_full + NSTAGE;
+    uint64_t* v_ready = v_empty + NSTAGE;    // V of the stage re-encoded to fp16
     uint64_t* s_full = v_ready + NSTAGE;
     uint64_t* p_full = s_full + 2;
     uint64_t* pv_done = p_full + 2;      // one per S/R buffer: PV of tiles g with g % 2 == b
@@ -153,9 +172,13 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
+        for (int s = 0; s < KSTAGE; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
             mbar_init(&v_ready[s], Cfg::CV_WARPS);
         }
         for (int b = 0; b < 2; ++b) {
@@ -170,6 +193,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         tma_prefetch_desc(&mapQ);
         tma_prefetch_desc(&mapK);
         tma_prefetch_desc(&mapV);
+        tma_prefetch_desc(&mapO);
         if (PLX) tma_prefetch_desc(&mapR);
     }
     tc_fence_before();
@@ -185,41 +209,57 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
     if (warp == 0) {
         // ===================================================== TMA producer
         if (lane == 0) {
-            int items = 0, kv_it = 0;
-            for (int r = 0;; ++r) {
+            int nq = 0, nk = 0, nv = 0;           // loads issued: Q tiles, K tiles, V tiles
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
                 const int u = snake_item(r, c, G);
                 if (u >= p.n_items || *abort_flag) break;
                 int bh, qt;
                 item_coords(u, p.BH, p.n_qt, bh, qt);
                 const int q0 = qt * BM;
                 const int n_kv = (min(p.N, q0 + BM) + BN - 1) / BN;
-                if (items > 0 && !mbar_wait(q_empty, (items - 1) & 1)) { fail(); break; }
+                const int un = snake_item(r + 1, c, G);    // this CTA's next item
+                if (nq > 0 && !mbar_wait(q_empty, (nq - 1) & 1)) { ok = false; break; }
                 mbar_arrive_expect_tx(q_full, (PLX ? 2 : 1) * Cfg::Q_BYTES);
                 for (int pn = 0; pn < NP; ++pn) {
                     tma_load_3d(sQ + pn * Cfg::Q_PANEL, &mapQ, q_full, pn * 64, q0, bh);
                     if (PLX) tma_load_3d(sR + pn * Cfg::Q_PANEL, &mapR, q_full, pn * 64, q0, bh);
                 }
-                for (int j = 0; j < n_kv; ++j, ++kv_it) {
-                    const int s = kv_it % NSTAGE;
-                    if (kv_it >= NSTAGE && !mbar_wait(&kv_empty[s], ((kv_it / NSTAGE) - 1) & 1)) {
-                        fail();
-                        break;
+                ++nq;
+                for (int j = 0; j < n_kv; ++j) {
+                    // the next item's Q (and rho) tile is read once, from HBM: start it
+                    // into L2 a few tiles before its load
+                    if (j == max(0, n_kv - 3) && un < p.n_items) {
+                        int nbh, nqt;
+                        item_coords(un, p.BH, p.n_qt, nbh, nqt);
+                        for (int pn = 0; pn < NP; ++pn) {
+                            tma_prefetch_l2_3d(&mapQ, pn * 64, nqt * BM, nbh);
+                            if (PLX) tma_prefetch_l2_3d(&mapR, pn * 64, nqt * BM, nbh);
+                        }
                     }
-                    mbar_arrive_expect_tx(&kv_full[s], 2 * Cfg::KV_BYTES);
-                    for (int pn = 0; pn < NP; ++pn) {
-                        tma_load_3d(sK + s * Cfg::KV_BYTES + pn * Cfg::KV_PANEL, &mapK, &kv_full[s], pn * 64,
+                    const int ks = nk % KSTAGE;
+                    if (nk >= KSTAGE && !mbar_wait(&k_empty[ks], ((nk / KSTAGE) - 1) & 1)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&k_full[ks], Cfg::KV_BYTES);
+                    for (int pn = 0; pn < NP; ++pn)
+                        tma_load_3d(sK + ks * Cfg::KV_BYTES + pn * Cfg::KV_PANEL, &mapK, &k_full[ks], pn * 64,
                                     j * BN, bh);
-                        tma_load_3d(sV + s * Cfg::KV_BYTES + pn * Cfg::KV_PANEL, &mapV, &kv_full[s], pn * 64,
+                    ++nk;
+                    const int vs = nv % NSTAGE;
+                    if (nv >= NSTAGE && !mbar_wait(&v_empty[vs], ((nv / NSTAGE) - 1) & 1)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&v_full[vs], Cfg::KV_BYTES);
+                    for (int pn = 0; pn < NP; ++pn)
+                        tma_load_3d(sV + vs * Cfg::KV_BYTES + pn * Cfg::KV_PANEL, &mapV, &v_full[vs], pn * 64,
                                     j * BN, bh);
-                    }
+                    ++nv;
                 }
-                ++items;
-                if (*abort_flag) break;
             }
+            if (!ok) fail();
             // never leave with loads in flight into this CTA's shared memory
-            for (int i = max(0, kv_it - NSTAGE); i < kv_it; ++i)
-                if (!mbar_wait(&kv_full[i % NSTAGE], (i / NSTAGE) & 1)) fail();
-            if (items > 0 && !mbar_wait(q_full, (items - 1) & 1)) fail();
+            for (int i = max(0, nk - KSTAGE); i < nk; ++i)
+                if (!mbar_wait(&k_full[i % KSTAGE], (i / KSTAGE) & 1)) fail();
+            for (int i = max(0, nv - NSTAGE); i < nv; ++i)
+                if (!mbar_wait(&v_full[i % NSTAGE], (i / NSTAGE) & 1)) fail();
+            if (nq > 0 && !mbar_wait(q_full, (nq - 1) & 1)) fail();
         }
     } else if (warp == 1) {
         // ===================================================== MMA issuer (whole warp)
@@ -229,14 +269,12 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity));
         };
-        int items = 0, kv_it = 0, g_sr = 0, g_pv = 0;
-        bool ok = true;
-        int pv_kv = 0;                        // ring index of the tile whose PV is next
-        auto issue_pv = [&](int jj, int kvi) -> bool {
-            const int b = g_pv & 1;
-            const int stage = kvi % NSTAGE;
-            if (!wait_warp(&p_full[b], (g_pv >> 1) & 1)) return false;
-            if (!wait_warp(&v_ready[stage], (kvi / NSTAGE) & 1)) return false;
+        // PV GEMMs of global tile pg; the first tile of an item overwrites O and U
+        auto issue_pv = [&](int pg, bool first) -> bool {
+            const int b = pg & 1;
+            const int stage = pg % NSTAGE;
+            if (!wait_warp(&p_full[b], (pg >> 1) & 1)) return false;
+            if (!wait_warp(&v_ready[stage], (pg / NSTAGE) & 1)) return false;
             tc_fence_after();
             const uint32_t tS = tmem + (b ? Cfg::TM_S1 : Cfg::TM_S0);
             const uint32_t tR = tmem + (b ? Cfg::TM_R1 : Cfg::TM_R0);
@@ -244,17 +282,18 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
                 const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, Cfg::KV_PANEL, 1024);
-                const uint32_t acc = (jj > 0 || kk > 0) ? 1u : 0u;
+                const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
                 // keys [32h, 32h + 32) of the tile sit, as fp16 pairs, in columns [32h, 32h + 16)
                 const uint32_t acol = (kk >> 1) * 32 + (kk & 1) * 8;
                 mma_ts_warp(tmem + Cfg::TM_O, tS + acol, bdesc, ID_PV, acc);
                 if (PLX) mma_ts_warp(tmem + Cfg::TM_U, tR + acol, bdesc, ID_PV, acc);
             }
-            mma_commit_warp(&kv_empty[stage]);
+            mma_commit_warp(&v_empty[stage]);
             mma_commit_warp(&pv_done[b]);
-            ++g_pv;
             return true;
         };
+        int items = 0, g = 0;
+        bool ok = true, pend = false, pend_first = false;
         for (int r = 0; ok; ++r) {
             const int u = snake_item(r, c, G);
             // one read of the flag for the whole warp: every lane takes the same branch
@@ -263,16 +302,16 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             item_coords(u, p.BH, p.n_qt, bh, qt);
             const int q0 = qt * BM;
             const int n_kv = (min(p.N, q0 + BM) + BN - 1) / BN;
-            if (!wait_warp(q_full, items & 1)) { fail(); break; }
+            if (!wait_warp(q_full, items & 1)) { ok = false; break; }
             tc_fence_after();
-            for (int j = 0; j < n_kv; ++j, ++kv_it, ++g_sr) {
-                const int s = kv_it % NSTAGE;
-                if (!wait_warp(&kv_full[s], (kv_it / NSTAGE) & 1)) { ok = false; break; }
+            for (int j = 0; j < n_kv; ++j, ++g) {
+                const int ks = g % KSTAGE;
+                if (!wait_warp(&k_full[ks], (g / KSTAGE) & 1)) { ok = false; break; }
                 tc_fence_after();
-                const int b = g_sr & 1;
+                const int b = g & 1;
                 const uint32_t tS = tmem + (b ? Cfg::TM_S1 : Cfg::TM_S0);
                 const uint32_t tR = tmem + (b ? Cfg::TM_R1 : Cfg::TM_R0);
-                const uint32_t kbase = sKa + s * Cfg::KV_BYTES;
+                const uint32_t kbase = sKa + ks * Cfg::KV_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * Cfg::Q_PANEL + (kk & 3) * 32;
@@ -281,15 +320,18 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                     mma_ss_warp(tS, sdesc_sw128(sQa + off, 16, 1024), bdesc, ID_S, kk > 0);
                     if (PLX) mma_ss_warp(tR, sdesc_sw128(sRa + off, 16, 1024), bdesc, ID_S, kk > 0);
                 }
+                mma_commit_warp(&k_empty[ks]);
                 mma_commit_warp(&s_full[b]);
                 if (j == n_kv - 1) mma_commit_warp(q_empty);
-                if (j >= 1 && !issue_pv(j - 1, pv_kv)) { ok = false; break; }
-                pv_kv = kv_it;
+                // then the PV of the tile before this one, of this item or the previous one
+                if (pend && !issue_pv(g - 1, pend_first)) { ok = false; break; }
+                pend = true;
+                pend_first = j == 0;
             }
-            if (!ok) { fail(); break; }
-            if (!issue_pv(n_kv - 1, pv_kv)) { fail(); break; }
             ++items;
         }
+        if (ok && pend && !issue_pv(g - 1, pend_first)) ok = false;
+        if (!ok) fail();
         // drain: every MMA issued by this warp has finished before TMEM is freed
         mma_commit_warp(drain);
         if (!wait_warp(drain, 0)) fail();
@@ -302,7 +344,8 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
         uint64_t* pbar = &pair_bar[quad];
-        int g_sr = 0, n_pair = 0, items = 0;
+        uint8_t* stg = smem + Cfg::OFF_STG + sw * 2 * Cfg::STG_BYTES;
+        int g = 0, n_pair = 0, items = 0, n_chunk = 0;
         // all waits and exits are warp-uniform: the tcgen05 loads/stores below are .sync.aligned
         auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity));
@@ -320,7 +363,109 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             tc_fence_after();
             return ok;
         };
-        for (int r = 0;; ++r) {
+        // One chunk of this warp's 32 output rows (64 bytes each) through the
+        // staging buffers to global memory.  Two buffers alternate; before one
+        // is rewritten the TMA store that read it two chunks ago has finished
+        // reading.  Thread r writes row r with the 64-byte swizzle of the
+        // tensor map (16-byte unit c of row r at unit c ^ ((r >> 1) & 3)), so a
+        // quarter-warp's eight rows hit eight different bank groups.
+        auto stage_store = [&](const uint4 (&w)[4], int x, int y, int z) {
+            uint8_t* buf = stg + (n_chunk & 1) * Cfg::STG_BYTES;
+            if (lane == 0) bulk_wait_read_1();
+            __syncwarp();
+            const int swz = (lane >> 1) & 3;
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4)
+                *reinterpret_cast<uint4*>(buf + lane * Cfg::STG_ROW + ((u4 ^ swz) << 4)) = w[u4];
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(&mapO, buf, x, y, z);
+                bulk_commit_group();
+            }
+            ++n_chunk;
+        };
+        // Epilogue of item eu, whose last tile is global tile eg: wait for its
+        // last PV (the one before it on the same buffer barrier is complete,
+        // and the next cannot start before this warp releases its P), combine
+        // the two warps' (l, C) from xe, then o = (1 + c) vbar - u on this
+        // warp's rows and half of the columns.
+        auto epilogue = [&](int eu, int eg, float em, const float2* xe) -> bool {
+            if (!wait_warp(&pv_done[eg & 1], (eg >> 1) & 1)) return false;
+            tc_fence_after();
+            int ebh, eqt;
+            item_coords(eu, p.BH, p.n_qt, ebh, eqt);
+            const int eq0 = eqt * BM;
+            const int ei = eq0 + row;
+            const float2 e0 = xe[row], e1 = xe[BM + row];
+            const float l_all = e0.x + e1.x, C_all = e0.y + e1.y;
+            const float inv_l = 1.f / l_all;
+            const float cc_ = C_all * inv_l;
+            // rows past N are clipped by the TMA store; a warp whose 32 rows all
+            // are past N stores nothing
+            const bool rows_in = eq0 + quad * 32 < p.N;
+            const int y = eq0 + quad * 32;
+            bool fin = true;
+#pragma unroll 1
+            for (int cb = half * (D / 2); cb < (half + 1) * (D / 2); cb += 32) {
+                uint32_t o32[32];
+                float o[32];
+                if constexpr (PLX) {
+                    uint32_t u32[32];
+                    tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_O + cb, o32);
+                    tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_U + cb, u32);
+                    tmem_ld_wait(o32);
+                    tmem_ld_wait(u32);
+#pragma unroll
+                    for (int cc = 0; cc < 32; ++cc) {
+                        const float vbar = __uint_as_float(o32[cc]) * inv_l;
+                        o[cc] = fmaf(cc_, vbar, vbar) - __uint_as_float(u32[cc]) * inv_l;
+                    }
+                } else {
+                    tmem_ld32x32b_x32(lane_addr + Cfg::TM_O + cb, o32);
+#pragma unroll
+                    for (int cc = 0; cc < 32; ++cc) o[cc] = __uint_as_float(o32[cc]) * inv_l;
+                }
+#pragma unroll
+                for (int cc = 0; cc < 32; ++cc) fin &= isfinite(o[cc]);
+                if (!rows_in) continue;
+                if (p.out_f32) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint4 w[4];
+#pragma unroll
+                        for (int u4 = 0; u4 < 4; ++u4)
+                            w[u4] = make_uint4(__float_as_uint(o[16 * h + 4 * u4]),
+                                               __float_as_uint(o[16 * h + 4 * u4 + 1]),
+                                               __float_as_uint(o[16 * h + 4 * u4 + 2]),
+                                               __float_as_uint(o[16 * h + 4 * u4 + 3]));
+                        stage_store(w, cb + 16 * h, y, ebh);
+                    }
+                } else {
+                    uint4 w[4];
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4)
+                        w[u4] = make_uint4(pack_bf16x2(o[8 * u4], o[8 * u4 + 1]),
+                                           pack_bf16x2(o[8 * u4 + 2], o[8 * u4 + 3]),
+                                           pack_bf16x2(o[8 * u4 + 4], o[8 * u4 + 5]),
+                                           pack_bf16x2(o[8 * u4 + 6], o[8 * u4 + 7]));
+                    stage_store(w, cb, y, ebh);
+                }
+            }
+            const bool store = ei < p.N;
+            if (store && half == 0 && p.lse)
+                p.lse[static_cast<size_t>(ebh) * p.N + ei] = (em + __log2f(l_all)) * 0.69314718055994531f;
+            if (__any_sync(0xffffffffu, store && !fin) && lane == 0)
+                atomicOr(&g_plx_status, PLX_DEV_ERR_NONFINITE);
+            return true;
+        };
+        // the item whose epilogue is still to run: its index, last global tile,
+        // and this warp's running max and partial sums
+        bool prev = false;
+        int prev_u = 0, prev_g = 0;
+        float prev_m = 0.f, prev_l = 0.f, prev_C = 0.f;
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
             const int u = snake_item(r, c, G);
             if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
             int bh, qt;
@@ -329,10 +474,9 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             const int i = q0 + row;                 // this thread's query row
             const int n_kv = (min(p.N, q0 + BM) + BN - 1) / BN;
             float m = -INFINITY, l = 0.f, C = 0.f;
-            bool ok = true;
-            for (int j = 0; j < n_kv; ++j, ++g_sr) {
-                const int b = g_sr & 1;
-                if (!wait_warp(&s_full[b], (g_sr >> 1) & 1)) { ok = false; break; }
+            for (int j = 0; j < n_kv; ++j, ++g) {
+                const int b = g & 1;
+                if (!wait_warp(&s_full[b], (g >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t tS = lane_addr + (b ? Cfg::TM_S1 : Cfg::TM_S0);
                 const uint32_t tR = lane_addr + (b ? Cfg::TM_R1 : Cfg::TM_R0);
@@ -367,8 +511,12 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 // 2^4, m stays, and they are final.  The first tile of an item, and a
                 // tile that does raise a row max that far (a warp-uniform decision,
                 // the same in both warps), take them again against the new m.
+                // The first tile of an item also carries the previous item's (l, C).
                 float* xm = xmax + (b * 2) * BM;
                 xm[half * BM + row] = mloc;
+                const bool epi = j == 0 && prev;
+                float2* xe = xlc + (((items - 1) & 1) * 2) * BM;
+                if (epi) xe[half * BM + row] = make_float2(prev_l, prev_C);
                 pair_arrive();
                 if constexpr (PLX) tmem_ld32x32b_x32_nowait(tR + half * HALF, rraw);
                 float pe[HALF];
@@ -443,7 +591,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                     // tile's buffer barrier is unambiguous, and no other tile waits.
                     // Both warps of the quadrant take the same decision; each
                     // rescales half of the accumulator columns.
-                    const int gp = g_sr - 1;
+                    const int gp = g - 1;
                     if (!wait_warp(&pv_done[gp & 1], (gp >> 1) & 1)) { ok = false; break; }
                     tc_fence_after();
                     constexpr int ACC = PLX ? 2 * D : D;
@@ -457,78 +605,34 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                         tmem_st32x32b_x32(lane_addr + Cfg::TM_O + cb, o32);
                     }
                 }
+                // the previous item's O and U are read out before this tile's P is
+                // released: the first PV of this item overwrites them
+                if (epi && !epilogue(prev_u, prev_g, prev_m, xe)) { ok = false; break; }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[b]);
             }
-            if (!ok) { fail(); break; }
-            // ---- epilogue: wait for the last PV (by the same argument the one
-            // before it on this buffer's barrier is complete), combine the two
-            // warps' partial sums, then o = (1 + c) vbar - u on this warp's half
-            // of the columns
-            {
-                const int gl = g_sr - 1;
-                if (!wait_warp(&pv_done[gl & 1], (gl >> 1) & 1)) { fail(); break; }
-            }
-            tc_fence_after();
-            float2* xe = xlc + ((items & 1) * 2) * BM;
-            xe[half * BM + row] = make_float2(l, C);
-            pair_arrive();
-            if (!pair_wait()) { fail(); break; }
-            const float2 e0 = xe[row], e1 = xe[BM + row];
-            const float l_all = e0.x + e1.x, C_all = e0.y + e1.y;
-            const float inv_l = 1.f / l_all;
-            const float cc_ = C_all * inv_l;
-            const bool store = i < p.N;
-            bool nonfinite_ok = true;
-            const size_t orow = (static_cast<size_t>(bh) * p.N + (store ? i : 0)) * D;
-#pragma unroll 1
-            for (int cb = half * (D / 2); cb < (half + 1) * (D / 2); cb += 32) {
-                uint32_t o32[32];
-                float o[32];
-                if constexpr (PLX) {
-                    uint32_t u32[32];
-                    tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_O + cb, o32);
-                    tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_U + cb, u32);
-                    tmem_ld_wait(o32);
-                    tmem_ld_wait(u32);
-#pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) {
-                        const float vbar = __uint_as_float(o32[cc]) * inv_l;
-                        o[cc] = fmaf(cc_, vbar, vbar) - __uint_as_float(u32[cc]) * inv_l;
-                    }
-                } else {
-                    tmem_ld32x32b_x32(lane_addr + Cfg::TM_O + cb, o32);
-#pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) o[cc] = __uint_as_float(o32[cc]) * inv_l;
-                }
-#pragma unroll
-                for (int cc = 0; cc < 32; ++cc) nonfinite_ok &= isfinite(o[cc]);
-                if (store) {
-                    if (p.out_f32) {
-                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow + cb);
-#pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            dst[v4] = make_float4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
-                    } else {
-                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow + cb);
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            dst[v4] = make_uint4(pack_bf16x2(o[8 * v4], o[8 * v4 + 1]),
-                                                 pack_bf16x2(o[8 * v4 + 2], o[8 * v4 + 3]),
-                                                 pack_bf16x2(o[8 * v4 + 4], o[8 * v4 + 5]),
-                                                 pack_bf16x2(o[8 * v4 + 6], o[8 * v4 + 7]));
-                    }
-                }
-            }
-            if (store && half == 0 && p.lse)
-                p.lse[static_cast<size_t>(bh) * p.N + i] = (m + __log2f(l_all)) * 0.69314718055994531f;
-            if (__any_sync(0xffffffffu, store && !nonfinite_ok) && lane == 0)
-                atomicOr(&g_plx_status, PLX_DEV_ERR_NONFINITE);
+            if (!ok) break;
+            prev = true;
+            prev_u = u;
+            prev_g = g - 1;
+            prev_m = m;
+            prev_l = l;
+            prev_C = C;
             ++items;
-            tc_fence_before();
         }
+        // the CTA's last item: its own (l, C) handshake, then its epilogue
+        if (ok && prev) {
+            float2* xe = xlc + (((items - 1) & 1) * 2) * BM;
+            xe[half * BM + row] = make_float2(prev_l, prev_C);
+            pair_arrive();
+            ok = pair_wait() && epilogue(prev_u, prev_g, prev_m, xe);
+        }
+        if (!ok) fail();
+        // the output stores have finished (and stopped reading shared memory)
+        if (lane == 0) bulk_wait_all();
+        tc_fence_before();
     } else if (warp >= 2 + Cfg::SM_WARPS) {
         // ===================================================== V re-encode (warps 10..11, on schedulers 2 and 3: scheduler 1 carries the MMA warp)
         // Each stage's V goes bf16 -> fp16 in place for the PV GEMMs as soon as
@@ -537,18 +641,18 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity));
         };
-        int kv_it = 0;
-        for (int r = 0;; ++r) {
+        int g = 0;
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
             const int u = snake_item(r, c, G);
             if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
             int bh, qt;
             item_coords(u, p.BH, p.n_qt, bh, qt);
             const int q0 = qt * BM;
             const int n_kv = (min(p.N, q0 + BM) + BN - 1) / BN;
-            bool ok = true;
-            for (int j = 0; j < n_kv; ++j, ++kv_it) {
-                const int stage = kv_it % NSTAGE;
-                if (!wait_warp(&kv_full[stage], (kv_it / NSTAGE) & 1)) { ok = false; break; }
+            for (int j = 0; j < n_kv; ++j, ++g) {
+                const int stage = g % NSTAGE;
+                if (!wait_warp(&v_full[stage], (g / NSTAGE) & 1)) { ok = false; break; }
                 uint4* vt = reinterpret_cast<uint4*>(sV + stage * Cfg::KV_BYTES);
 #pragma unroll
                 for (int k = 0; k < Cfg::KV_BYTES / 16 / Cfg::CV_THREADS; ++k) {
@@ -564,8 +668,8 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&v_ready[stage]);
             }
-            if (!ok) { fail(); break; }
         }
+        if (!ok) fail();
     }
 
     tc_fence_before();

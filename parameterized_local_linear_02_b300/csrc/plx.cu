@@ -104,6 +104,21 @@ bool make_map(CUtensorMap* map, const void* base, int d, int N, long long BH, in
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D output tensor map over [BH][N][d] (fp32 or bf16) for the prefill's TMA
+// stores: a {64 bytes of columns, 32 rows, 1} box, 64B swizzle.
+bool make_out_map(CUtensorMap* map, void* base, int d, int N, long long BH, bool f32) {
+    auto enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t es = f32 ? 4 : 2;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(N) * d * es};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(64 / es), 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 plx_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
 }
@@ -118,9 +133,9 @@ plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void
     const long long n_qt = (N + Cfg::BM - 1) / Cfg::BM;
     const long long n_items = BH * n_qt;
     if (n_items > INT_MAX || BH > INT_MAX) return PLX_ERR_UNSUPPORTED;
-    CUtensorMap mq, mr, mk, mv;
+    CUtensorMap mq, mr, mk, mv, mo;
     if (!make_map(&mq, q, D, N, BH, Cfg::BM) || !make_map(&mk, k, D, N, BH, Cfg::BN) ||
-        !make_map(&mv, v, D, N, BH, Cfg::BN))
+        !make_map(&mv, v, D, N, BH, Cfg::BN) || !make_out_map(&mo, out, D, N, BH, out_dtype == PLX_F32))
         return PLX_ERR_CUDA;
     if (PLX) {
         if (!make_map(&mr, rho, D, N, BH, Cfg::BM)) return PLX_ERR_CUDA;
@@ -128,7 +143,6 @@ plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void
         mr = mq;
     }
     plx::FwdTcParams p;
-    p.out = out;
     p.lse = lse;
     p.N = N;
     p.BH = static_cast<int>(BH);
@@ -137,7 +151,7 @@ plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void
     p.scale_log2 = scale * kLog2e;
     p.out_f32 = out_dtype == PLX_F32;
     const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
-    plx::plx_fwd_tc_kernel<D, PLX><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, p);
+    plx::plx_fwd_tc_kernel<D, PLX><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
     return launch_status();
 }
 
