@@ -74,10 +74,11 @@ struct FwdTcCfg {
     static constexpr int KV_PANEL = BN * 128;      // bytes per K/V panel
     static constexpr int Q_BYTES = NP * Q_PANEL;
     static constexpr int KV_BYTES = NP * KV_PANEL;
-    // output staging: per softmax warp two chunks of 32 rows x 64 bytes (16 fp32 or
-    // 32 bf16 columns), 64-byte swizzle, written to global memory by TMA stores
-    static constexpr int STG_ROW = 64;
-    static constexpr int STG_BYTES = 32 * STG_ROW;
+    // output staging: one slot per softmax warp for a 32-column block of its 32
+    // rows (fp32: 128-byte rows, 128-byte swizzle; bf16: 64-byte rows, 64-byte
+    // swizzle), written to global memory by a TMA store
+    static constexpr int NCH = D / 64;             // 32-column output blocks per softmax warp
+    static constexpr int STG_SLOT_BYTES = 32 * 128;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_R = OFF_Q + Q_BYTES;
     static constexpr int OFF_K = OFF_R + (PLX ? Q_BYTES : 0);
@@ -85,7 +86,7 @@ struct FwdTcCfg {
     static constexpr int OFF_STG = OFF_V + NSTAGE * KV_BYTES;
     // pair exchange: row max per tile [2 tile parities][2 halves][BM] floats,
     // (l, C) per item [2 item parities][2 halves][BM] float2
-    static constexpr int OFF_XMAX = OFF_STG + SM_WARPS * 2 * STG_BYTES;
+    static constexpr int OFF_XMAX = OFF_STG + SM_WARPS * STG_SLOT_BYTES;
     static constexpr int OFF_XLC = OFF_XMAX + 2 * 2 * BM * 4;
     static constexpr int OFF_BAR = OFF_XLC + 2 * 2 * BM * 8;
     // barriers: q_full, q_empty, k_full[KSTAGE], k_empty[KSTAGE], v_full[NSTAGE], v_empty[NSTAGE],
@@ -344,8 +345,8 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
         uint64_t* pbar = &pair_bar[quad];
-        uint8_t* stg = smem + Cfg::OFF_STG + sw * 2 * Cfg::STG_BYTES;
-        int g = 0, n_pair = 0, items = 0, n_chunk = 0;
+        uint8_t* stg = smem + Cfg::OFF_STG + sw * Cfg::STG_SLOT_BYTES;
+        int g = 0, n_pair = 0, items = 0;
         // all waits and exits are warp-uniform: the tcgen05 loads/stores below are .sync.aligned
         auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity));
@@ -363,99 +364,85 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             tc_fence_after();
             return ok;
         };
-        // One chunk of this warp's 32 output rows (64 bytes each) through the
-        // staging buffers to global memory.  Two buffers alternate; before one
-        // is rewritten the TMA store that read it two chunks ago has finished
-        // reading.  Thread r writes row r with the 64-byte swizzle of the
-        // tensor map (16-byte unit c of row r at unit c ^ ((r >> 1) & 3)), so a
-        // quarter-warp's eight rows hit eight different bank groups.
-        auto stage_store = [&](const uint4 (&w)[4], int x, int y, int z) {
-            uint8_t* buf = stg + (n_chunk & 1) * Cfg::STG_BYTES;
-            if (lane == 0) bulk_wait_read_1();
-            __syncwarp();
-            const int swz = (lane >> 1) & 3;
-#pragma unroll
-            for (int u4 = 0; u4 < 4; ++u4)
-                *reinterpret_cast<uint4*>(buf + lane * Cfg::STG_ROW + ((u4 ^ swz) << 4)) = w[u4];
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_3d(&mapO, buf, x, y, z);
-                bulk_commit_group();
-            }
-            ++n_chunk;
-        };
         // Epilogue of item eu, whose last tile is global tile eg: wait for its
         // last PV (the one before it on the same buffer barrier is complete,
         // and the next cannot start before this warp releases its P), combine
         // the two warps' (l, C) from xe, then o = (1 + c) vbar - u on this
-        // warp's rows and half of the columns.
+        // warp's 32 rows and half of the columns, one 32-column block at a time
+        // through this warp's staging slot and a TMA store.  Thread r writes row
+        // r in the tensor map's swizzle (16-byte unit u of row r at u ^ (r & 7)
+        // for 128-byte fp32 rows, u ^ ((r >> 1) & 3) for 64-byte bf16 rows), so
+        // the eight rows of a quarter-warp hit eight different bank groups.
         auto epilogue = [&](int eu, int eg, float em, const float2* xe) -> bool {
             if (!wait_warp(&pv_done[eg & 1], (eg >> 1) & 1)) return false;
             tc_fence_after();
             int ebh, eqt;
             item_coords(eu, p.BH, p.n_qt, ebh, eqt);
             const int eq0 = eqt * BM;
-            const int ei = eq0 + row;
+            // rows past N are clipped by the TMA store; a warp whose 32 rows all
+            // are past N has nothing to write
+            if (eq0 + quad * 32 >= p.N) return true;
             const float2 e0 = xe[row], e1 = xe[BM + row];
             const float l_all = e0.x + e1.x, C_all = e0.y + e1.y;
             const float inv_l = 1.f / l_all;
             const float cc_ = C_all * inv_l;
-            // rows past N are clipped by the TMA store; a warp whose 32 rows all
-            // are past N stores nothing
-            const bool rows_in = eq0 + quad * 32 < p.N;
-            const int y = eq0 + quad * 32;
-            bool fin = true;
+            // 0 * o is NaN exactly when o is not finite: one running sum flags them all
+            float bad = 0.f;
 #pragma unroll 1
-            for (int cb = half * (D / 2); cb < (half + 1) * (D / 2); cb += 32) {
-                uint32_t o32[32];
+            for (int ch = 0; ch < Cfg::NCH; ++ch) {
+                const int col = half * (D / 2) + 32 * ch;
+                uint32_t ov[32];
                 float o[32];
                 if constexpr (PLX) {
-                    uint32_t u32[32];
-                    tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_O + cb, o32);
-                    tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_U + cb, u32);
-                    tmem_ld_wait(o32);
-                    tmem_ld_wait(u32);
+                    uint32_t uv[32];
+                    tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_O + col, ov);
+                    tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_U + col, uv);
+                    tmem_ld_wait(ov);
+                    tmem_ld_wait(uv);
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) {
-                        const float vbar = __uint_as_float(o32[cc]) * inv_l;
-                        o[cc] = fmaf(cc_, vbar, vbar) - __uint_as_float(u32[cc]) * inv_l;
+                        const float vbar = __uint_as_float(ov[cc]) * inv_l;
+                        o[cc] = fmaf(cc_, vbar, vbar) - __uint_as_float(uv[cc]) * inv_l;
                     }
                 } else {
-                    tmem_ld32x32b_x32(lane_addr + Cfg::TM_O + cb, o32);
+                    tmem_ld32x32b_x32(lane_addr + Cfg::TM_O + col, ov);
 #pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) o[cc] = __uint_as_float(o32[cc]) * inv_l;
+                    for (int cc = 0; cc < 32; ++cc) o[cc] = __uint_as_float(ov[cc]) * inv_l;
                 }
 #pragma unroll
-                for (int cc = 0; cc < 32; ++cc) fin &= isfinite(o[cc]);
-                if (!rows_in) continue;
+                for (int cc = 0; cc < 32; ++cc) bad = fmaf(o[cc], 0.f, bad);
+                // the slot is free once this warp's previous store has read it
+                if (lane == 0) bulk_wait_read<0>();
+                __syncwarp();
                 if (p.out_f32) {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint4 w[4];
-#pragma unroll
-                        for (int u4 = 0; u4 < 4; ++u4)
-                            w[u4] = make_uint4(__float_as_uint(o[16 * h + 4 * u4]),
-                                               __float_as_uint(o[16 * h + 4 * u4 + 1]),
-                                               __float_as_uint(o[16 * h + 4 * u4 + 2]),
-                                               __float_as_uint(o[16 * h + 4 * u4 + 3]));
-                        stage_store(w, cb + 16 * h, y, ebh);
-                    }
+                    for (int u4 = 0; u4 < 8; ++u4)
+                        *reinterpret_cast<uint4*>(stg + lane * 128 + ((u4 ^ (lane & 7)) << 4)) =
+                            make_uint4(__float_as_uint(o[4 * u4]), __float_as_uint(o[4 * u4 + 1]),
+                                       __float_as_uint(o[4 * u4 + 2]), __float_as_uint(o[4 * u4 + 3]));
                 } else {
-                    uint4 w[4];
+                    const int swz = (lane >> 1) & 3;
 #pragma unroll
                     for (int u4 = 0; u4 < 4; ++u4)
-                        w[u4] = make_uint4(pack_bf16x2(o[8 * u4], o[8 * u4 + 1]),
-                                           pack_bf16x2(o[8 * u4 + 2], o[8 * u4 + 3]),
-                                           pack_bf16x2(o[8 * u4 + 4], o[8 * u4 + 5]),
-                                           pack_bf16x2(o[8 * u4 + 6], o[8 * u4 + 7]));
-                    stage_store(w, cb, y, ebh);
+                        *reinterpret_cast<uint4*>(stg + lane * 64 + ((u4 ^ swz) << 4)) =
+                            make_uint4(pack_bf16x2(o[8 * u4], o[8 * u4 + 1]),
+                                       pack_bf16x2(o[8 * u4 + 2], o[8 * u4 + 3]),
+                                       pack_bf16x2(o[8 * u4 + 4], o[8 * u4 + 5]),
+                                       pack_bf16x2(o[8 * u4 + 6], o[8 * u4 + 7]));
+                }
+                // the staged rows are read next by the TMA engine (async proxy)
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&mapO, stg, col, eq0 + quad * 32, ebh);
+                    bulk_commit_group();
                 }
             }
+            const int ei = eq0 + row;
             const bool store = ei < p.N;
             if (store && half == 0 && p.lse)
                 p.lse[static_cast<size_t>(ebh) * p.N + ei] = (em + __log2f(l_all)) * 0.69314718055994531f;
-            if (__any_sync(0xffffffffu, store && !fin) && lane == 0)
+            if (__any_sync(0xffffffffu, store && !(bad == 0.f)) && lane == 0)
                 atomicOr(&g_plx_status, PLX_DEV_ERR_NONFINITE);
             return true;
         };

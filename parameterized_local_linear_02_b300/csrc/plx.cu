@@ -105,17 +105,19 @@ bool make_map(CUtensorMap* map, const void* base, int d, int N, long long BH, in
 }
 
 // 3-D output tensor map over [BH][N][d] (fp32 or bf16) for the prefill's TMA
-// stores: a {64 bytes of columns, 32 rows, 1} box, 64B swizzle.
+// stores: a {32 columns, 32 rows, 1} box, swizzled across its row (128 bytes
+// for fp32, 64 for bf16).
 bool make_out_map(CUtensorMap* map, void* base, int d, int N, long long BH, bool f32) {
     auto enc = encoder();
     if (!enc) return false;
     const cuuint64_t es = f32 ? 4 : 2;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(N) * d * es};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(64 / es), 32, 1};
+    cuuint32_t box[3] = {32, 32, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims,
-               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
