@@ -546,13 +546,15 @@ def run_decode_sweep(args, world, rank, local):
 
 
 def run_backward_bench(args, world, rank, local):
-    """plx_bwd_f32 on the prefill workload's shape (B=4, H=16, N=2048, d=128),
-    fp32 inputs (the bf16-rounded values widened), the forward's o and lse
-    from plx_fwd_f32 (not timed).  TFLOP/s counts 14 d flop per causal pair:
-    S, R and dO V^T recomputed once (3 x 2d), dq, drho (2 x 2d), dk (4d),
-    dv (2d).  The kernels run on the CUDA cores, so the roofline is the fp32
-    FMA rate: SMs x 128 lanes x 2 flop x the maximum SM clock.  Prints one
-    JSON line."""
+    """plx_bwd (tensor cores, bf16 inputs) on the prefill workload's shape
+    (B=4, H=16, N=2048, d=128), with the forward's o (fp32) and lse from
+    plx_fwd (not timed) and a seeded bf16 dL/do.  TFLOP/s counts 14 d flop per
+    causal pair: S, R and dO V^T once (3 x 2d), dq, drho (2 x 2d), dk (4d),
+    dv (2d); the implementation runs 30 d (two softmax-attention forwards for
+    vbar and kbar, 8d, and S, R, G recomputed in each of its two passes).  The
+    roofline is the measured dense bf16 tensor rate.  plx_bwd_f32 (CUDA
+    cores) is timed beside it on the same values widened to fp32.  Prints
+    one JSON line."""
     import torch
     import parameterized_local_linear_02_b300 as plx
     import plx_inputs
@@ -565,50 +567,76 @@ def run_backward_bench(args, world, rank, local):
     pc = plx_inputs.CONFIGS[PREFILL]
     B, H, N, d = pc["B"], pc["H"], pc["N"], pc["d"]
     x = plx_inputs.prefill(B, H, N, d, seed=pc["seed"], dtype="bf16", rho=pc["rho"], keys=pc["keys"])
-    t = {n: torch.from_numpy(np.ascontiguousarray(getattr(x, n), np.float32)).to(dev) for n in ("q", "k", "v", "rho")}
+    tb = x.device_tensors(dev)
     g = torch.Generator(device=dev)
     g.manual_seed(11)
-    dout = torch.randn((B, H, N, d), generator=g, device=dev)
-    out, lse = plx.plx_fwd_f32(t["q"], t["k"], t["v"], t["rho"], scale=x.scale)
+    dout = torch.randn((B, H, N, d), generator=g, device=dev).to(torch.bfloat16)
+    out, lse = plx.plx_fwd(tb["q"], tb["k"], tb["v"], tb["rho"], scale=x.scale, out_dtype=torch.float32)
     grads = tuple(torch.empty((B, H, N, d), dtype=torch.float32, device=dev) for _ in range(4))
-    ws = torch.empty(plx.plx_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    ws = torch.empty(plx.plx_bwd_bf16_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    def call():
-        plx.plx_bwd_f32(t["q"], t["k"], t["v"], t["rho"], out, lse, dout, scale=x.scale, workspace=ws, grads=grads)
+    def timed(fn, steps, warmup):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        return float(np.median(ms)), len(ms)
 
+    def call():
+        plx.plx_bwd(tb["q"], tb["k"], tb["v"], tb["rho"], out, lse, dout, scale=x.scale, workspace=ws, grads=grads)
+
+    sampler = ClockSampler(local)
     for _ in range(max(3, args.warmup)):
         call()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local)
     sampler.start()
-    ms = []
-    for _ in range(max(3, args.steps)):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        call()
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms.append(a.elapsed_time(b))
+    med, nsteps = timed(call, max(3, args.steps), 0)
     clocks = sampler.stop()
-    med = float(np.median(ms))
+    # the pre-pass's softmax-attention forward, alone, for the breakdown
+    sa_ms, _ = timed(lambda: plx.plx_fwd(tb["q"], tb["k"], tb["v"], None, scale=x.scale, out_dtype=torch.float32,
+                                         with_lse=False), 10, 3)
+    # the fp32 path on the same values
+    t32 = {n: tb[n].float() for n in ("q", "k", "v", "rho")}
+    out32, lse32 = plx.plx_fwd_f32(t32["q"], t32["k"], t32["v"], t32["rho"], scale=x.scale)
+    ws32 = torch.empty(plx.plx_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    dout32 = dout.float()
+    f32_ms, _ = timed(lambda: plx.plx_bwd_f32(t32["q"], t32["k"], t32["v"], t32["rho"], out32, lse32, dout32,
+                                              scale=x.scale, workspace=ws32, grads=grads), 3, 1)
     pairs = B * H * N * (N + 1) / 2
     flops = pairs * 14 * d
+    value = flops / (med * 1e-3) / 1e12
+    peaks = read_peaks()
+    peak = peaks["bf16_tflops"]
+    peak_s = peaks["bf16_tflops_sustained"]
     props = torch.cuda.get_device_properties(dev)
     sm_max = clocks.get("sm_max_mhz") or 2032.0
-    peak = props.multi_processor_count * 128 * 2 * sm_max * 1e6 / 1e12
-    value = flops / (med * 1e-3) / 1e12
-    line = {"metric": "PLX backward (dq, dk, dv, drho) TFLOP/s, fp32 on the CUDA cores, 1 GPU", "value": value,
-            "unit": "TFLOP/s", "n_gpus": 1, "steps": len(ms), "warmup": max(3, args.warmup), "ms_per_step": med,
-            "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+    alu_peak = props.multi_processor_count * 128 * 2 * sm_max * 1e6 / 1e12
+    line = {"metric": "PLX backward (dq, dk, dv, drho) TFLOP/s, bf16 inputs on the tensor cores, 1 GPU",
+            "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": nsteps, "warmup": max(3, args.warmup),
+            "ms_per_step": med, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": PREFILL, "B": B, "H": H, "N": N, "d": d, "causal": True, "rho": "W_R x",
-                       "inputs": "fp32 (bf16-rounded values)", "l2": "flushed (256 MiB write) before every launch"},
-            "roofline": {"bound": "alu", "achieved": value, "peak": peak, "unit": "TFLOP/s", "frac": value / peak,
-                         "peak_source": f"{props.multi_processor_count} SMs x 128 fp32 FMA/clk x 2 x {sm_max:.0f} MHz",
-                         "flop_per_launch": flops, "flop_per_pair": 14 * d,
-                         "implementation_flop_per_pair": 28 * d},
-            "gpu_launches": 3 * len(ms), "clocks": clocks, "device_status": plx.plx_last_device_error()}
+                       "inputs": "bf16 q, k, v, rho, dout; fp32 o and lse from plx_fwd",
+                       "l2": "flushed (256 MiB write) before every launch"},
+            "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s", "frac": value / peak,
+                         "peak_source": f"{peaks['source']} bf16 dense (burst)",
+                         "frac_of_sustained": value / peak_s,
+                         "flop_per_launch": flops, "flop_per_pair": 14 * d, "implementation_flop_per_pair": 30 * d,
+                         "implementation_tflops": pairs * 30 * d / (med * 1e-3) / 1e12},
+            "breakdown_ms": {"softmax_attention_forward_each": sa_ms, "forwards_in_prepass": 2},
+            "f32_path": {"ms": f32_ms, "value": flops / (f32_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                         "roofline": {"bound": "alu", "peak": alu_peak,
+                                      "frac": flops / (f32_ms * 1e-3) / 1e12 / alu_peak}},
+            "speedup_over_f32_path": f32_ms / med,
+            "gpu_launches": 5 * nsteps, "clocks": clocks, "device_status": plx.plx_last_device_error()}
     print(json.dumps(line), flush=True)
     return 0
 

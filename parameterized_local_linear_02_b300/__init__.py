@@ -1,16 +1,17 @@
 """Parallax (PLX) parameterized local linear attention on B300 (sm_103a).
 
-The compute lives in ``libplx.so`` (hand-written CUDA: a tcgen05/TMEM
-prefill kernel, an fp32 prefill kernel and a split-KV decode kernel) behind
+The compute lives in ``libplx.so`` (hand-written CUDA: tcgen05/TMEM prefill
+and backward kernels, fp32 prefill and backward kernels and a split-KV decode
+kernel) behind
 the C ABI declared in ``include/plx.h``.  This package is a thin ctypes
 binding with the same entry-point names; torch provides device memory and
 streams only.  There is no CPU fallback: every call needs the CUDA library
 and a CUDA device, and fails loudly otherwise.
 """
-from .binding import (PlxError, plx_bwd_f32, plx_bwd_workspace_size, plx_decode, plx_decode_noalloc, plx_decode_num_splits, plx_decode_workspace_size,
+from .binding import (PlxError, plx_bwd, plx_bwd_bf16_workspace_size, plx_bwd_f32, plx_bwd_workspace_size, plx_decode, plx_decode_noalloc, plx_decode_num_splits, plx_decode_workspace_size,
                       plx_fwd, plx_fwd_f32, plx_last_device_error, plx_strerror, plx_version,
                       library, library_path)
 
-__all__ = ["PlxError", "plx_fwd", "plx_fwd_f32", "plx_bwd_f32", "plx_bwd_workspace_size", "plx_decode", "plx_decode_noalloc", "plx_decode_num_splits",
+__all__ = ["PlxError", "plx_fwd", "plx_fwd_f32", "plx_bwd", "plx_bwd_bf16_workspace_size", "plx_bwd_f32", "plx_bwd_workspace_size", "plx_decode", "plx_decode_noalloc", "plx_decode_num_splits",
            "plx_decode_workspace_size", "plx_last_device_error", "plx_strerror", "plx_version",
            "library", "library_path"]

@@ -2,8 +2,9 @@
 //
 // One translation unit: argument validation, launch configuration, TMA
 // tensor-map encoding and the device status word, around the kernels in
-// fwd_tc.cuh (tcgen05 prefill), fwd_f32.cuh (fp32 prefill), bwd_f32.cuh (fp32
-// backward) and decode.cuh (split-KV decode + combine).  Every entry point validates its arguments
+// fwd_tc.cuh (tcgen05 prefill), fwd_f32.cuh (fp32 prefill), bwd_tc.cuh (tcgen05
+// backward), bwd_f32.cuh (fp32 backward) and decode.cuh (split-KV decode +
+// combine).  Every entry point validates its arguments
 // before launching anything and never lets a C++ exception escape.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -18,9 +19,11 @@
 #include "decode.cuh"
 #include "fwd_f32.cuh"
 #include "fwd_tc.cuh"
+#include "bwd_tc.cuh"
 
 namespace {
 
+using plx::BwdTcCfg;
 using plx::DecodeCfg;
 using plx::FwdTcCfg;
 
@@ -58,6 +61,14 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, false>, FwdTcCfg<128, false>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, true>, FwdTcCfg<64, true>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, false>, FwdTcCfg<64, false>::SMEM);
+    e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, true, plx::BWD_DQ>, BwdTcCfg<128, true, plx::BWD_DQ>::SMEM);
+    e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, false, plx::BWD_DQ>, BwdTcCfg<128, false, plx::BWD_DQ>::SMEM);
+    e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, true, plx::BWD_DKV>, BwdTcCfg<128, true, plx::BWD_DKV>::SMEM);
+    e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, false, plx::BWD_DKV>, BwdTcCfg<128, false, plx::BWD_DKV>::SMEM);
+    e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, true, plx::BWD_DQ>, BwdTcCfg<64, true, plx::BWD_DQ>::SMEM);
+    e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, false, plx::BWD_DQ>, BwdTcCfg<64, false, plx::BWD_DQ>::SMEM);
+    e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, true, plx::BWD_DKV>, BwdTcCfg<64, true, plx::BWD_DKV>::SMEM);
+    e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, false, plx::BWD_DKV>, BwdTcCfg<64, false, plx::BWD_DKV>::SMEM);
     e = e ? e : set_smem(plx::plx_decode_split_kernel<128, true>, DecodeCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_decode_split_kernel<128, false>, DecodeCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_decode_split_kernel<64, true>, DecodeCfg<64>::SMEM);
@@ -154,6 +165,97 @@ plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void
     p.out_f32 = out_dtype == PLX_F32;
     const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
     plx::plx_fwd_tc_kernel<D, PLX><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
+    return launch_status();
+}
+
+// 3-D map over the backward's per-row statistics [BH][N] x float4, for the dkv
+// pass: a {4, 64, 1} box, rows past N zero-filled.
+bool make_stats_map(CUtensorMap* map, const void* base, int N, long long BH) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {4, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {16, static_cast<cuuint64_t>(N) * 16};
+    cuuint32_t box[3] = {4, 64, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Workspace of plx_bwd: per-row statistics, then vbar and kbar (fp32 [BH][N][d]).
+size_t bwd_bf16_ws_bytes(long long BH, int N, int d, size_t* off_vbar, size_t* off_kbar) {
+    const size_t rows = static_cast<size_t>(BH) * N;
+    const size_t stats = align256(rows * 16);
+    const size_t mat = align256(rows * d * sizeof(float));
+    if (off_vbar) *off_vbar = stats;
+    if (off_kbar) *off_kbar = stats + mat;
+    return stats + 2 * mat;
+}
+
+// plx_bwd on the tensor cores: the pre-pass (two softmax-attention forwards for
+// vbar and kbar, then the row statistics), the dq pass and the dkv pass.
+template <int D, bool PLX>
+plx_status launch_bwd_tc(const void* q, const void* k, const void* v, const void* rho, const void* out,
+                         plx_dtype out_dtype, const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                         float* drho, void* workspace, int N, long long BH, float scale, cudaStream_t s,
+                         int sm_count) {
+    using CfgQ = BwdTcCfg<D, PLX, plx::BWD_DQ>;
+    using CfgK = BwdTcCfg<D, PLX, plx::BWD_DKV>;
+    size_t off_vbar = 0, off_kbar = 0;
+    bwd_bf16_ws_bytes(BH, N, D, &off_vbar, &off_kbar);
+    auto* ws = static_cast<uint8_t*>(workspace);
+    auto* stats = reinterpret_cast<float4*>(ws);
+    auto* vbar = reinterpret_cast<float*>(ws + off_vbar);
+    auto* kbar = reinterpret_cast<float*>(ws + off_kbar);
+    plx_status st = launch_fwd_tc<D, false>(q, k, v, nullptr, vbar, nullptr, N, BH, scale, PLX_F32, s, sm_count);
+    if (st != PLX_OK) return st;
+    if (PLX) {
+        st = launch_fwd_tc<D, false>(q, k, k, nullptr, kbar, nullptr, N, BH, scale, PLX_F32, s, sm_count);
+        if (st != PLX_OK) return st;
+    }
+    const long long rows = BH * N;
+    plx::plx_bwd_rowstats_kernel<D, PLX><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(rho), kbar, static_cast<const __nv_bfloat16*>(dout), vbar, out,
+        out_dtype == PLX_F32, lse, stats, rows);
+    if (cudaGetLastError() != cudaSuccess) return PLX_ERR_CUDA;
+
+    const long long n_rt = (N + 127) / 128;
+    if (BH * n_rt > INT_MAX) return PLX_ERR_UNSUPPORTED;
+    plx::BwdTcParams p;
+    p.stats = stats;
+    p.N = N;
+    p.BH = static_cast<int>(BH);
+    p.n_rt = static_cast<int>(n_rt);
+    p.n_items = static_cast<int>(BH * n_rt);
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    const int grid = static_cast<int>(p.n_items < sm_count ? p.n_items : sm_count);
+    CUtensorMap mq_r, mr_r, mo_r, mk_s, mv_s, mk_r, mv_r, mq_s, mr_s, mo_s, mstat, m_dq, m_dr, m_dk, m_dv;
+    // dq pass: Q, rho, dO resident (128 rows); K, V streamed (64 rows)
+    if (!make_map(&mq_r, q, D, N, BH, 128) || !make_map(&mo_r, dout, D, N, BH, 128) ||
+        !make_map(&mk_s, k, D, N, BH, 64) || !make_map(&mv_s, v, D, N, BH, 64) ||
+        !make_map(&mk_r, k, D, N, BH, 128) || !make_map(&mv_r, v, D, N, BH, 128) ||
+        !make_map(&mq_s, q, D, N, BH, 64) || !make_map(&mo_s, dout, D, N, BH, 64) ||
+        !make_stats_map(&mstat, stats, N, BH) || !make_out_map(&m_dq, dq, D, N, BH, true) ||
+        !make_out_map(&m_dk, dk, D, N, BH, true) || !make_out_map(&m_dv, dv, D, N, BH, true))
+        return PLX_ERR_CUDA;
+    if (PLX) {
+        if (!make_map(&mr_r, rho, D, N, BH, 128) || !make_map(&mr_s, rho, D, N, BH, 64) ||
+            !make_out_map(&m_dr, drho, D, N, BH, true))
+            return PLX_ERR_CUDA;
+    } else {
+        mr_r = mq_r;
+        mr_s = mq_s;
+        m_dr = m_dq;
+    }
+    // unused slots get a valid map of the right kind
+    plx::plx_bwd_tc_kernel<D, PLX, plx::BWD_DQ><<<grid, CfgQ::THREADS, CfgQ::SMEM, s>>>(
+        mq_r, PLX ? mr_r : mo_r, mo_r, mk_s, mv_s, mv_s, mstat, m_dq, m_dr, p);
+    if (cudaGetLastError() != cudaSuccess) return PLX_ERR_CUDA;
+    plx::plx_bwd_tc_kernel<D, PLX, plx::BWD_DKV><<<grid, CfgK::THREADS, CfgK::SMEM, s>>>(
+        mk_r, mv_r, mv_r, mq_s, PLX ? mr_s : mo_s, mo_s, mstat, m_dv, m_dk, p);
     return launch_status();
 }
 
@@ -362,6 +464,45 @@ plx_status plx_bwd_f32(const float* q, const float* k, const float* v, const flo
         const bool ok = rho ? dispatch_bwd<true>(p, d, BH, s) : dispatch_bwd<false>(p, d, BH, s);
         if (!ok) return PLX_ERR_UNSUPPORTED;
         return launch_status();
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+size_t plx_bwd_bf16_workspace_size(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+    return bwd_bf16_ws_bytes(static_cast<long long>(B) * H, N, d, nullptr, nullptr);
+}
+
+plx_status plx_bwd(const void* q, const void* k, const void* v, const void* rho, const void* out,
+                   plx_dtype out_dtype, const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                   float* drho, void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale,
+                   void* stream) {
+    try {
+        if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || (rho && !drho))
+            return PLX_ERR_INVALID_ARG;
+        if (B < 1 || H < 1 || N < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
+        if (out_dtype != PLX_BF16 && out_dtype != PLX_F32) return PLX_ERR_INVALID_ARG;
+        if (d != 128 && d != 64) return PLX_ERR_UNSUPPORTED;
+        const void* ptrs16[] = {q, k, v, out, dout, dq, dk, dv, workspace};
+        for (const void* ptr : ptrs16)
+            if (ptr && !aligned(ptr, 16)) return PLX_ERR_MISALIGNED;
+        if ((rho && (!aligned(rho, 16) || !aligned(drho, 16))) || !aligned(lse, 4)) return PLX_ERR_MISALIGNED;
+        const size_t need = plx_bwd_bf16_workspace_size(B, H, N, d);
+        if (!workspace || workspace_bytes < need) return PLX_ERR_WORKSPACE;
+        const DeviceInfo* info = device_info();
+        if (!info) return PLX_ERR_CUDA;
+        const long long BH = static_cast<long long>(B) * H;
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        if (d == 128)
+            return rho ? launch_bwd_tc<128, true>(q, k, v, rho, out, out_dtype, lse, dout, dq, dk, dv, drho, workspace,
+                                                  N, BH, scale, s, info->sm_count)
+                       : launch_bwd_tc<128, false>(q, k, v, rho, out, out_dtype, lse, dout, dq, dk, dv, drho,
+                                                   workspace, N, BH, scale, s, info->sm_count);
+        return rho ? launch_bwd_tc<64, true>(q, k, v, rho, out, out_dtype, lse, dout, dq, dk, dv, drho, workspace, N,
+                                             BH, scale, s, info->sm_count)
+                   : launch_bwd_tc<64, false>(q, k, v, rho, out, out_dtype, lse, dout, dq, dk, dv, drho, workspace, N,
+                                              BH, scale, s, info->sm_count);
     } catch (...) {
         return PLX_ERR_CUDA;
     }
