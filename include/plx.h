@@ -141,32 +141,30 @@ size_t plx_bwd_workspace_size(int B, int H, int N, int d);
 /*
  * plx_bwd -- the same gradients for the bf16 forward, on the tensor cores
  * (tcgen05, fp32 accumulation; ds, dr and the dv weights enter their GEMMs as
- * bf16).  Same formulas as plx_bwd_f32.
+ * fp16, the streamed bf16 tiles they multiply re-encoded to fp16).  Same
+ * formulas as plx_bwd_f32.  The forward's o and lse are not inputs: a
+ * pre-pass (the forward kernel in a statistics mode) recomputes, per row,
+ * log2e lse_i, c_i, a_i = dO_i.vbar_i and D_i = dO_i.o_i + c_i a_i.
  *
  *   q, k, v, rho : bf16 [B][H][N][d], 16-byte aligned; rho may be NULL
  *                  (softmax attention; drho is then ignored).
- *   out          : the forward's o, [B][H][N][d] in out_dtype (PLX_F32 or
- *                  PLX_BF16), 16-byte aligned, e.g. from plx_fwd.
- *   lse          : the forward's lse, fp32 [B][H][N] (natural log).
  *   dout         : dL/do, bf16 [B][H][N][d], 16-byte aligned.
  *   dq, dk, dv, drho : fp32 [B][H][N][d] outputs (written, not accumulated),
  *                  16-byte aligned.
  *   workspace    : device scratch of plx_bwd_bf16_workspace_size(B, H, N, d)
- *                  bytes, 16-byte aligned, no initialisation needed: per-row
- *                  statistics and two fp32 [B][H][N][d] intermediates.
- *   B, H, N >= 1; d in {64, 128}.
- * Launches on `stream`: two softmax-attention forwards (vbar = sum_j w_ij v_j
- * and kbar = sum_j w_ij k_j; the second only with rho), a per-row pass for
- * (lse, c, a, D), a pass over 128-query tiles (dq, drho) and a pass over
- * 128-key tiles (dk, dv).  No atomics: the result is deterministic.
+ *                  bytes (16 per row), 16-byte aligned, no initialisation.
+ *   B, H, N >= 1; d in {64, 128}.  Inputs and the values ds, dr, wv must lie
+ *   within the fp16 range.
+ * Three launches on `stream`: the pre-pass, a pass over 128-query tiles (dq,
+ * drho) and a pass over 128-key tiles (dk, dv).  No atomics: the result is
+ * deterministic.
  * Errors: PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_MISALIGNED,
  * PLX_ERR_WORKSPACE, PLX_ERR_CUDA; device-side wait timeouts are reported by
  * plx_last_device_error.
  */
-plx_status plx_bwd(const void* q, const void* k, const void* v, const void* rho, const void* out,
-                   plx_dtype out_dtype, const float* lse, const void* dout, float* dq, float* dk, float* dv,
-                   float* drho, void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale,
-                   void* stream);
+plx_status plx_bwd(const void* q, const void* k, const void* v, const void* rho, const void* dout, float* dq,
+                   float* dk, float* dv, float* drho, void* workspace, size_t workspace_bytes, int B, int H, int N,
+                   int d, float scale, void* stream);
 
 /* Workspace bytes plx_bwd needs (0 for invalid sizes). */
 size_t plx_bwd_bf16_workspace_size(int B, int H, int N, int d);

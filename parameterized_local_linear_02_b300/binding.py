@@ -65,7 +65,7 @@ def library() -> ctypes.CDLL:
         lib.plx_bwd_workspace_size.restype = sz
         lib.plx_bwd_workspace_size.argtypes = [i, i, i, i]
         lib.plx_bwd.restype = i
-        lib.plx_bwd.argtypes = [vp] * 5 + [i] + [vp] * 7 + [sz, i, i, i, i, f, vp]
+        lib.plx_bwd.argtypes = [vp] * 10 + [sz, i, i, i, i, f, vp]
         lib.plx_bwd_bf16_workspace_size.restype = sz
         lib.plx_bwd_bf16_workspace_size.argtypes = [i, i, i, i]
         lib.plx_decode_noalloc.restype = i
@@ -204,19 +204,16 @@ def plx_bwd_bf16_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return library().plx_bwd_bf16_workspace_size(B, H, N, d)
 
 
-def plx_bwd(q, k, v, rho, out, lse, dout, *, scale=None, workspace=None, grads=None):
+def plx_bwd(q, k, v, rho, dout, *, scale=None, workspace=None, grads=None):
     """Gradients (dq, dk, dv, drho), fp32, of the bf16 causal PLX forward, on
-    the tensor cores.  q, k, v, rho and dout are bf16; ``out`` (fp32 or bf16)
-    and ``lse`` are the forward's outputs; ``rho=None`` gives the
-    softmax-attention gradients (drho is then None).  ``grads`` may pass
-    preallocated (dq, dk, dv, drho) tensors."""
+    the tensor cores.  q, k, v, rho and dout (dL/do) are bf16 [B, H, N, d];
+    the forward's row statistics are recomputed, so o and lse are not needed.
+    ``rho=None`` gives the softmax-attention gradients (drho is then None).
+    ``grads`` may pass preallocated (dq, dk, dv, drho) tensors."""
     B, H, N, d = q.shape
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)) + ((("rho", rho),) if rho is not None else ()):
         _need(t, name, torch.bfloat16, (B, H, N, d), dev)
-    out_code = _out_code(out.dtype)
-    _need(out, "out", out.dtype, (B, H, N, d), dev)
-    _need(lse, "lse", torch.float32, (B, H, N), dev)
     if grads is None:
         grads = tuple(torch.empty((B, H, N, d), dtype=torch.float32, device=dev) for _ in range(3)) + (
             torch.empty((B, H, N, d), dtype=torch.float32, device=dev) if rho is not None else None,)
@@ -228,9 +225,8 @@ def plx_bwd(q, k, v, rho, out, lse, dout, *, scale=None, workspace=None, grads=N
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    st = library().plx_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(out), out_code, _ptr(lse),
-                           _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(drho), _ptr(workspace), ws_bytes,
-                           B, H, N, d, scale, _stream(dev))
+    st = library().plx_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                           _ptr(drho), _ptr(workspace), ws_bytes, B, H, N, d, scale, _stream(dev))
     _check(st, "plx_bwd")
     return dq, dk, dv, drho
 

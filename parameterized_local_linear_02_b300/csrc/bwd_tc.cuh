@@ -12,8 +12,9 @@
 //   wv_ij = w_ij (1 + c_i - r_ij)                              (dv_j = sum_i wv_ij dO_i)
 //   dq_i = scale sum_j ds_ij k_j,   drho_i = sum_j dr_ij k_j,
 //   dk_j = scale sum_i ds_ij q_i + sum_i dr_ij rho_i,   dv_j = sum_i wv_ij dO_i,
-// with w_ij = 2^(scale log2e s_ij - log2e lse_i) from the forward's lse.  The
-// row statistics (log2e lse_i, c_i, a_i, D_i) come from a pre-pass.
+// with w_ij = 2^(scale log2e s_ij - log2e lse_i).  The row statistics
+// (log2e lse_i, c_i, a_i, D_i) come from a pre-pass: the forward kernel in its
+// statistics mode, which has O/l = vbar, C/l = c and o in hand at its epilogue.
 //
 // Two passes over the causal (i, j) tiles, one kernel template:
 //   dq pass  (PASS = BWD_DQ):  a CTA item is 128 query rows; Q, rho and dO of the
@@ -521,60 +522,6 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::TM_COLS);
     }
-}
-
-// Pre-pass of plx_bwd: per row i, (log2e lse_i, c_i, a_i, D_i) with
-//   c_i = rho_i . kbar_i   (kbar_i = sum_j w_ij k_j, so c_i = sum_j w_ij r_ij),
-//   a_i = dO_i . vbar_i,   D_i = dO_i . o_i + c_i a_i.
-// vbar and kbar are softmax-attention forwards (values v and k) computed by the
-// caller.  One warp per row; lane t holds elements [t D/32, (t + 1) D/32).
-template <int D, bool PLX>
-__global__ void __launch_bounds__(256) plx_bwd_rowstats_kernel(const __nv_bfloat16* __restrict__ rho,
-                                                                 const float* __restrict__ kbar,
-                                                                 const __nv_bfloat16* __restrict__ dout,
-                                                                 const float* __restrict__ vbar, const void* out,
-                                                                 int out_f32, const float* __restrict__ lse,
-                                                                 float4* __restrict__ stats, long long rows) {
-    constexpr int DPL = D / 32;
-    const long long r = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (r >= rows) return;
-    const size_t base = static_cast<size_t>(r) * D + lane * DPL;
-    float dov[DPL], vb[DPL], ov[DPL];
-    auto load_bf16 = [&](const __nv_bfloat16* src, float (&f)[DPL]) {
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(src + base);
-#pragma unroll
-        for (int e = 0; e < DPL / 2; ++e) {
-            const uint32_t x = w[e];
-            f[2 * e] = bf16x2_lo(x);
-            f[2 * e + 1] = bf16x2_hi(x);
-        }
-    };
-    load_bf16(dout, dov);
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) vb[e] = vbar[base + e];
-    if (out_f32) {
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) ov[e] = static_cast<const float*>(out)[base + e];
-    } else {
-        load_bf16(static_cast<const __nv_bfloat16*>(out), ov);
-    }
-    float a = 0.f, dd = 0.f, cc = 0.f;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-        a = fmaf(dov[e], vb[e], a);
-        dd = fmaf(dov[e], ov[e], dd);
-    }
-    if constexpr (PLX) {
-        float rv[DPL];
-        load_bf16(rho, rv);
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) cc = fmaf(rv[e], kbar[base + e], cc);
-        cc = warp_sum(cc);
-    }
-    a = warp_sum(a);
-    dd = warp_sum(dd);
-    if (lane == 0) stats[r] = make_float4(lse[r] * 1.4426950408889634f, cc, a, fmaf(cc, a, dd));
 }
 
 }  // namespace plx

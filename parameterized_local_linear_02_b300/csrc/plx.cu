@@ -61,6 +61,10 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, false>, FwdTcCfg<128, false>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, true>, FwdTcCfg<64, true>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, false>, FwdTcCfg<64, false>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, true, true>, FwdTcCfg<128, true>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, false, true>, FwdTcCfg<128, false>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, true, true>, FwdTcCfg<64, true>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, false, true>, FwdTcCfg<64, false>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, true, plx::BWD_DQ>, BwdTcCfg<128, true, plx::BWD_DQ>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, false, plx::BWD_DQ>, BwdTcCfg<128, false, plx::BWD_DQ>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, true, plx::BWD_DKV>, BwdTcCfg<128, true, plx::BWD_DKV>::SMEM);
@@ -138,17 +142,25 @@ plx_status launch_status() {
 
 bool valid_scale(float scale) { return std::isfinite(scale) && scale >= 0.f; }
 
-template <int D, bool PLX>
+// The tcgen05 forward.  STATS: the backward's pre-pass instead of o and lse,
+// per row (log2e lse, c, dO.vbar, dO.o + c dO.vbar) into `stats` from dL/do
+// rows `dout` (out is then unused and must be nullptr).
+template <int D, bool PLX, bool STATS = false>
 plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
                          int N, long long BH, float scale, plx_dtype out_dtype, cudaStream_t stream,
-                         int sm_count) {
+                         int sm_count, const void* dout = nullptr, void* stats = nullptr) {
     using Cfg = FwdTcCfg<D, PLX>;
     const long long n_qt = (N + Cfg::BM - 1) / Cfg::BM;
     const long long n_items = BH * n_qt;
     if (n_items > INT_MAX || BH > INT_MAX) return PLX_ERR_UNSUPPORTED;
     CUtensorMap mq, mr, mk, mv, mo;
     if (!make_map(&mq, q, D, N, BH, Cfg::BM) || !make_map(&mk, k, D, N, BH, Cfg::BN) ||
-        !make_map(&mv, v, D, N, BH, Cfg::BN) || !make_out_map(&mo, out, D, N, BH, out_dtype == PLX_F32))
+        !make_map(&mv, v, D, N, BH, Cfg::BN))
+        return PLX_ERR_CUDA;
+    // the statistics mode stores no o and never touches its output map
+    if (STATS)
+        mo = mq;
+    else if (!make_out_map(&mo, out, D, N, BH, out_dtype == PLX_F32))
         return PLX_ERR_CUDA;
     if (PLX) {
         if (!make_map(&mr, rho, D, N, BH, Cfg::BM)) return PLX_ERR_CUDA;
@@ -163,8 +175,10 @@ plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void
     p.n_items = static_cast<int>(n_items);
     p.scale_log2 = scale * kLog2e;
     p.out_f32 = out_dtype == PLX_F32;
+    p.dout = static_cast<const __nv_bfloat16*>(dout);
+    p.stats = static_cast<float4*>(stats);
     const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
-    plx::plx_fwd_tc_kernel<D, PLX><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
+    plx::plx_fwd_tc_kernel<D, PLX, STATS><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
     return launch_status();
 }
 
@@ -184,42 +198,21 @@ bool make_stats_map(CUtensorMap* map, const void* base, int N, long long BH) {
 
 constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Workspace of plx_bwd: per-row statistics, then vbar and kbar (fp32 [BH][N][d]).
-size_t bwd_bf16_ws_bytes(long long BH, int N, int d, size_t* off_vbar, size_t* off_kbar) {
-    const size_t rows = static_cast<size_t>(BH) * N;
-    const size_t stats = align256(rows * 16);
-    const size_t mat = align256(rows * d * sizeof(float));
-    if (off_vbar) *off_vbar = stats;
-    if (off_kbar) *off_kbar = stats + mat;
-    return stats + 2 * mat;
-}
+// Workspace of plx_bwd: the per-row statistics.
+size_t bwd_bf16_ws_bytes(long long BH, int N) { return align256(static_cast<size_t>(BH) * N * 16); }
 
-// plx_bwd on the tensor cores: the pre-pass (two softmax-attention forwards for
-// vbar and kbar, then the row statistics), the dq pass and the dkv pass.
+// plx_bwd on the tensor cores: the pre-pass (the forward in statistics mode),
+// the dq pass and the dkv pass.
 template <int D, bool PLX>
-plx_status launch_bwd_tc(const void* q, const void* k, const void* v, const void* rho, const void* out,
-                         plx_dtype out_dtype, const float* lse, const void* dout, float* dq, float* dk, float* dv,
-                         float* drho, void* workspace, int N, long long BH, float scale, cudaStream_t s,
-                         int sm_count) {
+plx_status launch_bwd_tc(const void* q, const void* k, const void* v, const void* rho, const void* dout, float* dq,
+                         float* dk, float* dv, float* drho, void* workspace, int N, long long BH, float scale,
+                         cudaStream_t s, int sm_count) {
     using CfgQ = BwdTcCfg<D, PLX, plx::BWD_DQ>;
     using CfgK = BwdTcCfg<D, PLX, plx::BWD_DKV>;
-    size_t off_vbar = 0, off_kbar = 0;
-    bwd_bf16_ws_bytes(BH, N, D, &off_vbar, &off_kbar);
-    auto* ws = static_cast<uint8_t*>(workspace);
-    auto* stats = reinterpret_cast<float4*>(ws);
-    auto* vbar = reinterpret_cast<float*>(ws + off_vbar);
-    auto* kbar = reinterpret_cast<float*>(ws + off_kbar);
-    plx_status st = launch_fwd_tc<D, false>(q, k, v, nullptr, vbar, nullptr, N, BH, scale, PLX_F32, s, sm_count);
+    auto* stats = static_cast<float4*>(workspace);
+    plx_status st = launch_fwd_tc<D, PLX, true>(q, k, v, rho, nullptr, nullptr, N, BH, scale, PLX_F32, s, sm_count,
+                                                dout, stats);
     if (st != PLX_OK) return st;
-    if (PLX) {
-        st = launch_fwd_tc<D, false>(q, k, k, nullptr, kbar, nullptr, N, BH, scale, PLX_F32, s, sm_count);
-        if (st != PLX_OK) return st;
-    }
-    const long long rows = BH * N;
-    plx::plx_bwd_rowstats_kernel<D, PLX><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(rho), kbar, static_cast<const __nv_bfloat16*>(dout), vbar, out,
-        out_dtype == PLX_F32, lse, stats, rows);
-    if (cudaGetLastError() != cudaSuccess) return PLX_ERR_CUDA;
 
     const long long n_rt = (N + 127) / 128;
     if (BH * n_rt > INT_MAX) return PLX_ERR_UNSUPPORTED;
@@ -471,23 +464,20 @@ plx_status plx_bwd_f32(const float* q, const float* k, const float* v, const flo
 
 size_t plx_bwd_bf16_workspace_size(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
-    return bwd_bf16_ws_bytes(static_cast<long long>(B) * H, N, d, nullptr, nullptr);
+    return bwd_bf16_ws_bytes(static_cast<long long>(B) * H, N);
 }
 
-plx_status plx_bwd(const void* q, const void* k, const void* v, const void* rho, const void* out,
-                   plx_dtype out_dtype, const float* lse, const void* dout, float* dq, float* dk, float* dv,
-                   float* drho, void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale,
-                   void* stream) {
+plx_status plx_bwd(const void* q, const void* k, const void* v, const void* rho, const void* dout, float* dq,
+                   float* dk, float* dv, float* drho, void* workspace, size_t workspace_bytes, int B, int H, int N,
+                   int d, float scale, void* stream) {
     try {
-        if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || (rho && !drho))
-            return PLX_ERR_INVALID_ARG;
+        if (!q || !k || !v || !dout || !dq || !dk || !dv || (rho && !drho)) return PLX_ERR_INVALID_ARG;
         if (B < 1 || H < 1 || N < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
-        if (out_dtype != PLX_BF16 && out_dtype != PLX_F32) return PLX_ERR_INVALID_ARG;
         if (d != 128 && d != 64) return PLX_ERR_UNSUPPORTED;
-        const void* ptrs16[] = {q, k, v, out, dout, dq, dk, dv, workspace};
+        const void* ptrs16[] = {q, k, v, dout, dq, dk, dv, workspace};
         for (const void* ptr : ptrs16)
             if (ptr && !aligned(ptr, 16)) return PLX_ERR_MISALIGNED;
-        if ((rho && (!aligned(rho, 16) || !aligned(drho, 16))) || !aligned(lse, 4)) return PLX_ERR_MISALIGNED;
+        if (rho && (!aligned(rho, 16) || !aligned(drho, 16))) return PLX_ERR_MISALIGNED;
         const size_t need = plx_bwd_bf16_workspace_size(B, H, N, d);
         if (!workspace || workspace_bytes < need) return PLX_ERR_WORKSPACE;
         const DeviceInfo* info = device_info();
@@ -495,14 +485,14 @@ plx_status plx_bwd(const void* q, const void* k, const void* v, const void* rho,
         const long long BH = static_cast<long long>(B) * H;
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         if (d == 128)
-            return rho ? launch_bwd_tc<128, true>(q, k, v, rho, out, out_dtype, lse, dout, dq, dk, dv, drho, workspace,
-                                                  N, BH, scale, s, info->sm_count)
-                       : launch_bwd_tc<128, false>(q, k, v, rho, out, out_dtype, lse, dout, dq, dk, dv, drho,
-                                                   workspace, N, BH, scale, s, info->sm_count);
-        return rho ? launch_bwd_tc<64, true>(q, k, v, rho, out, out_dtype, lse, dout, dq, dk, dv, drho, workspace, N,
-                                             BH, scale, s, info->sm_count)
-                   : launch_bwd_tc<64, false>(q, k, v, rho, out, out_dtype, lse, dout, dq, dk, dv, drho, workspace, N,
-                                              BH, scale, s, info->sm_count);
+            return rho ? launch_bwd_tc<128, true>(q, k, v, rho, dout, dq, dk, dv, drho, workspace, N, BH, scale, s,
+                                                  info->sm_count)
+                       : launch_bwd_tc<128, false>(q, k, v, rho, dout, dq, dk, dv, drho, workspace, N, BH, scale, s,
+                                                   info->sm_count);
+        return rho ? launch_bwd_tc<64, true>(q, k, v, rho, dout, dq, dk, dv, drho, workspace, N, BH, scale, s,
+                                             info->sm_count)
+                   : launch_bwd_tc<64, false>(q, k, v, rho, dout, dq, dk, dv, drho, workspace, N, BH, scale, s,
+                                              info->sm_count);
     } catch (...) {
         return PLX_ERR_CUDA;
     }

@@ -124,32 +124,30 @@ def test_bwd_tc_rejects_bad_arguments_before_launch():
     (so these calls are safe without a GPU)."""
     lib = plx.library()
     P, WS = P16, ctypes.c_void_p(0x20000)
-    F32 = 1
-    head = [P] * 5          # q, k, v, rho, out
-    tail = [P] * 6          # lse, dout, dq, dk, dv, drho
+    ins = [P] * 5           # q, k, v, rho, dout
+    outs = [P] * 4          # dq, dk, dv, drho
     need = lib.plx_bwd_bf16_workspace_size(2, 3, 64, 128)
-    rows = 2 * 3 * 64
-    assert need == rows * 16 + 2 * rows * 128 * 4
+    assert need == 2 * 3 * 64 * 16
     assert lib.plx_bwd_bf16_workspace_size(2, 3, 64, 96) == 0
     # head dim without a tensor-core kernel
-    assert lib.plx_bwd(*head, F32, *tail, WS, need, 2, 3, 64, 96, 0.1, None) == 2
-    # out dtype out of range
-    assert lib.plx_bwd(*head, 7, *tail, WS, need, 2, 3, 64, 128, 0.1, None) == 1
+    assert lib.plx_bwd(*ins, *outs, WS, need, 2, 3, 64, 96, 0.1, None) == 2
     # workspace missing or too small
-    assert lib.plx_bwd(*head, F32, *tail, None, 0, 2, 3, 64, 128, 0.1, None) == 6
-    assert lib.plx_bwd(*head, F32, *tail, WS, need - 16, 2, 3, 64, 128, 0.1, None) == 6
+    assert lib.plx_bwd(*ins, *outs, None, 0, 2, 3, 64, 128, 0.1, None) == 6
+    assert lib.plx_bwd(*ins, *outs, WS, need - 16, 2, 3, 64, 128, 0.1, None) == 6
     # misaligned dout and dv
-    for idx in (1, 4):
-        bad = tail[:]
-        bad[idx] = P_ODD
-        assert lib.plx_bwd(*head, F32, *bad, WS, need, 2, 3, 64, 128, 0.1, None) == 3
-    # rho given without drho; missing lse
-    bad = tail[:]
-    bad[5] = None
-    assert lib.plx_bwd(*head, F32, *bad, WS, need, 2, 3, 64, 128, 0.1, None) == 1
-    bad = tail[:]
-    bad[0] = None
-    assert lib.plx_bwd(*head, F32, *bad, WS, need, 2, 3, 64, 128, 0.1, None) == 1
+    bad = ins[:]
+    bad[4] = P_ODD
+    assert lib.plx_bwd(*bad, *outs, WS, need, 2, 3, 64, 128, 0.1, None) == 3
+    bad = outs[:]
+    bad[2] = P_ODD
+    assert lib.plx_bwd(*ins, *bad, WS, need, 2, 3, 64, 128, 0.1, None) == 3
+    # rho given without drho; missing dout
+    bad = outs[:]
+    bad[3] = None
+    assert lib.plx_bwd(*ins, *bad, WS, need, 2, 3, 64, 128, 0.1, None) == 1
+    bad = ins[:]
+    bad[4] = None
+    assert lib.plx_bwd(*bad, *outs, WS, need, 2, 3, 64, 128, 0.1, None) == 1
     # non-positive sizes, negative scale
-    assert lib.plx_bwd(*head, F32, *tail, WS, need, 0, 3, 64, 128, 0.1, None) == 1
-    assert lib.plx_bwd(*head, F32, *tail, WS, need, 2, 3, 64, 128, -1.0, None) == 1
+    assert lib.plx_bwd(*ins, *outs, WS, need, 0, 3, 64, 128, 0.1, None) == 1
+    assert lib.plx_bwd(*ins, *outs, WS, need, 2, 3, 64, 128, -1.0, None) == 1
