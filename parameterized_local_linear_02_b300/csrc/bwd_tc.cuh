@@ -77,7 +77,10 @@ struct BwdTcCfg {
     static constexpr int STAGE_BYTES = N_STR * STR_TILE + (STATS_BYTES + 1023) / 1024 * 1024;
     // the streamed tiles the output GEMMs read (dq: K; dkv: Q, rho, dO), re-encoded in place
     static constexpr int CONV_BYTES = PASS == BWD_DQ ? STR_TILE : N_STR * STR_TILE;
-    static constexpr int NSTAGE = (D == 128) ? 2 : 4;
+    // a stage is held until its step's output GEMMs finish, late in the step, so
+    // the ring needs three stages for the load to run under a whole step
+    // (the dkv pass at d = 128 has room for two)
+    static constexpr int NSTAGE = (D == 128) ? (PASS == BWD_DQ ? 3 : 2) : 4;
     static constexpr int STG_SLOT_BYTES = 32 * 128;   // per elementwise warp: 32 rows x 32 fp32
     static constexpr int OFF_RES = 0;
     static constexpr int OFF_STR = OFF_RES + N_RES * RES_TILE;
