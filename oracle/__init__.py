@@ -14,6 +14,9 @@ Forms (see ``plx_oracle.c`` for the formulas and their sources in
 * ``EXPLICIT`` -- o = o^SA - Sigma_KV rho with the d x d weighted covariance
                   built explicitly (ground truth)
 * ``STREAM``   -- o = (1 + c) vbar - u, c = sum w (rho.k), u = sum w (rho.k) v
+* ``NOINT``    -- the family's no-intercept member, o = -(sum w v k^T) rho with
+                  the raw second moment built explicitly (linear attention
+                  with probe -rho at uniform weights)
 
 Every function here takes arrays of values (float32 or float64) and widens
 them to float64 before calling the C code; nothing here does arithmetic of
@@ -33,8 +36,8 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-SA, EXPLICIT, STREAM = 0, 1, 2
-FORMS = {"sa": SA, "explicit": EXPLICIT, "stream": STREAM}
+SA, EXPLICIT, STREAM, NOINT = 0, 1, 2, 3
+FORMS = {"sa": SA, "explicit": EXPLICIT, "stream": STREAM, "noint": NOINT}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libplx_oracle.so")

@@ -41,12 +41,19 @@
  *   PLX_ORACLE_EXPLICIT  builds Sigma_KV as a d x d matrix, two-pass centred
  *   PLX_ORACLE_STREAM    c = sum w r, u = sum w r v, o = (1 + c) vbar - u,
  *                        r_j = rho . k_j
+ * and one member of the attention family the pages place PLX in (zhichai.net,
+ * the family taxonomy of section 2: bandwidth x probe x affine term):
+ *   PLX_ORACLE_NOINT     "no intercept": vbar = kbar = 0 inside Sigma_KV, so
+ *                        o = -M rho with the raw second moment
+ *                        M = sum_j w_j v_j k_j^T built as a d x d matrix; with
+ *                        uniform weights (scale = 0) it is linear attention
+ *                        with probe -rho.
  */
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
-enum { PLX_ORACLE_SA = 0, PLX_ORACLE_EXPLICIT = 1, PLX_ORACLE_STREAM = 2 };
+enum { PLX_ORACLE_SA = 0, PLX_ORACLE_EXPLICIT = 1, PLX_ORACLE_STREAM = 2, PLX_ORACLE_NOINT = 3 };
 
 /* Softmax weights of q over K[0..n): fills w[0..n), returns the natural-log
  * sum-exp of the scaled scores.  n >= 1. */
@@ -188,6 +195,44 @@ int plx_oracle_stream(const double *q, const double *rho, const double *K,
     return 0;
 }
 
+/* No-intercept member of the family: o = -(sum_j w_j v_j k_j^T) rho, the
+ * d x d raw second moment built explicitly. */
+int plx_oracle_noint(const double *q, const double *rho, const double *K,
+                     const double *V, long n, int d, double scale,
+                     double *out, double *lse)
+{
+    if (n <= 0) {
+        empty_result(d, out, lse);
+        return 0;
+    }
+    double *w = (double *)malloc(sizeof(double) * (size_t)n);
+    double *mom = (double *)calloc((size_t)d * (size_t)d, sizeof(double));
+    if (!w || !mom) {
+        free(w); free(mom);
+        return -1;
+    }
+    *lse = softmax_weights(q, K, n, d, scale, w);
+    for (long j = 0; j < n; ++j) {
+        const double *vj = V + (size_t)j * d;
+        const double *kj = K + (size_t)j * d;
+        for (int a = 0; a < d; ++a) {
+            double wv = w[j] * vj[a];
+            double *row = mom + (size_t)a * d;
+            for (int b = 0; b < d; ++b)
+                row[b] += wv * kj[b];
+        }
+    }
+    for (int a = 0; a < d; ++a) {
+        const double *row = mom + (size_t)a * d;
+        double acc = 0.0;
+        for (int b = 0; b < d; ++b)
+            acc += row[b] * rho[b];
+        out[a] = -acc;
+    }
+    free(w); free(mom);
+    return 0;
+}
+
 /* One query, chosen form.  rho is ignored for PLX_ORACLE_SA. */
 int plx_oracle_query(int form, const double *q, const double *rho,
                      const double *K, const double *V, long n, int d,
@@ -200,6 +245,8 @@ int plx_oracle_query(int form, const double *q, const double *rho,
         return plx_oracle_explicit(q, rho, K, V, n, d, scale, out, lse);
     case PLX_ORACLE_STREAM:
         return plx_oracle_stream(q, rho, K, V, n, d, scale, out, lse);
+    case PLX_ORACLE_NOINT:
+        return plx_oracle_noint(q, rho, K, V, n, d, scale, out, lse);
     default:
         return -2;
     }

@@ -9,7 +9,8 @@ AssertionError when the oracle disagrees with the fact.  The facts come from
 * zhichai.net section 2.1 (the attention family) and gist.science
   "Significato e Affermazioni" (W_R = 0 gives back the Transformer):
   a zero probe is softmax attention; uniform weights with no intercept are a
-  linear-attention form.
+  linear-attention form (pinned for the centred PLX forms and for the
+  no-intercept form itself).
 * zhichai.net section 1.2 and gist.science "Enunciato del Problema": local
   linear attention is the intercept of a locally weighted linear regression
   of v on k around the query; the solved probe rho* makes PLX equal to it.
@@ -276,7 +277,40 @@ def pin_empty(o):
         assert np.all(out == 0) and lse == -np.inf, f"{form} empty"
 
 
+def pin_no_intercept(o):
+    """The family's no-intercept member (zhichai.net section 2.1: without the
+    affine term the covariance loses its centring, vbar = kbar = 0).
+    * Uniform weights (scale = 0): o_i = -S_i rho_i / n with the prefix sums
+      S_i = sum_j v_j k_j^T, linear attention with probe -rho.
+    * Against the centred form: Sigma_KV = M - vbar kbar^T for the raw moment
+      M = sum w v k^T, so o_PLX - o_noint = (1 + rho.kbar) o_SA, with the
+      weights, kbar and o_SA from scipy's softmax.
+    * One key: o = -(rho.k_0) v_0."""
+    rng = _rng(29)
+    N, d = 20, 6
+    Q = rng.standard_normal((N, d))
+    R = rng.standard_normal((N, d))
+    K = rng.standard_normal((N, d))
+    V = rng.standard_normal((N, d))
+    n = np.arange(1, N + 1)[:, None]
+    S = np.cumsum(V[:, :, None] * K[:, None, :], axis=0)
+    out, lse = o.prefill_head("noint", Q, K, V, R, 0.0)
+    _close(out, -np.einsum("iab,ib->ia", S, R) / n, 1e-12, "noint uniform = linear attention with -rho")
+    _close(lse, np.log(n[:, 0]), 1e-13, "noint uniform lse")
+    scale = 0.45
+    plx, _ = o.prefill_head("explicit", Q, K, V, R, scale)
+    noint, lse = o.prefill_head("noint", Q, K, V, R, scale)
+    for i in range(N):
+        w = softmax(scale * K[: i + 1] @ Q[i])
+        kbar = w @ K[: i + 1]
+        osa = w @ V[: i + 1]
+        _close(plx[i] - noint[i], (1.0 + R[i] @ kbar) * osa, 1e-12, f"noint vs centred row {i}")
+        _close(lse[i], logsumexp(scale * K[: i + 1] @ Q[i]), 1e-13, f"noint lse row {i}")
+    out, _ = o.query("noint", Q[0], R[0], K[:1], V[:1], scale)
+    _close(out, -(R[0] @ K[0]) * V[0], 1e-14, "noint one key")
+
+
 ALL_PINS = [pin_sa_closed_forms, pin_rho_zero_is_sa, pin_plx_closed_forms,
             pin_local_linear_regression, pin_uniform_weights_linear_attention,
             pin_invariants, pin_brute_force, pin_causal_prefix, pin_forms_agree,
-            pin_empty]
+            pin_empty, pin_no_intercept]

@@ -1,7 +1,7 @@
 """Each plausible mistake planted in a copy of the oracle (compiled on the
 CPU) must fail at least one pin.  Shows the pins constrain every step:
 softmax scale, normalisation, lse, causal prefix, centring, orientation,
-sign, and the streaming identity."""
+sign, the streaming identity, and the no-intercept form."""
 import os
 import tempfile
 
@@ -28,6 +28,9 @@ MUTANTS = {
     "causal_excludes_diagonal": ("K, V, i + 1, d, scale", "K, V, i, d, scale"),
     "bessel_correction": ("row[b] += dv * (kj[b] - kbar[b]);",
                           "row[b] += dv * (kj[b] - kbar[b]) * ((double)n / (double)(n > 1 ? n - 1 : 1));"),
+    "noint_sign": ("out[a] = -acc;", "out[a] = acc;"),
+    "noint_transposed_moment": ("acc += row[b] * rho[b];", "acc += mom[(size_t)b * d + a] * rho[b];"),
+    "noint_unweighted_moment": ("double wv = w[j] * vj[a];", "double wv = vj[a];"),
 }
 
 
