@@ -95,6 +95,31 @@ plx_status plx_fwd(const void* q, const void* k, const void* v, const void* rho,
                    int B, int H, int N, int d, float scale, plx_dtype out_dtype, void* stream);
 
 /*
+ * Family switches (zhichai.net section 2.1: the attention family is spanned
+ * by the kernel bandwidth, the probe and the affine term; gist.science
+ * "Significato e Affermazioni"):
+ *   PLX_FAMILY_UNIFORM_WEIGHTS  w_ij = 1/(i+1) over the causal prefix, the
+ *                               bandwidth -> infinity limit (scale is taken
+ *                               as 0; lse is then ln(i+1)).
+ *   PLX_FAMILY_NO_INTERCEPT     no affine term: vbar = kbar = 0 inside
+ *                               Sigma_KV, so o_i = -sum_j w_ij (rho_i.k_j) v_j
+ *                               (needs rho).  With uniform weights this is
+ *                               linear attention with probe -rho.
+ */
+#define PLX_FAMILY_UNIFORM_WEIGHTS 0x1u
+#define PLX_FAMILY_NO_INTERCEPT 0x2u
+
+/*
+ * plx_fwd_family -- plx_fwd with family switches (flags: a bitwise OR of the
+ * PLX_FAMILY_* values; 0 is plx_fwd itself).  Same kernels, same arguments.
+ * Errors: as plx_fwd, plus PLX_ERR_INVALID_ARG for unknown flag bits and for
+ * PLX_FAMILY_NO_INTERCEPT without rho.
+ */
+plx_status plx_fwd_family(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
+                          int B, int H, int N, int d, float scale, unsigned flags, plx_dtype out_dtype,
+                          void* stream);
+
+/*
  * plx_fwd_f32 -- the same causal forward with fp32 inputs, fp32 arithmetic on
  * the CUDA cores (the high-precision path; no tensor cores).
  *
@@ -204,6 +229,17 @@ int plx_decode_num_splits(int B, int H, int d, int S_cap);
 
 /* Workspace bytes plx_decode needs (0 when one split suffices). */
 size_t plx_decode_workspace_size(int B, int H, int d, int S_cap, int num_splits);
+
+/*
+ * plx_decode_family -- plx_decode with the family switches above (flags 0 is
+ * plx_decode itself).  Same kernels, same arguments and errors, plus
+ * PLX_ERR_INVALID_ARG for unknown flag bits and for PLX_FAMILY_NO_INTERCEPT
+ * without rho.
+ */
+plx_status plx_decode_family(const void* q, const void* rho, const void* k_cache, const void* v_cache,
+                             const int32_t* seqlens, void* out, float* lse, int B, int H, int d, int S_cap,
+                             float scale, int num_splits, void* workspace, size_t workspace_bytes, unsigned flags,
+                             plx_dtype out_dtype, void* stream);
 
 /*
  * plx_decode_noalloc -- plx_decode for callers that cannot allocate device

@@ -18,6 +18,8 @@ import torch
 from . import build as _build
 
 PLX_BF16, PLX_F32 = 0, 1
+# family switches (see plx_fwd_family in include/plx.h)
+PLX_FAMILY_UNIFORM_WEIGHTS, PLX_FAMILY_NO_INTERCEPT = 0x1, 0x2
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "misaligned", 4: "CUDA error", 7: "range",
            5: "device-side wait timed out", 6: "workspace too small"}
 
@@ -52,10 +54,14 @@ def library() -> ctypes.CDLL:
         lib.plx_strerror.argtypes = [i]
         lib.plx_fwd.restype = i
         lib.plx_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.plx_fwd_family.restype = i
+        lib.plx_fwd_family.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, ctypes.c_uint, i, vp]
         lib.plx_fwd_f32.restype = i
         lib.plx_fwd_f32.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, vp]
         lib.plx_decode.restype = i
         lib.plx_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, i, vp]
+        lib.plx_decode_family.restype = i
+        lib.plx_decode_family.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, ctypes.c_uint, i, vp]
         lib.plx_decode_num_splits.restype = i
         lib.plx_decode_num_splits.argtypes = [i, i, i, i]
         lib.plx_decode_workspace_size.restype = sz
@@ -127,6 +133,17 @@ def plx_fwd(q, k, v, rho=None, *, scale=None, out=None, lse=None, out_dtype=torc
 
     ``rho=None`` runs the softmax-attention instantiation of the same kernel.
     Returns ``(out, lse)``; ``lse`` is None when ``with_lse`` is False."""
+    return _fwd(q, k, v, rho, None, scale, out, lse, out_dtype, with_lse)
+
+
+def plx_fwd_family(q, k, v, rho=None, *, flags, scale=None, out=None, lse=None, out_dtype=torch.bfloat16,
+                   with_lse=True):
+    """plx_fwd with family switches: ``flags`` is a bitwise OR of
+    PLX_FAMILY_UNIFORM_WEIGHTS and PLX_FAMILY_NO_INTERCEPT (0 is plx_fwd)."""
+    return _fwd(q, k, v, rho, int(flags), scale, out, lse, out_dtype, with_lse)
+
+
+def _fwd(q, k, v, rho, flags, scale, out, lse, out_dtype, with_lse):
     B, H, N, d = q.shape
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v)) + ((("rho", rho),) if rho is not None else ()):
@@ -140,9 +157,14 @@ def plx_fwd(q, k, v, rho=None, *, scale=None, out=None, lse=None, out_dtype=torc
     elif lse is not None:
         _need(lse, "lse", torch.float32, (B, H, N), dev)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    st = library().plx_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(out), _ptr(lse), B, H, N, d,
-                           scale, _out_code(out.dtype), _stream(dev))
-    _check(st, "plx_fwd")
+    if flags is None:
+        st = library().plx_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(out), _ptr(lse), B, H, N, d,
+                               scale, _out_code(out.dtype), _stream(dev))
+        _check(st, "plx_fwd")
+    else:
+        st = library().plx_fwd_family(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(out), _ptr(lse), B, H, N, d,
+                                      scale, flags, _out_code(out.dtype), _stream(dev))
+        _check(st, "plx_fwd_family")
     return out, lse
 
 
@@ -245,6 +267,19 @@ def plx_decode(q, rho, k_cache, v_cache, seqlens, *, scale=None, num_splits=0, w
 
     ``q``, ``rho``: bf16 [B, H, d] (``rho=None``: softmax attention);
     ``seqlens``: int32 [B] on the device.  Returns ``(out, lse)``."""
+    return _decode(q, rho, k_cache, v_cache, seqlens, None, scale, num_splits, workspace, out, lse, out_dtype,
+                   with_lse)
+
+
+def plx_decode_family(q, rho, k_cache, v_cache, seqlens, *, flags, scale=None, num_splits=0, workspace=None,
+                      out=None, lse=None, out_dtype=torch.bfloat16, with_lse=True):
+    """plx_decode with family switches (``flags`` as for plx_fwd_family)."""
+    return _decode(q, rho, k_cache, v_cache, seqlens, int(flags), scale, num_splits, workspace, out, lse,
+                   out_dtype, with_lse)
+
+
+def _decode(q, rho, k_cache, v_cache, seqlens, flags, scale, num_splits, workspace, out, lse, out_dtype,
+            with_lse):
     B, H, S_cap, d = k_cache.shape
     dev = k_cache.device
     _need(q, "q", torch.bfloat16, (B, H, d), dev)
@@ -266,10 +301,16 @@ def plx_decode(q, rho, k_cache, v_cache, seqlens, *, scale=None, num_splits=0, w
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    st = library().plx_decode(_ptr(q), _ptr(rho), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
-                              _ptr(out), _ptr(lse), B, H, d, S_cap, scale, int(num_splits),
-                              _ptr(workspace), ws_bytes, _out_code(out.dtype), _stream(dev))
-    _check(st, "plx_decode")
+    if flags is None:
+        st = library().plx_decode(_ptr(q), _ptr(rho), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
+                                  _ptr(out), _ptr(lse), B, H, d, S_cap, scale, int(num_splits),
+                                  _ptr(workspace), ws_bytes, _out_code(out.dtype), _stream(dev))
+        _check(st, "plx_decode")
+    else:
+        st = library().plx_decode_family(_ptr(q), _ptr(rho), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
+                                         _ptr(out), _ptr(lse), B, H, d, S_cap, scale, int(num_splits),
+                                         _ptr(workspace), ws_bytes, flags, _out_code(out.dtype), _stream(dev))
+        _check(st, "plx_decode_family")
     return out, lse
 
 

@@ -59,6 +59,7 @@ struct DecodeParams {
     int splits;
     float scale_log2;   // scale * log2(e)
     int out_f32;
+    int no_intercept;   // the family's no-intercept member: o = -u
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -285,7 +286,7 @@ plx_decode_split_kernel(const DecodeParams p) {
             if (Lsum > 0.f) {
                 const float inv = 1.f / Lsum;
                 const float vbar = As * inv;
-                o = PLX ? fmaf(Cs * inv, vbar, vbar) - Us * inv : vbar;
+                o = PLX ? (p.no_intercept ? -Us * inv : fmaf(Cs * inv, vbar, vbar) - Us * inv) : vbar;
             }
             store_out(p.out, p.out_f32, static_cast<size_t>(bh) * D + t, o);
             if (t == 0 && p.lse)
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(D) plx_decode_combine_kernel(const DecodeParam
     if (Lsum > 0.f) {
         const float inv = 1.f / Lsum;
         const float vbar = As * inv;
-        o = PLX ? fmaf(Cs * inv, vbar, vbar) - Us * inv : vbar;
+        o = PLX ? (p.no_intercept ? -Us * inv : fmaf(Cs * inv, vbar, vbar) - Us * inv) : vbar;
     }
     store_out(p.out, p.out_f32, static_cast<size_t>(bh) * D + t, o);
     if (t == 0 && p.lse) p.lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;

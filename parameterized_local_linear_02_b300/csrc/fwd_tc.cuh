@@ -117,6 +117,7 @@ struct FwdTcParams {
     int n_items;
     float scale_log2;
     int out_f32;
+    int no_intercept;      // the family's no-intercept member: o = -u
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -446,10 +447,15 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                     tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_U + col, uv);
                     tmem_ld_wait(ov);
                     tmem_ld_wait(uv);
+                    if (p.no_intercept) {
 #pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) {
-                        const float vbar = __uint_as_float(ov[cc]) * inv_l;
-                        o[cc] = fmaf(cc_, vbar, vbar) - __uint_as_float(uv[cc]) * inv_l;
+                        for (int cc = 0; cc < 32; ++cc) o[cc] = -__uint_as_float(uv[cc]) * inv_l;
+                    } else {
+#pragma unroll
+                        for (int cc = 0; cc < 32; ++cc) {
+                            const float vbar = __uint_as_float(ov[cc]) * inv_l;
+                            o[cc] = fmaf(cc_, vbar, vbar) - __uint_as_float(uv[cc]) * inv_l;
+                        }
                     }
                 } else {
                     tmem_ld32x32b_x32(lane_addr + Cfg::TM_O + col, ov);

@@ -148,7 +148,7 @@ bool valid_scale(float scale) { return std::isfinite(scale) && scale >= 0.f; }
 template <int D, bool PLX, bool STATS = false>
 plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
                          int N, long long BH, float scale, plx_dtype out_dtype, cudaStream_t stream,
-                         int sm_count, const void* dout = nullptr, void* stats = nullptr) {
+                         int sm_count, const void* dout = nullptr, void* stats = nullptr, bool no_intercept = false) {
     using Cfg = FwdTcCfg<D, PLX>;
     const long long n_qt = (N + Cfg::BM - 1) / Cfg::BM;
     const long long n_items = BH * n_qt;
@@ -177,6 +177,7 @@ plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void
     p.out_f32 = out_dtype == PLX_F32;
     p.dout = static_cast<const __nv_bfloat16*>(dout);
     p.stats = static_cast<float4*>(stats);
+    p.no_intercept = no_intercept ? 1 : 0;
     const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
     plx::plx_fwd_tc_kernel<D, PLX, STATS><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
     return launch_status();
@@ -384,12 +385,21 @@ const char* plx_strerror(plx_status status) {
     }
 }
 
-plx_status plx_fwd(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse, int B,
-                   int H, int N, int d, float scale, plx_dtype out_dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// plx_fwd with the family flags (0 = PLX itself).
+plx_status fwd_impl(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse, int B,
+                    int H, int N, int d, float scale, unsigned flags, plx_dtype out_dtype, void* stream) {
     try {
         if (!q || !k || !v || !out) return PLX_ERR_INVALID_ARG;
         if (B < 1 || H < 1 || N < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
         if (out_dtype != PLX_BF16 && out_dtype != PLX_F32) return PLX_ERR_INVALID_ARG;
+        if ((flags & ~(PLX_FAMILY_UNIFORM_WEIGHTS | PLX_FAMILY_NO_INTERCEPT)) != 0) return PLX_ERR_INVALID_ARG;
+        if ((flags & PLX_FAMILY_NO_INTERCEPT) && !rho) return PLX_ERR_INVALID_ARG;
+        if (flags & PLX_FAMILY_UNIFORM_WEIGHTS) scale = 0.f;
+        const bool noint = (flags & PLX_FAMILY_NO_INTERCEPT) != 0;
         if (d != 128 && d != 64) return PLX_ERR_UNSUPPORTED;
         if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
             (rho && !aligned(rho, 16)) || (lse && !aligned(lse, 4)))
@@ -399,14 +409,31 @@ plx_status plx_fwd(const void* q, const void* k, const void* v, const void* rho,
         const long long BH = static_cast<long long>(B) * H;
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         if (d == 128)
-            return rho ? launch_fwd_tc<128, true>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count)
+            return rho ? launch_fwd_tc<128, true>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count,
+                                                  nullptr, nullptr, noint)
                        : launch_fwd_tc<128, false>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s,
                                                    info->sm_count);
-        return rho ? launch_fwd_tc<64, true>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count)
+        return rho ? launch_fwd_tc<64, true>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count,
+                                             nullptr, nullptr, noint)
                    : launch_fwd_tc<64, false>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count);
     } catch (...) {
         return PLX_ERR_CUDA;
     }
+}
+
+}  // namespace
+
+extern "C" {
+
+plx_status plx_fwd(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse, int B,
+                   int H, int N, int d, float scale, plx_dtype out_dtype, void* stream) {
+    return fwd_impl(q, k, v, rho, out, lse, B, H, N, d, scale, 0u, out_dtype, stream);
+}
+
+plx_status plx_fwd_family(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
+                          int B, int H, int N, int d, float scale, unsigned flags, plx_dtype out_dtype,
+                          void* stream) {
+    return fwd_impl(q, k, v, rho, out, lse, B, H, N, d, scale, flags, out_dtype, stream);
 }
 
 plx_status plx_fwd_f32(const float* q, const float* k, const float* v, const float* rho, float* out, float* lse,
@@ -515,14 +542,23 @@ size_t plx_decode_workspace_size(int B, int H, int d, int S_cap, int num_splits)
     return decode_ws_bytes(static_cast<long long>(B) * H, d, splits);
 }
 
-plx_status plx_decode(const void* q, const void* rho, const void* k_cache, const void* v_cache,
-                      const int32_t* seqlens, void* out, float* lse, int B, int H, int d, int S_cap, float scale,
-                      int num_splits, void* workspace, size_t workspace_bytes, plx_dtype out_dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// plx_decode with the family flags (0 = PLX itself).
+plx_status decode_impl(const void* q, const void* rho, const void* k_cache, const void* v_cache,
+                       const int32_t* seqlens, void* out, float* lse, int B, int H, int d, int S_cap, float scale,
+                       int num_splits, void* workspace, size_t workspace_bytes, unsigned flags, plx_dtype out_dtype,
+                       void* stream) {
     try {
         if (!q || !k_cache || !v_cache || !seqlens || !out) return PLX_ERR_INVALID_ARG;
         if (B < 1 || H < 1 || S_cap < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
         if (num_splits < 0 || num_splits > 1024) return PLX_ERR_INVALID_ARG;
         if (out_dtype != PLX_BF16 && out_dtype != PLX_F32) return PLX_ERR_INVALID_ARG;
+        if ((flags & ~(PLX_FAMILY_UNIFORM_WEIGHTS | PLX_FAMILY_NO_INTERCEPT)) != 0) return PLX_ERR_INVALID_ARG;
+        if ((flags & PLX_FAMILY_NO_INTERCEPT) && !rho) return PLX_ERR_INVALID_ARG;
+        if (flags & PLX_FAMILY_UNIFORM_WEIGHTS) scale = 0.f;
         if (d != 64 && d != 128) return PLX_ERR_UNSUPPORTED;
         if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
             (rho && !aligned(rho, 16)) || !aligned(seqlens, 4) || (lse && !aligned(lse, 4)) ||
@@ -549,6 +585,7 @@ plx_status plx_decode(const void* q, const void* rho, const void* k_cache, const
         p.splits = splits;
         p.scale_log2 = scale * kLog2e;
         p.out_f32 = out_dtype == PLX_F32;
+        p.no_intercept = (flags & PLX_FAMILY_NO_INTERCEPT) ? 1 : 0;
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         if (d == 128) {
             if (rho) launch_decode<128, true>(p, BH, s);
@@ -567,6 +604,25 @@ plx_status plx_decode(const void* q, const void* rho, const void* k_cache, const
 // static device array of PLX_DECODE_NOALLOC_SCRATCH_BYTES per GPU; its device
 // address is looked up once per device and handed to plx_decode as the
 // workspace, so this path allocates nothing.
+}  // namespace
+
+extern "C" {
+
+plx_status plx_decode(const void* q, const void* rho, const void* k_cache, const void* v_cache,
+                      const int32_t* seqlens, void* out, float* lse, int B, int H, int d, int S_cap, float scale,
+                      int num_splits, void* workspace, size_t workspace_bytes, plx_dtype out_dtype, void* stream) {
+    return decode_impl(q, rho, k_cache, v_cache, seqlens, out, lse, B, H, d, S_cap, scale, num_splits, workspace,
+                       workspace_bytes, 0u, out_dtype, stream);
+}
+
+plx_status plx_decode_family(const void* q, const void* rho, const void* k_cache, const void* v_cache,
+                             const int32_t* seqlens, void* out, float* lse, int B, int H, int d, int S_cap,
+                             float scale, int num_splits, void* workspace, size_t workspace_bytes, unsigned flags,
+                             plx_dtype out_dtype, void* stream) {
+    return decode_impl(q, rho, k_cache, v_cache, seqlens, out, lse, B, H, d, S_cap, scale, num_splits, workspace,
+                       workspace_bytes, flags, out_dtype, stream);
+}
+
 plx_status plx_decode_noalloc(const void* q, const void* rho, const void* k_cache, const void* v_cache,
                               const int32_t* seqlens, void* out, float* lse, int B, int H, int d, int S_cap,
                               float scale, int num_splits, plx_dtype out_dtype, void* stream) {

@@ -151,3 +151,19 @@ def test_bwd_tc_rejects_bad_arguments_before_launch():
     # non-positive sizes, negative scale
     assert lib.plx_bwd(*ins, *outs, WS, need, 0, 3, 64, 128, 0.1, None) == 1
     assert lib.plx_bwd(*ins, *outs, WS, need, 2, 3, 64, 128, -1.0, None) == 1
+
+def test_family_entry_points_reject_bad_flags_before_launch():
+    """plx_fwd_family / plx_decode_family: unknown flag bits and the
+    no-intercept switch without a probe are rejected on the host."""
+    lib = plx.library()
+    P = P16
+    F32 = 1
+    # unknown bit
+    assert lib.plx_fwd_family(P, P, P, P, P, P, 1, 1, 64, 128, 0.1, 0x4, F32, None) == 1
+    # no intercept without rho
+    assert lib.plx_fwd_family(P, P, P, None, P, P, 1, 1, 64, 128, 0.1, 0x2, F32, None) == 1
+    # still validated like plx_fwd: head dim
+    assert lib.plx_fwd_family(P, P, P, P, P, P, 1, 1, 64, 96, 0.1, 0x1, F32, None) == 2
+    SL = ctypes.c_void_p(0x30000)
+    assert lib.plx_decode_family(P, P, P, P, SL, P, P, 1, 1, 128, 64, 0.1, 1, None, 0, 0x8, F32, None) == 1
+    assert lib.plx_decode_family(P, None, P, P, SL, P, P, 1, 1, 128, 64, 0.1, 1, None, 0, 0x2, F32, None) == 1
