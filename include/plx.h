@@ -231,6 +231,27 @@ int plx_decode_num_splits(int B, int H, int d, int S_cap);
 size_t plx_decode_workspace_size(int B, int H, int d, int S_cap, int num_splits);
 
 /*
+ * plx_decode_paged -- plx_decode over a paged KV cache.
+ *
+ *   k_pages, v_pages : bf16 [num_blocks][H][page_size][d], 16-byte aligned.
+ *   block_table      : int32 [B][max_blocks_per_seq] on the device, 4-byte
+ *                      aligned: row r (0 <= r < seqlens[b]) of sequence b is
+ *                      row r % page_size of block block_table[b][r / page_size].
+ *   page_size        : a multiple of 32 (a decode tile never straddles blocks).
+ *   The cache capacity per sequence is max_blocks_per_seq * page_size; it plays
+ *   the part of S_cap (lengths above it are clamped and flagged, as in
+ *   plx_decode), also for plx_decode_workspace_size.  A block id outside
+ *   [0, num_blocks) is never dereferenced: block 0 is read in its place and the
+ *   device status word reports PLX_ERR_INVALID_ARG through
+ *   plx_last_device_error.
+ * Other arguments, the result and the errors are those of plx_decode.
+ */
+plx_status plx_decode_paged(const void* q, const void* rho, const void* k_pages, const void* v_pages,
+                            const int32_t* block_table, const int32_t* seqlens, void* out, float* lse, int B, int H,
+                            int d, int page_size, int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
+                            void* workspace, size_t workspace_bytes, plx_dtype out_dtype, void* stream);
+
+/*
  * plx_decode_family -- plx_decode with the family switches above (flags 0 is
  * plx_decode itself).  Same kernels, same arguments and errors, plus
  * PLX_ERR_INVALID_ARG for unknown flag bits and for PLX_FAMILY_NO_INTERCEPT

@@ -60,6 +60,8 @@ def library() -> ctypes.CDLL:
         lib.plx_fwd_f32.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, vp]
         lib.plx_decode.restype = i
         lib.plx_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, i, vp]
+        lib.plx_decode_paged.restype = i
+        lib.plx_decode_paged.argtypes = [vp] * 8 + [i] * 6 + [f, i, vp, sz, i, vp]
         lib.plx_decode_family.restype = i
         lib.plx_decode_family.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, ctypes.c_uint, i, vp]
         lib.plx_decode_num_splits.restype = i
@@ -269,6 +271,43 @@ def plx_decode(q, rho, k_cache, v_cache, seqlens, *, scale=None, num_splits=0, w
     ``seqlens``: int32 [B] on the device.  Returns ``(out, lse)``."""
     return _decode(q, rho, k_cache, v_cache, seqlens, None, scale, num_splits, workspace, out, lse, out_dtype,
                    with_lse)
+
+
+def plx_decode_paged(q, rho, k_pages, v_pages, block_table, seqlens, *, scale=None, num_splits=0,
+                     workspace=None, out=None, lse=None, out_dtype=torch.bfloat16, with_lse=True):
+    """plx_decode over a paged bf16 cache: ``k_pages``, ``v_pages`` are
+    [num_blocks, H, page_size, d]; ``block_table`` is int32 [B, max_blocks]
+    (row r of sequence b is row r % page_size of block block_table[b, r //
+    page_size]); ``q``, ``rho`` bf16 [B, H, d]; ``seqlens`` int32 [B]."""
+    num_blocks, H, page, d = k_pages.shape
+    B, max_blocks = block_table.shape
+    dev = k_pages.device
+    _need(q, "q", torch.bfloat16, (B, H, d), dev)
+    if rho is not None:
+        _need(rho, "rho", torch.bfloat16, (B, H, d), dev)
+    _need(k_pages, "k_pages", torch.bfloat16, (num_blocks, H, page, d), dev)
+    _need(v_pages, "v_pages", torch.bfloat16, (num_blocks, H, page, d), dev)
+    _need(block_table, "block_table", torch.int32, (B, max_blocks), dev)
+    _need(seqlens, "seqlens", torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty((B, H, d), dtype=out_dtype, device=dev)
+    else:
+        _need(out, "out", out.dtype, (B, H, d), dev)
+    if lse is None and with_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, (B, H), dev)
+    need = plx_decode_workspace_size(B, H, d, max_blocks * page, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().plx_decode_paged(_ptr(q), _ptr(rho), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                    _ptr(seqlens), _ptr(out), _ptr(lse), B, H, d, page, max_blocks, num_blocks,
+                                    scale, int(num_splits), _ptr(workspace), ws_bytes, _out_code(out.dtype),
+                                    _stream(dev))
+    _check(st, "plx_decode_paged")
+    return out, lse
 
 
 def plx_decode_family(q, rho, k_cache, v_cache, seqlens, *, flags, scale=None, num_splits=0, workspace=None,

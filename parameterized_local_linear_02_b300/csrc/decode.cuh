@@ -60,6 +60,14 @@ struct DecodeParams {
     float scale_log2;   // scale * log2(e)
     int out_f32;
     int no_intercept;   // the family's no-intercept member: o = -u
+    // paged cache (block_table != nullptr): kc, vc are [num_blocks][H][page][D]
+    // and row r of sequence b lives in block block_table[b][r / page] at row
+    // r % page; S_cap is max_blocks * page.  page is a multiple of T, so a
+    // tile never straddles two blocks.
+    const int* block_table;
+    int max_blocks;
+    int page;
+    int num_blocks;
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -143,7 +151,19 @@ plx_decode_split_kernel(const DecodeParams p) {
                 const int t = t_begin + i;
                 const int rows = min(T, L - t * T);
                 const uint32_t bytes = static_cast<uint32_t>(rows) * D * 2;
-                const size_t g = (head_row0 + static_cast<size_t>(t) * T) * D;
+                size_t g = (head_row0 + static_cast<size_t>(t) * T) * D;
+                if (p.block_table) {
+                    const int r0 = t * T;
+                    const int pg = r0 / p.page;
+                    int blk = p.block_table[static_cast<size_t>(b) * p.max_blocks + pg];
+                    if (blk < 0 || blk >= p.num_blocks) {
+                        // an invalid block id: flag it and read block 0 instead, so
+                        // the copy stays inside the cache
+                        atomicOr(&g_plx_status, PLX_DEV_ERR_SEQLEN);
+                        blk = 0;
+                    }
+                    g = ((static_cast<size_t>(blk) * p.H + (bh % p.H)) * p.page + (r0 - pg * p.page)) * D;
+                }
                 mbar_arrive_expect_tx(&full[s], 2 * bytes);
                 bulk_g2s_hint(kbuf + s * T * D, p.kc + g, bytes, &full[s], pol);
                 bulk_g2s_hint(vbuf + s * T * D, p.vc + g, bytes, &full[s], pol);

@@ -546,11 +546,19 @@ size_t plx_decode_workspace_size(int B, int H, int d, int S_cap, int num_splits)
 
 namespace {
 
-// plx_decode with the family flags (0 = PLX itself).
+// A paged KV cache: the block table and its sizes (block_table == nullptr: contiguous).
+struct PagedCache {
+    const int32_t* block_table = nullptr;
+    int max_blocks = 0;
+    int page = 0;
+    int num_blocks = 0;
+};
+
+// plx_decode with the family flags (0 = PLX itself), on a contiguous or paged cache.
 plx_status decode_impl(const void* q, const void* rho, const void* k_cache, const void* v_cache,
                        const int32_t* seqlens, void* out, float* lse, int B, int H, int d, int S_cap, float scale,
                        int num_splits, void* workspace, size_t workspace_bytes, unsigned flags, plx_dtype out_dtype,
-                       void* stream) {
+                       void* stream, const PagedCache& paged = PagedCache()) {
     try {
         if (!q || !k_cache || !v_cache || !seqlens || !out) return PLX_ERR_INVALID_ARG;
         if (B < 1 || H < 1 || S_cap < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
@@ -586,6 +594,10 @@ plx_status decode_impl(const void* q, const void* rho, const void* k_cache, cons
         p.scale_log2 = scale * kLog2e;
         p.out_f32 = out_dtype == PLX_F32;
         p.no_intercept = (flags & PLX_FAMILY_NO_INTERCEPT) ? 1 : 0;
+        p.block_table = paged.block_table;
+        p.max_blocks = paged.max_blocks;
+        p.page = paged.page;
+        p.num_blocks = paged.num_blocks;
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         if (d == 128) {
             if (rho) launch_decode<128, true>(p, BH, s);
@@ -621,6 +633,29 @@ plx_status plx_decode_family(const void* q, const void* rho, const void* k_cache
                              plx_dtype out_dtype, void* stream) {
     return decode_impl(q, rho, k_cache, v_cache, seqlens, out, lse, B, H, d, S_cap, scale, num_splits, workspace,
                        workspace_bytes, flags, out_dtype, stream);
+}
+
+plx_status plx_decode_paged(const void* q, const void* rho, const void* k_pages, const void* v_pages,
+                            const int32_t* block_table, const int32_t* seqlens, void* out, float* lse, int B, int H,
+                            int d, int page_size, int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
+                            void* workspace, size_t workspace_bytes, plx_dtype out_dtype, void* stream) {
+    try {
+        if (!block_table) return PLX_ERR_INVALID_ARG;
+        if (page_size < 32 || page_size % 32 != 0 || max_blocks_per_seq < 1 || num_blocks < 1)
+            return PLX_ERR_INVALID_ARG;
+        if (!aligned(block_table, 4)) return PLX_ERR_MISALIGNED;
+        const long long S_cap = static_cast<long long>(max_blocks_per_seq) * page_size;
+        if (S_cap > INT_MAX) return PLX_ERR_UNSUPPORTED;
+        PagedCache pc;
+        pc.block_table = block_table;
+        pc.max_blocks = max_blocks_per_seq;
+        pc.page = page_size;
+        pc.num_blocks = num_blocks;
+        return decode_impl(q, rho, k_pages, v_pages, seqlens, out, lse, B, H, d, static_cast<int>(S_cap), scale,
+                           num_splits, workspace, workspace_bytes, 0u, out_dtype, stream, pc);
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
 }
 
 plx_status plx_decode_noalloc(const void* q, const void* rho, const void* k_cache, const void* v_cache,

@@ -167,3 +167,18 @@ def test_family_entry_points_reject_bad_flags_before_launch():
     SL = ctypes.c_void_p(0x30000)
     assert lib.plx_decode_family(P, P, P, P, SL, P, P, 1, 1, 128, 64, 0.1, 1, None, 0, 0x8, F32, None) == 1
     assert lib.plx_decode_family(P, None, P, P, SL, P, P, 1, 1, 128, 64, 0.1, 1, None, 0, 0x2, F32, None) == 1
+
+
+def test_decode_paged_rejects_bad_arguments_before_launch():
+    lib = plx.library()
+    P = P16
+    F32 = 1
+    T = ctypes.c_void_p(0x40000)
+    SL = ctypes.c_void_p(0x30000)
+    args = lambda table, page, maxb, nblk: (P, P, P, P, table, SL, P, P, 2, 2, 128, page, maxb, nblk, 0.1, 1,
+                                            None, 0, F32, None)
+    assert lib.plx_decode_paged(*args(None, 64, 4, 8)) == 1            # no block table
+    assert lib.plx_decode_paged(*args(T, 48, 4, 8)) == 1               # page not a multiple of 32
+    assert lib.plx_decode_paged(*args(T, 64, 0, 8)) == 1               # no blocks per sequence
+    assert lib.plx_decode_paged(*args(T, 64, 4, 0)) == 1               # empty cache
+    assert lib.plx_decode_paged(*args(ctypes.c_void_p(0x40002), 64, 4, 8)) == 3   # misaligned table
