@@ -95,6 +95,29 @@ plx_status plx_fwd(const void* q, const void* k, const void* v, const void* rho,
                    int B, int H, int N, int d, float scale, plx_dtype out_dtype, void* stream);
 
 /*
+ * plx_fwd_cached -- several new query tokens per sequence against a bf16 KV
+ * cache, on the tensor cores: the T newest positions of each sequence attend
+ * causally to its cache (speculative verification, chunked prefill).  Query
+ * row i of sequence b sits at position seqlens[b] - T + i and attends to
+ * cache rows 0 .. seqlens[b] - T + i.  The same kernel as plx_fwd (plx_fwd is
+ * this with T = N and seqlens[b] = N).
+ *
+ *   q, rho       : bf16 [B][H][T][d], 16-byte aligned; rho may be NULL (SA).
+ *   k_cache, v_cache : bf16 [B][H][S_cap][d], 16-byte aligned, already holding
+ *                  the T new tokens at positions seqlens[b] - T .. seqlens[b] - 1.
+ *   seqlens      : int32 [B] on the device, T <= seqlens[b] <= S_cap; a length
+ *                  outside that range is clamped into it and reported by
+ *                  plx_last_device_error as PLX_ERR_INVALID_ARG.
+ *   out          : [B][H][T][d] of out_dtype;  lse : fp32 [B][H][T] or NULL.
+ *   B, H >= 1, 1 <= T <= S_cap; d in {64, 128}.  Cache rows past seqlens[b]
+ *   are never used (they may hold anything, including non-finite values).
+ * Errors: as plx_fwd.
+ */
+plx_status plx_fwd_cached(const void* q, const void* rho, const void* k_cache, const void* v_cache,
+                          const int32_t* seqlens, void* out, float* lse, int B, int H, int T, int S_cap, int d,
+                          float scale, plx_dtype out_dtype, void* stream);
+
+/*
  * Family switches (zhichai.net section 2.1: the attention family is spanned
  * by the kernel bandwidth, the probe and the affine term; gist.science
  * "Significato e Affermazioni"):

@@ -54,6 +54,8 @@ def library() -> ctypes.CDLL:
         lib.plx_strerror.argtypes = [i]
         lib.plx_fwd.restype = i
         lib.plx_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.plx_fwd_cached.restype = i
+        lib.plx_fwd_cached.argtypes = [vp] * 7 + [i] * 5 + [f, i, vp]
         lib.plx_fwd_family.restype = i
         lib.plx_fwd_family.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, ctypes.c_uint, i, vp]
         lib.plx_fwd_f32.restype = i
@@ -136,6 +138,37 @@ def plx_fwd(q, k, v, rho=None, *, scale=None, out=None, lse=None, out_dtype=torc
     ``rho=None`` runs the softmax-attention instantiation of the same kernel.
     Returns ``(out, lse)``; ``lse`` is None when ``with_lse`` is False."""
     return _fwd(q, k, v, rho, None, scale, out, lse, out_dtype, with_lse)
+
+
+def plx_fwd_cached(q, rho, k_cache, v_cache, seqlens, *, scale=None, out=None, lse=None,
+                   out_dtype=torch.bfloat16, with_lse=True):
+    """T new query tokens per sequence against a bf16 KV cache, on the tensor
+    cores: ``q``, ``rho`` bf16 [B, H, T, d]; ``k_cache``, ``v_cache`` bf16
+    [B, H, S_cap, d] already holding the new tokens at positions
+    seqlens[b] - T .. seqlens[b] - 1; ``seqlens`` int32 [B].  Query row i of
+    sequence b attends to cache rows 0 .. seqlens[b] - T + i."""
+    B, H, T, d = q.shape
+    S_cap = k_cache.shape[2]
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (B, H, T, d), dev)
+    if rho is not None:
+        _need(rho, "rho", torch.bfloat16, (B, H, T, d), dev)
+    _need(k_cache, "k_cache", torch.bfloat16, (B, H, S_cap, d), dev)
+    _need(v_cache, "v_cache", torch.bfloat16, (B, H, S_cap, d), dev)
+    _need(seqlens, "seqlens", torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty((B, H, T, d), dtype=out_dtype, device=dev)
+    else:
+        _need(out, "out", out.dtype, (B, H, T, d), dev)
+    if lse is None and with_lse:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, T), dev)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().plx_fwd_cached(_ptr(q), _ptr(rho), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(out),
+                                  _ptr(lse), B, H, T, S_cap, d, scale, _out_code(out.dtype), _stream(dev))
+    _check(st, "plx_fwd_cached")
+    return out, lse
 
 
 def plx_fwd_family(q, k, v, rho=None, *, flags, scale=None, out=None, lse=None, out_dtype=torch.bfloat16,

@@ -111,7 +111,12 @@ struct FwdTcParams {
     // (log2e lse, c, dO.vbar, dO.o + c dO.vbar) out instead of o
     const __nv_bfloat16* dout;
     float4* stats;
-    int N;
+    int N;                 // K/V rows per head (the cache capacity in the cached mode)
+    int Tq;                // query rows per head (N for the self-attention prefill)
+    // cached mode: queries are the last Tq positions of a cache of seqlens[b]
+    // rows (positions seqlens[b] - Tq + i); nullptr: query row i is position i
+    const int* seqlens;
+    int H;
     int BH;
     int n_qt;
     int n_items;
@@ -130,6 +135,30 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ void item_coords(int u, int BH, int n_qt, int& bh, int& qt) {
     qt = n_qt - 1 - u / BH;
     bh = u % BH;
+}
+// Geometry of item u: head bh, first query row q0, the position of query row
+// 0 (off: 0 for the self-attention prefill, seqlens[b] - Tq in the cached
+// mode, with seqlens[b] clamped to [Tq, N]) and the number of K/V tiles it
+// reads.  Every role computes it the same way.
+struct ItemSpan {
+    int bh, q0, off, n_kv;
+};
+__device__ __forceinline__ ItemSpan item_span(const FwdTcParams& p, int u, int BM, int BN, bool flag_bad = false) {
+    ItemSpan it;
+    int qt;
+    item_coords(u, p.BH, p.n_qt, it.bh, qt);
+    it.q0 = qt * BM;
+    int L = p.N;
+    if (p.seqlens) {
+        L = p.seqlens[it.bh / p.H];
+        if (L < p.Tq || L > p.N) {
+            if (flag_bad) atomicOr(&g_plx_status, PLX_DEV_ERR_SEQLEN);
+            L = L < p.Tq ? p.Tq : p.N;
+        }
+    }
+    it.off = L - p.Tq;
+    it.n_kv = (it.off + min(p.Tq, it.q0 + BM) + BN - 1) / BN;
+    return it;
 }
 // u for round r of CTA c in a snake over the grid
 __device__ __forceinline__ int snake_item(int r, int c, int G) {
@@ -220,10 +249,8 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             for (int r = 0; ok; ++r) {
                 const int u = snake_item(r, c, G);
                 if (u >= p.n_items || *abort_flag) break;
-                int bh, qt;
-                item_coords(u, p.BH, p.n_qt, bh, qt);
-                const int q0 = qt * BM;
-                const int n_kv = (min(p.N, q0 + BM) + BN - 1) / BN;
+                const ItemSpan it = item_span(p, u, BM, BN, true);
+                const int bh = it.bh, q0 = it.q0, n_kv = it.n_kv;
                 const int un = snake_item(r + 1, c, G);    // this CTA's next item
                 if (nq > 0 && !mbar_wait(q_empty, (nq - 1) & 1)) { ok = false; break; }
                 mbar_arrive_expect_tx(q_full, (PLX ? 2 : 1) * Cfg::Q_BYTES);
@@ -304,10 +331,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             const int u = snake_item(r, c, G);
             // one read of the flag for the whole warp: every lane takes the same branch
             if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            int bh, qt;
-            item_coords(u, p.BH, p.n_qt, bh, qt);
-            const int q0 = qt * BM;
-            const int n_kv = (min(p.N, q0 + BM) + BN - 1) / BN;
+            const int n_kv = item_span(p, u, BM, BN).n_kv;
             if (!wait_warp(q_full, items & 1)) { ok = false; break; }
             tc_fence_after();
             for (int j = 0; j < n_kv; ++j, ++g) {
@@ -386,7 +410,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             const int eq0 = eqt * BM;
             // rows past N are clipped by the TMA store; a warp whose 32 rows all
             // are past N has nothing to write (both warps of the pair decide alike)
-            if (eq0 + quad * 32 >= p.N) return true;
+            if (eq0 + quad * 32 >= p.Tq) return true;
             const float2 e0 = xe[row], e1 = xe[BM + row];
             const float l_all = e0.x + e1.x, C_all = e0.y + e1.y;
             const float inv_l = 1.f / l_all;
@@ -395,8 +419,8 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 // dO_i . vbar_i and dO_i . o_i over this warp's half of the columns,
                 // then summed across the pair through shared memory
                 const int ei = eq0 + row;
-                const bool live = ei < p.N;
-                const __nv_bfloat16* drow = p.dout + (static_cast<size_t>(ebh) * p.N + (live ? ei : 0)) * D;
+                const bool live = ei < p.Tq;
+                const __nv_bfloat16* drow = p.dout + (static_cast<size_t>(ebh) * p.Tq + (live ? ei : 0)) * D;
                 float pa = 0.f, pd = 0.f;
 #pragma unroll 1
                 for (int ch = 0; ch < Cfg::NCH; ++ch) {
@@ -431,7 +455,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 const float a = s0.x + s1.x, dd = s0.y + s1.y;
                 const float c = PLX ? cc_ : 0.f;
                 if (live && half == 0)
-                    p.stats[static_cast<size_t>(ebh) * p.N + ei] = make_float4(em + __log2f(l_all), c, a, fmaf(c, a, dd));
+                    p.stats[static_cast<size_t>(ebh) * p.Tq + ei] = make_float4(em + __log2f(l_all), c, a, fmaf(c, a, dd));
                 return true;
             }
             // 0 * o is NaN exactly when o is not finite: one running sum flags them all
@@ -492,9 +516,9 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 }
             }
             const int ei = eq0 + row;
-            const bool store = ei < p.N;
+            const bool store = ei < p.Tq;
             if (store && half == 0 && p.lse)
-                p.lse[static_cast<size_t>(ebh) * p.N + ei] = (em + __log2f(l_all)) * 0.69314718055994531f;
+                p.lse[static_cast<size_t>(ebh) * p.Tq + ei] = (em + __log2f(l_all)) * 0.69314718055994531f;
             if (__any_sync(0xffffffffu, store && !(bad == 0.f)) && lane == 0)
                 atomicOr(&g_plx_status, PLX_DEV_ERR_NONFINITE);
             return true;
@@ -508,11 +532,10 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         for (int r = 0; ok; ++r) {
             const int u = snake_item(r, c, G);
             if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            int bh, qt;
-            item_coords(u, p.BH, p.n_qt, bh, qt);
-            const int q0 = qt * BM;
+            const ItemSpan it = item_span(p, u, BM, BN);
+            const int q0 = it.q0, n_kv = it.n_kv;
             const int i = q0 + row;                 // this thread's query row
-            const int n_kv = (min(p.N, q0 + BM) + BN - 1) / BN;
+            const int pos = it.off + i;             // its position: keys 0 .. pos
             float m = -INFINITY, l = 0.f, C = 0.f;
             for (int j = 0; j < n_kv; ++j, ++g) {
                 const int b = g & 1;
@@ -528,13 +551,13 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 float sc[HALF];
 #pragma unroll
                 for (int cc = 0; cc < HALF; ++cc) sc[cc] = __uint_as_float(sraw[cc]);
-                // causal mask on tiles that reach past the first row of the item
-                const bool diag = (j + 1) * BN - 1 > q0;
+                // causal mask on tiles that reach past the first position of the item
+                const bool diag = (j + 1) * BN - 1 > it.off + q0;
                 const int kbase = j * BN + half * HALF;
                 if (diag) {
 #pragma unroll
                     for (int cc = 0; cc < HALF; ++cc)
-                        if (kbase + cc > i) sc[cc] = -INFINITY;
+                        if (kbase + cc > pos) sc[cc] = -INFINITY;
                 }
                 // row max over this warp's 32 keys: a tree of three-input maxes
                 float mx[11];
@@ -594,7 +617,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 if (diag) {
 #pragma unroll
                     for (int cc = 0; cc < HALF; ++cc)
-                        if (kbase + cc > i) pe[cc] = 0.f;       // also covers scale == 0
+                        if (kbase + cc > pos) pe[cc] = 0.f;     // also covers scale == 0
                 }
                 // P and PR go to the tensor cores as fp16; l and C are summed from
                 // the same rounded values, so o = (1 + C/l) O/l - U/l is exactly
@@ -611,6 +634,13 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 tmem_st32x32b_x16(tS + half * HALF, pk);
                 if constexpr (PLX) {
                     tmem_ld_wait(rraw);
+                    // masked keys contribute nothing, even where R is not finite
+                    // (cache rows past the sequence in the cached mode)
+                    if (diag) {
+#pragma unroll
+                        for (int cc = 0; cc < HALF; ++cc)
+                            if (kbase + cc > pos) rraw[cc] = 0u;
+                    }
                     float cs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int cc = 0; cc < HALF / 2; ++cc) {
@@ -686,22 +716,30 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         for (int r = 0; ok; ++r) {
             const int u = snake_item(r, c, G);
             if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            int bh, qt;
-            item_coords(u, p.BH, p.n_qt, bh, qt);
-            const int q0 = qt * BM;
-            const int n_kv = (min(p.N, q0 + BM) + BN - 1) / BN;
+            const ItemSpan it = item_span(p, u, BM, BN);
+            const int n_kv = it.n_kv;
+            const int L = it.off + p.Tq;          // keys at L and beyond are masked for every row
             for (int j = 0; j < n_kv; ++j, ++g) {
                 const int stage = g % NSTAGE;
                 if (!wait_warp(&v_full[stage], (g / NSTAGE) & 1)) { ok = false; break; }
                 uint4* vt = reinterpret_cast<uint4*>(sV + stage * Cfg::KV_BYTES);
 #pragma unroll
                 for (int k = 0; k < Cfg::KV_BYTES / 16 / Cfg::CV_THREADS; ++k) {
-                    uint4 w = vt[t + Cfg::CV_THREADS * k];
-                    w.x = bf16x2_to_f16x2(w.x);
-                    w.y = bf16x2_to_f16x2(w.y);
-                    w.z = bf16x2_to_f16x2(w.z);
-                    w.w = bf16x2_to_f16x2(w.w);
-                    vt[t + Cfg::CV_THREADS * k] = w;
+                    const int idx = t + Cfg::CV_THREADS * k;
+                    // 16-byte unit idx lies in key row (idx mod (64 rows x 8 units)) / 8
+                    // of its panel: rows at or past L become zeros (P is 0 there, and
+                    // 0 x a non-finite stale value would still reach O)
+                    const int key = j * BN + ((idx % (Cfg::KV_PANEL / 16)) >> 3);
+                    uint4 w = vt[idx];
+                    if (key >= L) {
+                        w = make_uint4(0u, 0u, 0u, 0u);
+                    } else {
+                        w.x = bf16x2_to_f16x2(w.x);
+                        w.y = bf16x2_to_f16x2(w.y);
+                        w.z = bf16x2_to_f16x2(w.z);
+                        w.w = bf16x2_to_f16x2(w.w);
+                    }
+                    vt[idx] = w;
                 }
                 // the re-encoded V is read next by the tensor cores (async proxy)
                 fence_proxy_async_smem();

@@ -145,31 +145,46 @@ bool valid_scale(float scale) { return std::isfinite(scale) && scale >= 0.f; }
 // The tcgen05 forward.  STATS: the backward's pre-pass instead of o and lse,
 // per row (log2e lse, c, dO.vbar, dO.o + c dO.vbar) into `stats` from dL/do
 // rows `dout` (out is then unused and must be nullptr).
+// The cached mode: Tq query rows per head (q, rho, out, lse are [BH][Tq]),
+// K/V from a cache of N rows per head, query row i at position
+// seqlens[b] - Tq + i.  Tq = 0 and seqlens = nullptr: the self-attention
+// prefill (Tq = N, query row i at position i).
+struct CachedQueries {
+    int Tq = 0;
+    const int32_t* seqlens = nullptr;
+    int H = 1;
+};
+
 template <int D, bool PLX, bool STATS = false>
 plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
                          int N, long long BH, float scale, plx_dtype out_dtype, cudaStream_t stream,
-                         int sm_count, const void* dout = nullptr, void* stats = nullptr, bool no_intercept = false) {
+                         int sm_count, const void* dout = nullptr, void* stats = nullptr, bool no_intercept = false,
+                         const CachedQueries& cq = CachedQueries()) {
     using Cfg = FwdTcCfg<D, PLX>;
-    const long long n_qt = (N + Cfg::BM - 1) / Cfg::BM;
+    const int Tq = cq.Tq > 0 ? cq.Tq : N;
+    const long long n_qt = (Tq + Cfg::BM - 1) / Cfg::BM;
     const long long n_items = BH * n_qt;
     if (n_items > INT_MAX || BH > INT_MAX) return PLX_ERR_UNSUPPORTED;
     CUtensorMap mq, mr, mk, mv, mo;
-    if (!make_map(&mq, q, D, N, BH, Cfg::BM) || !make_map(&mk, k, D, N, BH, Cfg::BN) ||
+    if (!make_map(&mq, q, D, Tq, BH, Cfg::BM) || !make_map(&mk, k, D, N, BH, Cfg::BN) ||
         !make_map(&mv, v, D, N, BH, Cfg::BN))
         return PLX_ERR_CUDA;
     // the statistics mode stores no o and never touches its output map
     if (STATS)
         mo = mq;
-    else if (!make_out_map(&mo, out, D, N, BH, out_dtype == PLX_F32))
+    else if (!make_out_map(&mo, out, D, Tq, BH, out_dtype == PLX_F32))
         return PLX_ERR_CUDA;
     if (PLX) {
-        if (!make_map(&mr, rho, D, N, BH, Cfg::BM)) return PLX_ERR_CUDA;
+        if (!make_map(&mr, rho, D, Tq, BH, Cfg::BM)) return PLX_ERR_CUDA;
     } else {
         mr = mq;
     }
     plx::FwdTcParams p;
     p.lse = lse;
     p.N = N;
+    p.Tq = Tq;
+    p.seqlens = cq.seqlens;
+    p.H = cq.H;
     p.BH = static_cast<int>(BH);
     p.n_qt = static_cast<int>(n_qt);
     p.n_items = static_cast<int>(n_items);
@@ -434,6 +449,39 @@ plx_status plx_fwd_family(const void* q, const void* k, const void* v, const voi
                           int B, int H, int N, int d, float scale, unsigned flags, plx_dtype out_dtype,
                           void* stream) {
     return fwd_impl(q, k, v, rho, out, lse, B, H, N, d, scale, flags, out_dtype, stream);
+}
+
+plx_status plx_fwd_cached(const void* q, const void* rho, const void* k_cache, const void* v_cache,
+                          const int32_t* seqlens, void* out, float* lse, int B, int H, int T, int S_cap, int d,
+                          float scale, plx_dtype out_dtype, void* stream) {
+    try {
+        if (!q || !k_cache || !v_cache || !seqlens || !out) return PLX_ERR_INVALID_ARG;
+        if (B < 1 || H < 1 || T < 1 || S_cap < T || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
+        if (out_dtype != PLX_BF16 && out_dtype != PLX_F32) return PLX_ERR_INVALID_ARG;
+        if (d != 128 && d != 64) return PLX_ERR_UNSUPPORTED;
+        if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+            (rho && !aligned(rho, 16)) || !aligned(seqlens, 4) || (lse && !aligned(lse, 4)))
+            return PLX_ERR_MISALIGNED;
+        const DeviceInfo* info = device_info();
+        if (!info) return PLX_ERR_CUDA;
+        const long long BH = static_cast<long long>(B) * H;
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        CachedQueries cq;
+        cq.Tq = T;
+        cq.seqlens = seqlens;
+        cq.H = H;
+        if (d == 128)
+            return rho ? launch_fwd_tc<128, true>(q, k_cache, v_cache, rho, out, lse, S_cap, BH, scale, out_dtype, s,
+                                                  info->sm_count, nullptr, nullptr, false, cq)
+                       : launch_fwd_tc<128, false>(q, k_cache, v_cache, rho, out, lse, S_cap, BH, scale, out_dtype,
+                                                   s, info->sm_count, nullptr, nullptr, false, cq);
+        return rho ? launch_fwd_tc<64, true>(q, k_cache, v_cache, rho, out, lse, S_cap, BH, scale, out_dtype, s,
+                                             info->sm_count, nullptr, nullptr, false, cq)
+                   : launch_fwd_tc<64, false>(q, k_cache, v_cache, rho, out, lse, S_cap, BH, scale, out_dtype, s,
+                                              info->sm_count, nullptr, nullptr, false, cq);
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
 }
 
 plx_status plx_fwd_f32(const float* q, const float* k, const float* v, const float* rho, float* out, float* lse,

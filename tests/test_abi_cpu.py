@@ -182,3 +182,16 @@ def test_decode_paged_rejects_bad_arguments_before_launch():
     assert lib.plx_decode_paged(*args(T, 64, 0, 8)) == 1               # no blocks per sequence
     assert lib.plx_decode_paged(*args(T, 64, 4, 0)) == 1               # empty cache
     assert lib.plx_decode_paged(*args(ctypes.c_void_p(0x40002), 64, 4, 8)) == 3   # misaligned table
+
+
+def test_fwd_cached_rejects_bad_arguments_before_launch():
+    lib = plx.library()
+    P = P16
+    SL = ctypes.c_void_p(0x30000)
+    F32 = 1
+    assert lib.plx_fwd_cached(P, P, P, P, None, P, P, 1, 2, 16, 64, 128, 0.1, F32, None) == 1   # no seqlens
+    assert lib.plx_fwd_cached(P, P, P, P, SL, P, P, 1, 2, 65, 64, 128, 0.1, F32, None) == 1     # T > S_cap
+    assert lib.plx_fwd_cached(P, P, P, P, SL, P, P, 1, 2, 0, 64, 128, 0.1, F32, None) == 1      # T < 1
+    assert lib.plx_fwd_cached(P, P, P, P, SL, P, P, 1, 2, 16, 64, 96, 0.1, F32, None) == 2      # head dim
+    assert lib.plx_fwd_cached(P, P, P, P, ctypes.c_void_p(0x30002), P, P, 1, 2, 16, 64, 128, 0.1, F32,
+                              None) == 3                                                        # misaligned seqlens
