@@ -639,6 +639,73 @@ def run_backward_bench(args, world, rank, local):
     return 0
 
 
+def run_cached_bench(args, world, rank, local):
+    """plx_fwd_cached (T new tokens per sequence on the tensor cores) on the
+    decode workload's cache (B=64, H=16, every length 4096, d=128), for T in
+    (1, 16, 64, 128), beside plx_decode on the same cache.  The cache is read
+    once per (b, h) whatever T is, so the roofline is HBM bandwidth over the
+    K/V bytes; tokens/s = B * T / time.  L2 is flushed before every launch.
+    Prints one JSON line."""
+    import torch
+    import parameterized_local_linear_02_b300 as plx
+    import plx_inputs
+
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    dc = plx_inputs.CONFIGS[DECODE]
+    B, H, d, S = dc["B"], dc["H"], dc["d"], dc["S_cap"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(dc["seed"])
+    kc = torch.randn((B, H, S, d), generator=g, device=dev).to(torch.bfloat16)
+    vc = torch.randn((B, H, S, d), generator=g, device=dev).to(torch.bfloat16)
+    seqlens = torch.full((B,), S, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    peaks = read_peaks()
+
+    def timed(fn, steps):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        return float(np.median(ms))
+
+    kv_bytes = B * H * S * d * 2 * 2
+    q1 = torch.randn((B, H, d), generator=g, device=dev).to(torch.bfloat16)
+    r1 = (0.1 * torch.randn((B, H, d), generator=g, device=dev)).to(torch.bfloat16)
+    dec_ms = timed(lambda: plx.plx_decode(q1, r1, kc, vc, seqlens), max(3, args.steps))
+    rows = []
+    for T in (1, 16, 64, 128):
+        q = torch.randn((B, H, T, d), generator=g, device=dev).to(torch.bfloat16)
+        r = (0.1 * torch.randn((B, H, T, d), generator=g, device=dev)).to(torch.bfloat16)
+        out = torch.empty((B, H, T, d), dtype=torch.bfloat16, device=dev)
+        ms = timed(lambda: plx.plx_fwd_cached(q, r, kc, vc, seqlens, out=out, with_lse=False), max(3, args.steps))
+        gbs = kv_bytes / (ms * 1e-3) / 1e9
+        rows.append({"T": T, "ms": ms, "kv_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+                     "tokens_per_s": B * T / (ms * 1e-3), "vs_T_decode_calls": T * dec_ms / ms})
+    line = {"metric": "PLX multi-token decode against a KV cache (plx_fwd_cached), K/V GB/s and tokens/s, 1 GPU",
+            "unit": "GB/s", "value": rows[1]["kv_gbs"], "n_gpus": 1, "steps": max(3, args.steps),
+            "warmup": max(3, args.warmup), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": DECODE, "B": B, "H": H, "S": S, "d": d, "value_at_T": 16,
+                       "l2": "flushed (256 MiB write) before every launch"},
+            "roofline": {"bound": "hbm", "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "peak_source": f"{peaks['source']} HBM copy"},
+            "plx_decode_ms": dec_ms, "plx_decode_kv_gbs": kv_bytes / (dec_ms * 1e-3) / 1e9, "by_T": rows,
+            "gpu_launches": (4 + 1) * max(3, args.steps), "device_status": plx.plx_last_device_error()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -655,7 +722,9 @@ def main():
                     help="time plx_decode over the batch x context sweep instead of the step")
     ap.add_argument("--sweep-iters", type=int, default=10)
     ap.add_argument("--backward", action="store_true",
-                    help="time plx_bwd_f32 on the prefill workload's shape instead of the step")
+                    help="time plx_bwd (and plx_bwd_f32) on the prefill workload's shape instead of the step")
+    ap.add_argument("--cached", action="store_true",
+                    help="time plx_fwd_cached (T new tokens per sequence) on the decode workload's cache")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the softmax-attention comparison and the end-to-end leg")
     args = ap.parse_args()
@@ -667,6 +736,8 @@ def main():
         return run_decode_sweep(args, world, rank, local)
     if args.backward:
         return run_backward_bench(args, world, rank, local)
+    if args.cached:
+        return run_cached_bench(args, world, rank, local)
     return run_ours(args, world, rank, local)
 
 
