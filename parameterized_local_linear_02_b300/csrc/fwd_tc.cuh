@@ -143,20 +143,21 @@ __device__ __forceinline__ void item_coords(int u, int BH, int n_qt, int& bh, in
 struct ItemSpan {
     int bh, q0, off, n_kv;
 };
+template <bool CACHED>
 __device__ __forceinline__ ItemSpan item_span(const FwdTcParams& p, int u, int BM, int BN, bool flag_bad = false) {
     ItemSpan it;
     int qt;
     item_coords(u, p.BH, p.n_qt, it.bh, qt);
     it.q0 = qt * BM;
     int L = p.N;
-    if (p.seqlens) {
+    if (CACHED) {
         L = p.seqlens[it.bh / p.H];
         if (L < p.Tq || L > p.N) {
             if (flag_bad) atomicOr(&g_plx_status, PLX_DEV_ERR_SEQLEN);
             L = L < p.Tq ? p.Tq : p.N;
         }
     }
-    it.off = L - p.Tq;
+    it.off = CACHED ? L - p.Tq : 0;       // the self-attention prefill: query row i is position i
     it.n_kv = (it.off + min(p.Tq, it.q0 + BM) + BN - 1) / BN;
     return it;
 }
@@ -165,7 +166,7 @@ __device__ __forceinline__ int snake_item(int r, int c, int G) {
     return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
-template <int D, bool PLX, bool STATS = false>
+template <int D, bool PLX, bool STATS = false, bool CACHED = false>
 __global__ void __launch_bounds__(FwdTcCfg<D, PLX>::THREADS, 1)
 plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapR,
                   const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
@@ -249,7 +250,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             for (int r = 0; ok; ++r) {
                 const int u = snake_item(r, c, G);
                 if (u >= p.n_items || *abort_flag) break;
-                const ItemSpan it = item_span(p, u, BM, BN, true);
+                const ItemSpan it = item_span<CACHED>(p, u, BM, BN, true);
                 const int bh = it.bh, q0 = it.q0, n_kv = it.n_kv;
                 const int un = snake_item(r + 1, c, G);    // this CTA's next item
                 if (nq > 0 && !mbar_wait(q_empty, (nq - 1) & 1)) { ok = false; break; }
@@ -331,7 +332,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             const int u = snake_item(r, c, G);
             // one read of the flag for the whole warp: every lane takes the same branch
             if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            const int n_kv = item_span(p, u, BM, BN).n_kv;
+            const int n_kv = item_span<CACHED>(p, u, BM, BN).n_kv;
             if (!wait_warp(q_full, items & 1)) { ok = false; break; }
             tc_fence_after();
             for (int j = 0; j < n_kv; ++j, ++g) {
@@ -532,7 +533,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         for (int r = 0; ok; ++r) {
             const int u = snake_item(r, c, G);
             if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            const ItemSpan it = item_span(p, u, BM, BN);
+            const ItemSpan it = item_span<CACHED>(p, u, BM, BN);
             const int q0 = it.q0, n_kv = it.n_kv;
             const int i = q0 + row;                 // this thread's query row
             const int pos = it.off + i;             // its position: keys 0 .. pos
@@ -634,9 +635,9 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 tmem_st32x32b_x16(tS + half * HALF, pk);
                 if constexpr (PLX) {
                     tmem_ld_wait(rraw);
-                    // masked keys contribute nothing, even where R is not finite
-                    // (cache rows past the sequence in the cached mode)
-                    if (diag) {
+                    // cached mode: masked keys contribute nothing, even where R is
+                    // not finite (cache rows past the sequence)
+                    if (CACHED && diag) {
 #pragma unroll
                         for (int cc = 0; cc < HALF; ++cc)
                             if (kbase + cc > pos) rraw[cc] = 0u;
@@ -716,30 +717,43 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         for (int r = 0; ok; ++r) {
             const int u = snake_item(r, c, G);
             if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            const ItemSpan it = item_span(p, u, BM, BN);
+            const ItemSpan it = item_span<CACHED>(p, u, BM, BN);
             const int n_kv = it.n_kv;
             const int L = it.off + p.Tq;          // keys at L and beyond are masked for every row
             for (int j = 0; j < n_kv; ++j, ++g) {
                 const int stage = g % NSTAGE;
                 if (!wait_warp(&v_full[stage], (g / NSTAGE) & 1)) { ok = false; break; }
                 uint4* vt = reinterpret_cast<uint4*>(sV + stage * Cfg::KV_BYTES);
+                if (!CACHED || (j + 1) * BN <= L) {
 #pragma unroll
-                for (int k = 0; k < Cfg::KV_BYTES / 16 / Cfg::CV_THREADS; ++k) {
-                    const int idx = t + Cfg::CV_THREADS * k;
-                    // 16-byte unit idx lies in key row (idx mod (64 rows x 8 units)) / 8
-                    // of its panel: rows at or past L become zeros (P is 0 there, and
-                    // 0 x a non-finite stale value would still reach O)
-                    const int key = j * BN + ((idx % (Cfg::KV_PANEL / 16)) >> 3);
-                    uint4 w = vt[idx];
-                    if (key >= L) {
-                        w = make_uint4(0u, 0u, 0u, 0u);
-                    } else {
+                    for (int k = 0; k < Cfg::KV_BYTES / 16 / Cfg::CV_THREADS; ++k) {
+                        uint4 w = vt[t + Cfg::CV_THREADS * k];
                         w.x = bf16x2_to_f16x2(w.x);
                         w.y = bf16x2_to_f16x2(w.y);
                         w.z = bf16x2_to_f16x2(w.z);
                         w.w = bf16x2_to_f16x2(w.w);
+                        vt[t + Cfg::CV_THREADS * k] = w;
                     }
-                    vt[idx] = w;
+                } else {
+                    // the item's last tile: 16-byte unit idx lies in key row
+                    // (idx mod (64 rows x 8 units)) / 8 of its panel, and rows at or
+                    // past L become zeros (P is 0 there, and 0 x a non-finite stale
+                    // value would still reach O)
+#pragma unroll 4
+                    for (int k = 0; k < Cfg::KV_BYTES / 16 / Cfg::CV_THREADS; ++k) {
+                        const int idx = t + Cfg::CV_THREADS * k;
+                        const int key = j * BN + ((idx % (Cfg::KV_PANEL / 16)) >> 3);
+                        uint4 w = vt[idx];
+                        if (key >= L) {
+                            w = make_uint4(0u, 0u, 0u, 0u);
+                        } else {
+                            w.x = bf16x2_to_f16x2(w.x);
+                            w.y = bf16x2_to_f16x2(w.y);
+                            w.z = bf16x2_to_f16x2(w.z);
+                            w.w = bf16x2_to_f16x2(w.w);
+                        }
+                        vt[idx] = w;
+                    }
                 }
                 // the re-encoded V is read next by the tensor cores (async proxy)
                 fence_proxy_async_smem();

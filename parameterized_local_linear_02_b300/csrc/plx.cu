@@ -61,6 +61,10 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, false>, FwdTcCfg<128, false>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, true>, FwdTcCfg<64, true>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, false>, FwdTcCfg<64, false>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, true, false, true>, FwdTcCfg<128, true>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, false, false, true>, FwdTcCfg<128, false>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, true, false, true>, FwdTcCfg<64, true>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, false, false, true>, FwdTcCfg<64, false>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, true, true>, FwdTcCfg<128, true>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, false, true>, FwdTcCfg<128, false>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, true, true>, FwdTcCfg<64, true>::SMEM);
@@ -194,7 +198,10 @@ plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void
     p.stats = static_cast<float4*>(stats);
     p.no_intercept = no_intercept ? 1 : 0;
     const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
-    plx::plx_fwd_tc_kernel<D, PLX, STATS><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
+    if (cq.seqlens)
+        plx::plx_fwd_tc_kernel<D, PLX, false, true><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
+    else
+        plx::plx_fwd_tc_kernel<D, PLX, STATS><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
     return launch_status();
 }
 
