@@ -538,10 +538,21 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             const int i = q0 + row;                 // this thread's query row
             const int pos = it.off + i;             // its position: keys 0 .. pos
             float m = -INFINITY, l = 0.f, C = 0.f;
+            // cached mode: a quadrant none of whose 32 rows is a query row (T < 128)
+            // stores nothing, so after the first tile (which runs the previous
+            // item's epilogue and the pair handshakes) it only keeps the barrier
+            // phases in step; the garbage left in its lanes stays in its own rows
+            const bool idle = CACHED && q0 + quad * 32 >= p.Tq;
             for (int j = 0; j < n_kv; ++j, ++g) {
                 const int b = g & 1;
                 if (!wait_warp(&s_full[b], (g >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
+                if (idle && j > 0) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[b]);
+                    continue;
+                }
                 const uint32_t tS = lane_addr + (b ? Cfg::TM_S1 : Cfg::TM_S0);
                 const uint32_t tR = lane_addr + (b ? Cfg::TM_R1 : Cfg::TM_R0);
                 // S now; R is loaded after the max is published, so its TMEM
