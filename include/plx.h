@@ -191,8 +191,9 @@ size_t plx_bwd_workspace_size(int B, int H, int N, int d);
  * (tcgen05, fp32 accumulation; ds, dr and the dv weights enter their GEMMs as
  * fp16, the streamed bf16 tiles they multiply re-encoded to fp16).  Same
  * formulas as plx_bwd_f32.  The forward's o and lse are not inputs: a
- * pre-pass (the forward kernel in a statistics mode) recomputes, per row,
- * log2e lse_i, c_i, a_i = dO_i.vbar_i and D_i = dO_i.o_i + c_i a_i.
+ * statistics pass recomputes, per row and with the weights the gradient
+ * passes use, log2e lse_i, c_i, a_i = dO_i.vbar_i = sum_j w_ij G_ij and
+ * D_i = dO_i.o_i + c_i a_i = (1 + 2 c_i) a_i - sum_j w_ij r_ij G_ij.
  *
  *   q, k, v, rho : bf16 [B][H][N][d], 16-byte aligned; rho may be NULL
  *                  (softmax attention; drho is then ignored).
@@ -203,8 +204,9 @@ size_t plx_bwd_workspace_size(int B, int H, int N, int d);
  *                  bytes (16 per row), 16-byte aligned, no initialisation.
  *   B, H, N >= 1; d in {64, 128}.  Inputs and the values ds, dr, wv must lie
  *   within the fp16 range.
- * Three launches on `stream`: the pre-pass, a pass over 128-query tiles (dq,
- * drho) and a pass over 128-key tiles (dk, dv).  No atomics: the result is
+ * Three launches on `stream`: the statistics pass and a pass over 128-query
+ * tiles (dq, drho), both over query tiles, then a pass over 128-key tiles
+ * (dk, dv).  No atomics: the result is
  * deterministic.
  * Errors: PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_MISALIGNED,
  * PLX_ERR_WORKSPACE, PLX_ERR_CUDA; device-side wait timeouts are reported by

@@ -19,6 +19,11 @@ Pins (tests/test_oracle_backward.py): central finite differences of the
 independent C oracle's explicit forward, the value-shift invariant
 sum_j dL/dv_j = sum_i dO_i, and the affinity of o in rho (dL/drho does not
 depend on rho; the other gradients are affine in it).
+
+``plx_backward_closed`` is a second, independent route for long sequences,
+where the explicit form's [N, N, d] intermediates do not fit: the gradients
+written out in closed form (the forward differentiated by hand, on dense
+N x N fp64 matrices with numpy), pinned against ``plx_backward``.
 """
 from __future__ import annotations
 
@@ -58,3 +63,40 @@ def plx_backward(q, k, v, rho, dout, scale):
                 outs[n][b, h] = grads[n].numpy()
             o_all[b, h] = o.detach().numpy()
     return (*outs, o_all)
+
+
+def plx_backward_closed(q, k, v, rho, dout, scale, heads=None):
+    """Gradients of L = sum(dout * o) in closed form, fp64 numpy, for the
+    listed (b, h) heads (all by default).  With s = scale q k^T, w = the causal
+    softmax of s, r = rho k^T, vbar = w v, c_i = sum_j w_ij r_ij,
+    o = (1 + c) vbar - (w o r) v, G = dO v^T, a_i = dO_i . vbar_i and
+    D_i = dO_i . o_i + c_i a_i:
+        dL/ds = w o ((1 + c - r) o G + a r - D),   dL/dr = w o (a - G),
+        dq = scale (dL/ds) k,  drho = (dL/dr) k,
+        dk = scale (dL/ds)^T q + (dL/dr)^T rho,  dv = (w o (1 + c - r))^T dO.
+    Returns {(b, h): (dq, dk, dv, drho)}."""
+    B, H, N, d = q.shape
+    heads = [(b, h) for b in range(B) for h in range(H)] if heads is None else heads
+    tril = np.tril(np.ones((N, N), dtype=bool))
+    res = {}
+    for b, h in heads:
+        Q, K, V, R, dO = (np.asarray(a[b, h], np.float64) for a in (q, k, v, rho, dout))
+        s = scale * (Q @ K.T)
+        s = np.where(tril, s, -np.inf)
+        w = np.exp(s - s.max(axis=1, keepdims=True))
+        w /= w.sum(axis=1, keepdims=True)
+        r = R @ K.T
+        vbar = w @ V
+        c = np.sum(w * r, axis=1, keepdims=True)
+        o = (1.0 + c) * vbar - (w * r) @ V
+        G = dO @ V.T
+        a = np.sum(dO * vbar, axis=1, keepdims=True)
+        D = np.sum(dO * o, axis=1, keepdims=True) + c * a
+        ds = w * ((1.0 + c - r) * G + a * r - D)
+        dr = w * (a - G)
+        dq = scale * (ds @ K)
+        drho = dr @ K
+        dk = scale * (ds.T @ Q) + dr.T @ R
+        dv = (w * (1.0 + c - r)).T @ dO
+        res[(b, h)] = (dq, dk, dv, drho)
+    return res

@@ -13,8 +13,10 @@
 //   dq_i = scale sum_j ds_ij k_j,   drho_i = sum_j dr_ij k_j,
 //   dk_j = scale sum_i ds_ij q_i + sum_i dr_ij rho_i,   dv_j = sum_i wv_ij dO_i,
 // with w_ij = 2^(scale log2e s_ij - log2e lse_i).  The row statistics
-// (log2e lse_i, c_i, a_i, D_i) come from a pre-pass: the forward kernel in its
-// statistics mode, which has O/l = vbar, C/l = c and o in hand at its epilogue.
+// (log2e lse_i, c_i, a_i, D_i) come from a third pass of the same template
+// (PASS = BWD_STATS): S, R and G per tile, and online fp32 row sums
+// c_i = sum w r, a_i = sum w G, e_i = sum w r G with D_i = (1 + 2 c_i) a_i - e_i,
+// so the statistics use exactly the weights the two gradient passes use.
 //
 // Two passes over the causal (i, j) tiles, one kernel template:
 //   dq pass  (PASS = BWD_DQ):  a CTA item is 128 query rows; Q, rho and dO of the
@@ -53,7 +55,7 @@
 
 namespace plx {
 
-enum { BWD_DQ = 0, BWD_DKV = 1 };
+enum { BWD_DQ = 0, BWD_DKV = 1, BWD_STATS = 2 };
 
 template <int D, bool PLX, int PASS>
 struct BwdTcCfg {
@@ -69,26 +71,28 @@ struct BwdTcCfg {
     static constexpr int STR_PANEL = COLS * 128;
     static constexpr int RES_TILE = NP * RES_PANEL;
     static constexpr int STR_TILE = NP * STR_PANEL;
-    // resident operands: dq -> Q, rho, dO (A of S, R, G); dkv -> K (A of S and R), V (A of G)
-    static constexpr int N_RES = PASS == BWD_DQ ? (PLX ? 3 : 2) : 2;
-    // streamed operands: dq -> K, V; dkv -> Q, rho, dO (+ the queries' statistics)
-    static constexpr int N_STR = PASS == BWD_DQ ? 2 : (PLX ? 3 : 2);
+    // resident operands: dq and statistics passes -> Q, rho, dO (A of S, R, G); dkv -> K (A of
+    // S and R), V (A of G)
+    static constexpr int N_RES = PASS != BWD_DKV ? (PLX ? 3 : 2) : 2;
+    // streamed operands: dq and statistics passes -> K, V; dkv -> Q, rho, dO (+ the queries'
+    // statistics)
+    static constexpr int N_STR = PASS != BWD_DKV ? 2 : (PLX ? 3 : 2);
     static constexpr int STATS_BYTES = PASS == BWD_DKV ? COLS * 16 : 0;
     static constexpr int STAGE_BYTES = N_STR * STR_TILE + (STATS_BYTES + 1023) / 1024 * 1024;
     // the streamed tiles the output GEMMs read (dq: K; dkv: Q, rho, dO), re-encoded in place
-    static constexpr int CONV_BYTES = PASS == BWD_DQ ? STR_TILE : N_STR * STR_TILE;
+    static constexpr int CONV_BYTES = PASS == BWD_DQ ? STR_TILE : PASS == BWD_DKV ? N_STR * STR_TILE : 0;
     // a stage is held until its step's output GEMMs finish, late in the step, so
     // the ring needs three stages for the load to run under a whole step
     // (the dkv pass at d = 128 has room for two)
-    static constexpr int NSTAGE = (D == 128) ? (PASS == BWD_DQ ? 3 : 2) : 4;
+    static constexpr int NSTAGE = (D == 128) ? (PASS != BWD_DKV ? 3 : 2) : 4;
     static constexpr int STG_SLOT_BYTES = 32 * 128;   // per elementwise warp: 32 rows x 32 fp32
     static constexpr int OFF_RES = 0;
     static constexpr int OFF_STR = OFF_RES + N_RES * RES_TILE;
     static constexpr int OFF_STG = OFF_STR + NSTAGE * STAGE_BYTES;
     static constexpr int OFF_BAR = OFF_STG + EW_WARPS * STG_SLOT_BYTES;
     // res_full, res_empty, str_full[NSTAGE], str_empty[NSTAGE], srg_stage[NSTAGE], conv_done[NSTAGE],
-    // srg_full, srg_free, ab_full, out_done, drain
-    static constexpr int NBARS = 2 + 4 * NSTAGE + 5;
+    // srg_full, srg_free, ab_full, out_done, drain, pair[4] (statistics pass)
+    static constexpr int NBARS = 2 + 4 * NSTAGE + 5 + 4;
     static constexpr int SMEM_USED = OFF_BAR + NBARS * 8 + 16;
     static constexpr int SMEM = SMEM_USED + 1024;
     static constexpr uint32_t TM_S = 0, TM_R = 64, TM_G = 128, TM_DS = 192, TM_DR = 224, TM_ACC0 = 256,
@@ -98,10 +102,13 @@ struct BwdTcCfg {
     static_assert(STAGE_BYTES % 1024 == 0 && OFF_STR % 1024 == 0 && OFF_STG % 1024 == 0, "1024-byte tiles");
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert((CONV_BYTES / 16) % CV_THREADS == 0, "re-encode splits evenly over its threads");
+    // statistics pass: the pair merge of (m, l, C, A, E) per row, in the idle staging area
+    static_assert(2 * 2 * ROWS * 5 * 4 <= EW_WARPS * STG_SLOT_BYTES, "merge area");
 };
 
 struct BwdTcParams {
     const float4* stats;   // per row (log2e lse, c, a, D), [BH][N]  (dq pass: read per row)
+    float4* stats_out;     // the statistics pass writes them here
     int N;
     int BH;
     int n_rt;              // 128-row tiles per head
@@ -120,6 +127,8 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
     using Cfg = BwdTcCfg<D, PLX, PASS>;
     constexpr int ROWS = Cfg::ROWS, COLS = Cfg::COLS, NP = Cfg::NP, NSTAGE = Cfg::NSTAGE, HALF = Cfg::HALF;
     constexpr bool DQ = PASS == BWD_DQ;
+    constexpr bool ST = PASS == BWD_STATS;
+    constexpr bool QROWS = PASS != BWD_DKV;     // items are query tiles
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sRes = smem + Cfg::OFF_RES;
@@ -136,7 +145,8 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
     uint64_t* ab_full = srg_free + 1;          // ds/dr/wv of the current step are in TMEM
     uint64_t* out_done = ab_full + 1;          // the output GEMMs of the step have completed
     uint64_t* drain = out_done + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* pair_bar = drain + 1;            // statistics pass: the two warps of a lane quadrant
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pair_bar + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -160,6 +170,7 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
         mbar_init(ab_full, Cfg::EW_WARPS);
         mbar_init(out_done, 1);
         mbar_init(drain, 1);
+        for (int qd = 0; qd < 4; ++qd) mbar_init(&pair_bar[qd], 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -177,9 +188,9 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
     auto item = [&](int u, int& bh, int& r0, int& n_steps, int& s0) {
         const int t = u / p.BH;
         bh = u % p.BH;
-        const int rt = DQ ? p.n_rt - 1 - t : t;
+        const int rt = QROWS ? p.n_rt - 1 - t : t;
         r0 = rt * ROWS;
-        if (DQ) {
+        if (QROWS) {
             s0 = 0;                                                  // keys 0 .. min(N, r0 + 128) - 1
             n_steps = (min(p.N, r0 + ROWS) + COLS - 1) / COLS;
         } else {
@@ -222,7 +233,8 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
                             tma_load_3d(base + 2 * Cfg::STR_TILE + pn * Cfg::STR_PANEL, &mapStr2, &str_full[st],
                                         pn * 64, y, bh);
                     }
-                    if (!DQ) tma_load_3d(base + Cfg::N_STR * Cfg::STR_TILE, &mapStats, &str_full[st], 0, y, bh);
+                    if (PASS == BWD_DKV)
+                        tma_load_3d(base + Cfg::N_STR * Cfg::STR_TILE, &mapStats, &str_full[st], 0, y, bh);
                     ++nstr;
                 }
             }
@@ -296,7 +308,15 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
                 if (g > 0 && !wait_warp(srg_free, (g - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t base = sStrA + st * Cfg::STAGE_BYTES;
-                if (DQ) {
+                if (ST) {
+                    // the statistics pass: S, R, G only; the stage's one reader is done with them
+                    gemm_rs(tmem + Cfg::TM_S, sResA, base);
+                    if (PLX) gemm_rs(tmem + Cfg::TM_R, sResA + Cfg::RES_TILE, base);
+                    gemm_rs(tmem + Cfg::TM_G, sResA + (Cfg::N_RES - 1) * Cfg::RES_TILE, base + Cfg::STR_TILE);
+                    mma_commit_warp(srg_full);
+                    mma_commit_warp(&str_empty[st]);
+                    if (t == n_steps - 1) mma_commit_warp(res_empty);
+                } else if (DQ) {
                     gemm_rs(tmem + Cfg::TM_S, sResA, base);                                    // S = Q K^T
                     if (PLX) gemm_rs(tmem + Cfg::TM_R, sResA + Cfg::RES_TILE, base);           // R = rho K^T
                     gemm_rs(tmem + Cfg::TM_G, sResA + (Cfg::N_RES - 1) * Cfg::RES_TILE, base + Cfg::STR_TILE);  // G = dO V^T
@@ -333,7 +353,7 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
             ++nres;
         }
         // the output GEMMs of the last step
-        if (ok && g > 0) {
+        if (ok && g > 0 && !ST) {
             if (DQ) {
                 ok = out_gemms(g - 1, prev_first);
             } else if (!out_ready(g - 1)) {
@@ -365,7 +385,7 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
             return __all_sync(0xffffffffu, mbar_wait(bar, parity));
         };
         int g = 0;
-        bool ok = true;
+        bool ok = !ST;          // the statistics pass has no output GEMMs: nothing to re-encode
         for (int r = 0; ok; ++r) {
             const int u = snake_item(r, c, G);
             if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
@@ -392,6 +412,105 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&conv_done[st]);
             }
+        }
+        if (!ok && !ST) fail();
+    } else if (ST) {
+        // ===================================================== statistics (warps 2..9)
+        // Per query row, with the weights the other passes use, w_ij = 2^(scale
+        // log2e s_ij - log2e lse_i):  c_i = sum_j w_ij r_ij,  a_i = sum_j w_ij G_ij
+        // (= dO_i . vbar_i),  e_i = sum_j w_ij r_ij G_ij,  and
+        // D_i = sum_j w_ij ((1 + c_i - r_ij) G_ij + a_i r_ij) = (1 + 2 c_i) a_i - e_i.
+        // Each warp keeps an online state (m, l, C, A, E) over its 32 keys of every
+        // tile in fp32.  No rounded weights: the statistics must match the weights
+        // of the dq and dkv passes, or D_i - sum_j w_ij (...) no longer cancels.
+        // The pair merges its two states once per item.
+        const int ew = warp - 2;
+        const int quad = warp & 3;
+        const int half = ew >> 2;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        float* xs = reinterpret_cast<float*>(smem + Cfg::OFF_STG);   // [2 items][2 halves][5][ROWS]
+        auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+        };
+        int g = 0, items = 0;
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+            const int u = snake_item(r, c, G);
+            if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            int bh, r0, n_steps, s0;
+            item(u, bh, r0, n_steps, s0);
+            const int rw = r0 + row;
+            float m = -INFINITY, l = 0.f, C = 0.f, A = 0.f, E = 0.f;
+            for (int t = 0; t < n_steps; ++t, ++g) {
+                if (!wait_warp(srg_full, g & 1)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t sraw[HALF], rraw[HALF], graw[HALF];
+                tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_S + half * HALF, sraw);
+                if constexpr (PLX) tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_R + half * HALF, rraw);
+                tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_G + half * HALF, graw);
+                tmem_ld_wait(sraw);
+                if constexpr (PLX) tmem_ld_wait(rraw);
+                tmem_ld_wait(graw);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(srg_free);
+                const int cbase = s0 + t * COLS + half * HALF;
+                float tl[HALF];
+                float mloc = -INFINITY;
+#pragma unroll
+                for (int cc = 0; cc < HALF; ++cc) {
+                    tl[cc] = cbase + cc <= rw ? __uint_as_float(sraw[cc]) * p.scale_log2 : -INFINITY;
+                    mloc = fmaxf(mloc, tl[cc]);
+                }
+                if (mloc == -INFINITY) continue;          // every key of this warp masked
+                if (mloc > m) {
+                    const float f = fast_exp2(m - mloc);  // 0 while m is still -inf
+                    l *= f;
+                    C *= f;
+                    A *= f;
+                    E *= f;
+                    m = mloc;
+                }
+#pragma unroll
+                for (int cc = 0; cc < HALF; ++cc) {
+                    const float pw = fast_exp2(tl[cc] - m);     // 0 where masked
+                    const float gg = __uint_as_float(graw[cc]);
+                    l += pw;
+                    A = fmaf(pw, gg, A);
+                    if constexpr (PLX) {
+                        const float pr = pw * __uint_as_float(rraw[cc]);
+                        C += pr;
+                        E = fmaf(pr, gg, E);
+                    }
+                }
+            }
+            if (!ok) break;
+            // merge the pair's states through shared memory (slots alternate by item,
+            // so a slot is rewritten only after the partner passed the next merge)
+            float* xe = xs + (items & 1) * (2 * 5 * ROWS);
+            float* mine = xe + half * 5 * ROWS;
+            mine[0 * ROWS + row] = m;
+            mine[1 * ROWS + row] = l;
+            mine[2 * ROWS + row] = C;
+            mine[3 * ROWS + row] = A;
+            mine[4 * ROWS + row] = E;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pair_bar[quad]);
+            if (!wait_warp(&pair_bar[quad], items & 1)) { ok = false; break; }
+            const float* other = xe + (1 - half) * 5 * ROWS;
+            const float mo = other[row];
+            const float M = fmaxf(m, mo);
+            const float f0 = m == -INFINITY ? 0.f : fast_exp2(m - M);
+            const float f1 = mo == -INFINITY ? 0.f : fast_exp2(mo - M);
+            const float L = l * f0 + other[1 * ROWS + row] * f1;
+            const float ci = (C * f0 + other[2 * ROWS + row] * f1) / L;
+            const float ai = (A * f0 + other[3 * ROWS + row] * f1) / L;
+            const float ei = (E * f0 + other[4 * ROWS + row] * f1) / L;
+            if (half == 0 && rw < p.N)
+                p.stats_out[static_cast<size_t>(bh) * p.N + rw] =
+                    make_float4(M + __log2f(L), ci, ai, fmaf(2.f * ci, ai, ai) - ei);
+            ++items;
         }
         if (!ok) fail();
     } else {

@@ -107,10 +107,6 @@ struct FwdTcCfg {
 
 struct FwdTcParams {
     float* lse;
-    // statistics mode (the backward's pre-pass): dL/do rows in, per-row
-    // (log2e lse, c, dO.vbar, dO.o + c dO.vbar) out instead of o
-    const __nv_bfloat16* dout;
-    float4* stats;
     int N;                 // K/V rows per head (the cache capacity in the cached mode)
     int Tq;                // query rows per head (N for the self-attention prefill)
     // cached mode: queries are the last Tq positions of a cache of seqlens[b]
@@ -166,7 +162,7 @@ __device__ __forceinline__ int snake_item(int r, int c, int G) {
     return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
-template <int D, bool PLX, bool STATS = false, bool CACHED = false>
+template <int D, bool PLX, bool CACHED = false>
 __global__ void __launch_bounds__(FwdTcCfg<D, PLX>::THREADS, 1)
 plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapR,
                   const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
@@ -416,49 +412,6 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             const float l_all = e0.x + e1.x, C_all = e0.y + e1.y;
             const float inv_l = 1.f / l_all;
             const float cc_ = C_all * inv_l;
-            if constexpr (STATS) {
-                // dO_i . vbar_i and dO_i . o_i over this warp's half of the columns,
-                // then summed across the pair through shared memory
-                const int ei = eq0 + row;
-                const bool live = ei < p.Tq;
-                const __nv_bfloat16* drow = p.dout + (static_cast<size_t>(ebh) * p.Tq + (live ? ei : 0)) * D;
-                float pa = 0.f, pd = 0.f;
-#pragma unroll 1
-                for (int ch = 0; ch < Cfg::NCH; ++ch) {
-                    const int col = half * (D / 2) + 32 * ch;
-                    uint32_t ov[32];
-                    uint32_t uv[PLX ? 32 : 1];
-                    tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_O + col, ov);
-                    if constexpr (PLX) tmem_ld32x32b_x32_nowait(lane_addr + Cfg::TM_U + col, uv);
-                    uint4 dw[4];
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        dw[q4] = live ? reinterpret_cast<const uint4*>(drow + col)[q4] : make_uint4(0u, 0u, 0u, 0u);
-                    tmem_ld_wait(ov);
-                    if constexpr (PLX) tmem_ld_wait(uv);
-#pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) {
-                        const uint32_t w2 = (&dw[cc / 8].x)[(cc / 2) % 4];
-                        const float dov = (cc & 1) ? bf16x2_hi(w2) : bf16x2_lo(w2);
-                        const float vbar = __uint_as_float(ov[cc]) * inv_l;
-                        float o = vbar;
-                        if constexpr (PLX) o = fmaf(cc_, vbar, vbar) - __uint_as_float(uv[cc]) * inv_l;
-                        pa = fmaf(dov, vbar, pa);
-                        pd = fmaf(dov, o, pd);
-                    }
-                }
-                // the staging slots are idle in this mode: the pair's partial sums go there
-                float2* xab = reinterpret_cast<float2*>(smem + Cfg::OFF_STG);
-                xab[half * BM + row] = make_float2(pa, pd);
-                pair_arrive();
-                if (!pair_wait()) return false;
-                const float2 s0 = xab[row], s1 = xab[BM + row];
-                const float a = s0.x + s1.x, dd = s0.y + s1.y;
-                const float c = PLX ? cc_ : 0.f;
-                if (live && half == 0)
-                    p.stats[static_cast<size_t>(ebh) * p.Tq + ei] = make_float4(em + __log2f(l_all), c, a, fmaf(c, a, dd));
-                return true;
-            }
             // 0 * o is NaN exactly when o is not finite: one running sum flags them all
             float bad = 0.f;
 #pragma unroll 1

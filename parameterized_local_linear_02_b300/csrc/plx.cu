@@ -61,14 +61,14 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, false>, FwdTcCfg<128, false>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, true>, FwdTcCfg<64, true>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, false>, FwdTcCfg<64, false>::SMEM);
-    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, true, false, true>, FwdTcCfg<128, true>::SMEM);
-    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, false, false, true>, FwdTcCfg<128, false>::SMEM);
-    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, true, false, true>, FwdTcCfg<64, true>::SMEM);
-    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, false, false, true>, FwdTcCfg<64, false>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, true, true>, FwdTcCfg<128, true>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, false, true>, FwdTcCfg<128, false>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, true, true>, FwdTcCfg<64, true>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, false, true>, FwdTcCfg<64, false>::SMEM);
+    e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, true, plx::BWD_STATS>, BwdTcCfg<128, true, plx::BWD_STATS>::SMEM);
+    e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, false, plx::BWD_STATS>, BwdTcCfg<128, false, plx::BWD_STATS>::SMEM);
+    e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, true, plx::BWD_STATS>, BwdTcCfg<64, true, plx::BWD_STATS>::SMEM);
+    e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, false, plx::BWD_STATS>, BwdTcCfg<64, false, plx::BWD_STATS>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, true, plx::BWD_DQ>, BwdTcCfg<128, true, plx::BWD_DQ>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, false, plx::BWD_DQ>, BwdTcCfg<128, false, plx::BWD_DQ>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, true, plx::BWD_DKV>, BwdTcCfg<128, true, plx::BWD_DKV>::SMEM);
@@ -146,10 +146,7 @@ plx_status launch_status() {
 
 bool valid_scale(float scale) { return std::isfinite(scale) && scale >= 0.f; }
 
-// The tcgen05 forward.  STATS: the backward's pre-pass instead of o and lse,
-// per row (log2e lse, c, dO.vbar, dO.o + c dO.vbar) into `stats` from dL/do
-// rows `dout` (out is then unused and must be nullptr).
-// The cached mode: Tq query rows per head (q, rho, out, lse are [BH][Tq]),
+// The cached mode of the tcgen05 forward: Tq query rows per head (q, rho, out, lse are [BH][Tq]),
 // K/V from a cache of N rows per head, query row i at position
 // seqlens[b] - Tq + i.  Tq = 0 and seqlens = nullptr: the self-attention
 // prefill (Tq = N, query row i at position i).
@@ -159,11 +156,11 @@ struct CachedQueries {
     int H = 1;
 };
 
-template <int D, bool PLX, bool STATS = false>
+// The tcgen05 forward: the self-attention prefill, or the cached mode.
+template <int D, bool PLX>
 plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
                          int N, long long BH, float scale, plx_dtype out_dtype, cudaStream_t stream,
-                         int sm_count, const void* dout = nullptr, void* stats = nullptr, bool no_intercept = false,
-                         const CachedQueries& cq = CachedQueries()) {
+                         int sm_count, bool no_intercept = false, const CachedQueries& cq = CachedQueries()) {
     using Cfg = FwdTcCfg<D, PLX>;
     const int Tq = cq.Tq > 0 ? cq.Tq : N;
     const long long n_qt = (Tq + Cfg::BM - 1) / Cfg::BM;
@@ -173,11 +170,7 @@ plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void
     if (!make_map(&mq, q, D, Tq, BH, Cfg::BM) || !make_map(&mk, k, D, N, BH, Cfg::BN) ||
         !make_map(&mv, v, D, N, BH, Cfg::BN))
         return PLX_ERR_CUDA;
-    // the statistics mode stores no o and never touches its output map
-    if (STATS)
-        mo = mq;
-    else if (!make_out_map(&mo, out, D, Tq, BH, out_dtype == PLX_F32))
-        return PLX_ERR_CUDA;
+    if (!make_out_map(&mo, out, D, Tq, BH, out_dtype == PLX_F32)) return PLX_ERR_CUDA;
     if (PLX) {
         if (!make_map(&mr, rho, D, Tq, BH, Cfg::BM)) return PLX_ERR_CUDA;
     } else {
@@ -194,14 +187,12 @@ plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void
     p.n_items = static_cast<int>(n_items);
     p.scale_log2 = scale * kLog2e;
     p.out_f32 = out_dtype == PLX_F32;
-    p.dout = static_cast<const __nv_bfloat16*>(dout);
-    p.stats = static_cast<float4*>(stats);
     p.no_intercept = no_intercept ? 1 : 0;
     const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
     if (cq.seqlens)
-        plx::plx_fwd_tc_kernel<D, PLX, false, true><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
+        plx::plx_fwd_tc_kernel<D, PLX, true><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
     else
-        plx::plx_fwd_tc_kernel<D, PLX, STATS><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
+        plx::plx_fwd_tc_kernel<D, PLX, false><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
     return launch_status();
 }
 
@@ -230,17 +221,15 @@ template <int D, bool PLX>
 plx_status launch_bwd_tc(const void* q, const void* k, const void* v, const void* rho, const void* dout, float* dq,
                          float* dk, float* dv, float* drho, void* workspace, int N, long long BH, float scale,
                          cudaStream_t s, int sm_count) {
+    using CfgS = BwdTcCfg<D, PLX, plx::BWD_STATS>;
     using CfgQ = BwdTcCfg<D, PLX, plx::BWD_DQ>;
     using CfgK = BwdTcCfg<D, PLX, plx::BWD_DKV>;
     auto* stats = static_cast<float4*>(workspace);
-    plx_status st = launch_fwd_tc<D, PLX, true>(q, k, v, rho, nullptr, nullptr, N, BH, scale, PLX_F32, s, sm_count,
-                                                dout, stats);
-    if (st != PLX_OK) return st;
-
     const long long n_rt = (N + 127) / 128;
     if (BH * n_rt > INT_MAX) return PLX_ERR_UNSUPPORTED;
     plx::BwdTcParams p;
     p.stats = stats;
+    p.stats_out = stats;
     p.N = N;
     p.BH = static_cast<int>(BH);
     p.n_rt = static_cast<int>(n_rt);
@@ -267,6 +256,10 @@ plx_status launch_bwd_tc(const void* q, const void* k, const void* v, const void
         m_dr = m_dq;
     }
     // unused slots get a valid map of the right kind
+    // the row statistics (lse, c, a, D) with the weights the two gradient passes use
+    plx::plx_bwd_tc_kernel<D, PLX, plx::BWD_STATS><<<grid, CfgS::THREADS, CfgS::SMEM, s>>>(
+        mq_r, PLX ? mr_r : mo_r, mo_r, mk_s, mv_s, mv_s, mstat, m_dq, m_dr, p);
+    if (cudaGetLastError() != cudaSuccess) return PLX_ERR_CUDA;
     plx::plx_bwd_tc_kernel<D, PLX, plx::BWD_DQ><<<grid, CfgQ::THREADS, CfgQ::SMEM, s>>>(
         mq_r, PLX ? mr_r : mo_r, mo_r, mk_s, mv_s, mv_s, mstat, m_dq, m_dr, p);
     if (cudaGetLastError() != cudaSuccess) return PLX_ERR_CUDA;
@@ -432,11 +425,11 @@ plx_status fwd_impl(const void* q, const void* k, const void* v, const void* rho
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         if (d == 128)
             return rho ? launch_fwd_tc<128, true>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count,
-                                                  nullptr, nullptr, noint)
+                                                  noint)
                        : launch_fwd_tc<128, false>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s,
                                                    info->sm_count);
         return rho ? launch_fwd_tc<64, true>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count,
-                                             nullptr, nullptr, noint)
+                                             noint)
                    : launch_fwd_tc<64, false>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count);
     } catch (...) {
         return PLX_ERR_CUDA;
@@ -479,13 +472,13 @@ plx_status plx_fwd_cached(const void* q, const void* rho, const void* k_cache, c
         cq.H = H;
         if (d == 128)
             return rho ? launch_fwd_tc<128, true>(q, k_cache, v_cache, rho, out, lse, S_cap, BH, scale, out_dtype, s,
-                                                  info->sm_count, nullptr, nullptr, false, cq)
+                                                  info->sm_count, false, cq)
                        : launch_fwd_tc<128, false>(q, k_cache, v_cache, rho, out, lse, S_cap, BH, scale, out_dtype,
-                                                   s, info->sm_count, nullptr, nullptr, false, cq);
+                                                   s, info->sm_count, false, cq);
         return rho ? launch_fwd_tc<64, true>(q, k_cache, v_cache, rho, out, lse, S_cap, BH, scale, out_dtype, s,
-                                             info->sm_count, nullptr, nullptr, false, cq)
+                                             info->sm_count, false, cq)
                    : launch_fwd_tc<64, false>(q, k_cache, v_cache, rho, out, lse, S_cap, BH, scale, out_dtype, s,
-                                              info->sm_count, nullptr, nullptr, false, cq);
+                                              info->sm_count, false, cq);
     } catch (...) {
         return PLX_ERR_CUDA;
     }

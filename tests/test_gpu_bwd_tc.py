@@ -84,3 +84,23 @@ def test_bwd_tc_several_items_ragged(shape):
     got = run_bwd(x, dout)
     ref = plx_backward(x.q, x.k, x.v, x.rho, dout, x.scale)[:4]
     check(got, ref, ("dq", "dk", "dv", "drho"), f"{shape}")
+
+
+def test_bwd_tc_full_size_sampled_heads():
+    """The bench's backward workload (B=4, H=16, N=2048, d=128, rho = W_R x) in
+    the launch configuration the bench times (every head in one plx_bwd call);
+    three whole heads against the closed-form fp64 gradients."""
+    import torch
+    import parameterized_local_linear_02_b300 as plx
+    from oracle.backward import plx_backward_closed
+    pc = plx_inputs.CONFIGS["prefill_b4_h16_n2048_d128"]
+    B, H, N, d = pc["B"], pc["H"], pc["N"], pc["d"]
+    x = plx_inputs.prefill(B, H, N, d, seed=pc["seed"], dtype="bf16", rho=pc["rho"], keys=pc["keys"])
+    dout = _bf16_round(np.random.default_rng(2048).standard_normal((B, H, N, d)).astype(np.float32))
+    got = run_bwd(x, dout)
+    heads = [(0, 0), (1, 7), (3, 15)]
+    ref = plx_backward_closed(x.q, x.k, x.v, x.rho, dout, x.scale, heads=heads)
+    for (b, h), grads in ref.items():
+        for name, g, r in zip(("dq", "dk", "dv", "drho"), got, grads):
+            mx, mn = assert_bf16(g[b, h], r, f"full size ({b}, {h}) {name}")
+            print(f"full size ({b}, {h}) {name}: max {mx:.2e} mean {mn:.2e}")
