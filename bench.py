@@ -549,8 +549,8 @@ def run_backward_bench(args, world, rank, local):
     """plx_bwd (tensor cores, bf16 inputs) on the prefill workload's shape
     (B=4, H=16, N=2048, d=128) with a seeded bf16 dL/do.  TFLOP/s counts 14 d
     flop per causal pair: S, R and dO V^T once (3 x 2d), dq, drho (2 x 2d),
-    dk (4d), dv (2d); the implementation runs 30 d (the statistics pre-pass is
-    a forward, 8d, and S, R, G are recomputed in each of its two passes).  The
+    dk (4d), dv (2d); the implementation runs 28 d (S, R, G in each of its three
+    passes: the row statistics, dq/drho, dk/dv).  The
     roofline is the measured dense bf16 tensor rate.  plx_bwd_f32 (CUDA
     cores) is timed beside it on the same values widened to fp32, with its o
     and lse from plx_fwd_f32 (not timed).  Prints one JSON line."""
@@ -599,9 +599,6 @@ def run_backward_bench(args, world, rank, local):
     sampler.start()
     med, nsteps = timed(call, max(3, args.steps), 0)
     clocks = sampler.stop()
-    # a PLX forward alone, the cost of the statistics pre-pass, for the breakdown
-    fwd_ms, _ = timed(lambda: plx.plx_fwd(tb["q"], tb["k"], tb["v"], tb["rho"], scale=x.scale,
-                                          out_dtype=torch.float32), 10, 3)
     # the fp32 path on the same values
     t32 = {n: tb[n].float() for n in ("q", "k", "v", "rho")}
     out32, lse32 = plx.plx_fwd_f32(t32["q"], t32["k"], t32["v"], t32["rho"], scale=x.scale)
@@ -622,14 +619,13 @@ def run_backward_bench(args, world, rank, local):
             "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": nsteps, "warmup": max(3, args.warmup),
             "ms_per_step": med, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": PREFILL, "B": B, "H": H, "N": N, "d": d, "causal": True, "rho": "W_R x",
-                       "inputs": "bf16 q, k, v, rho, dout (o and lse recomputed by the statistics pre-pass)",
+                       "inputs": "bf16 q, k, v, rho, dout (lse and the row statistics recomputed by the statistics pass)",
                        "l2": "flushed (256 MiB write) before every launch"},
             "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s", "frac": value / peak,
                          "peak_source": f"{peaks['source']} bf16 dense (burst)",
                          "frac_of_sustained": value / peak_s,
-                         "flop_per_launch": flops, "flop_per_pair": 14 * d, "implementation_flop_per_pair": 30 * d,
-                         "implementation_tflops": pairs * 30 * d / (med * 1e-3) / 1e12},
-            "breakdown_ms": {"plx_forward_alone": fwd_ms, "dq_and_dkv_passes_about": med - fwd_ms},
+                         "flop_per_launch": flops, "flop_per_pair": 14 * d, "implementation_flop_per_pair": 28 * d,
+                         "implementation_tflops": pairs * 28 * d / (med * 1e-3) / 1e12},
             "f32_path": {"ms": f32_ms, "value": flops / (f32_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                          "roofline": {"bound": "alu", "peak": alu_peak,
                                       "frac": flops / (f32_ms * 1e-3) / 1e12 / alu_peak}},
