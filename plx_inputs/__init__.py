@@ -42,6 +42,7 @@ import numpy as np
 __all__ = [
     "bf16_round", "bf16_bits_to_f32", "PrefillInputs", "DecodeInputs",
     "prefill", "decode", "decode_device", "ragged_seqlens", "CONFIGS",
+    "ProbeInputs", "probe",
 ]
 
 
@@ -233,6 +234,38 @@ def decode_device(B: int, H: int, d: int, S_cap: int, *, seed: int,
     out["seqlens_host"] = sl
     out["seqlens"] = torch.from_numpy(sl).to(device)
     return out
+
+
+@dataclass
+class ProbeInputs:
+    """Inputs of the probe projection: hidden states x [B, N, Dx] and the
+    probe weights W_R [H * d, Dx], both bf16-exact float32 values."""
+    B: int
+    N: int
+    H: int
+    d: int
+    Dx: int
+    x: np.ndarray
+    w_r: np.ndarray
+    bits: dict = field(default_factory=dict)
+
+    def device_tensors(self, device="cuda"):
+        import torch
+        return {name: torch.from_numpy(self.bits[name].view(np.int16)).view(torch.bfloat16).to(device).contiguous()
+                for name in ("x", "w_r")}
+
+
+def probe(B: int, N: int, H: int, d: int, Dx: int, *, seed: int, x_std: float = 1.0) -> ProbeInputs:
+    """Seeded probe-projection inputs: x ~ N(0, x_std^2) of shape [B, N, Dx]
+    and W_R ~ N(0, 1/Dx) of shape [H * d, Dx], each rounded once to bf16.
+    Only the draws; the product is the oracle's."""
+    rng = np.random.default_rng(seed)
+    x = _normal(rng, (B, N, Dx), x_std)
+    w = _normal(rng, (H * d, Dx), 1.0 / math.sqrt(Dx))
+    bits, vals = {}, {}
+    for name, arr in (("x", x), ("w_r", w)):
+        bits[name], vals[name] = bf16_round(arr)
+    return ProbeInputs(B, N, H, d, Dx, vals["x"], vals["w_r"], bits)
 
 
 # The five workloads of the benchmark/parity plan (sizes by what they are).
