@@ -702,6 +702,152 @@ def run_cached_bench(args, world, rank, local):
     return 0
 
 
+def run_proj_bench(args, world, rank, local):
+    """plx_probe_proj (tcgen05 GEMM rho = W_R x written in the [B, H, N, d]
+    layout) on the prefill workload's probe: x [4, 2048, 1024] bf16, W_R
+    [16 * 128, 1024] bf16.  flop = 2 B N (H d) Dx; the roofline is the
+    measured dense bf16 tensor rate.  For context, torch's matmul (cuBLAS) of
+    the same operands, alone and followed by the [B, N, H, d] -> [B, H, N, d]
+    copy the PLX kernels need.  L2 is flushed before every launch.  Prints
+    one JSON line."""
+    import torch
+    import parameterized_local_linear_02_b300 as plx
+
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    B, N, H, d, Dx = 4, 2048, 16, 128, 1024
+    g = torch.Generator(device=dev)
+    g.manual_seed(13)
+    x = torch.randn((B, N, Dx), generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn((H * d, Dx), generator=g, device=dev) / math.sqrt(Dx)).to(torch.bfloat16)
+    rho = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn, steps):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        return float(np.median(ms)), len(ms)
+
+    sampler = ClockSampler(local)
+    for _ in range(max(3, args.warmup)):
+        plx.plx_probe_proj(x, w, heads=H, out=rho)
+    torch.cuda.synchronize()
+    sampler.start()
+    med, nsteps = timed(lambda: plx.plx_probe_proj(x, w, heads=H, out=rho), max(3, args.steps))
+    clocks = sampler.stop()
+    y = torch.empty((B * N, H * d), dtype=torch.bfloat16, device=dev)
+    x2 = x.view(B * N, Dx)
+    mm_ms, _ = timed(lambda: torch.matmul(x2, w.t(), out=y), max(3, args.steps))
+    mmp_ms, _ = timed(lambda: rho.copy_(torch.matmul(x2, w.t(), out=y).view(B, N, H, d).permute(0, 2, 1, 3)),
+                      max(3, args.steps))
+    flops = 2.0 * B * N * H * d * Dx
+    value = flops / (med * 1e-3) / 1e12
+    peaks = read_peaks()
+    peak, peak_s = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
+    hbm_bytes = (B * N * Dx + H * d * Dx + B * H * N * d) * 2
+    line = {"metric": "probe projection rho = W_R x (plx_probe_proj) TFLOP/s, bf16 on the tensor cores, 1 GPU",
+            "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": nsteps, "warmup": max(3, args.warmup),
+            "ms_per_step": med, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "probe_proj_b4_n2048_dx1024_h16_d128", "B": B, "N": N, "Dx": Dx, "H": H, "d": d,
+                       "l2": "flushed (256 MiB write) before every launch"},
+            "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s", "frac": value / peak,
+                         "peak_source": f"{peaks['source']} bf16 dense (burst)", "frac_of_sustained": value / peak_s,
+                         "flop_per_launch": flops, "hbm_bytes_per_launch": hbm_bytes,
+                         "hbm_gbs_at_this_time": hbm_bytes / (med * 1e-3) / 1e9},
+            "torch_matmul_ms": mm_ms, "torch_matmul_tflops": flops / (mm_ms * 1e-3) / 1e12,
+            "torch_matmul_plus_head_transpose_ms": mmp_ms,
+            "gpu_launches": nsteps, "clocks": clocks, "device_status": plx.plx_last_device_error()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_lla_bench(args, world, rank, local):
+    """plx_lla_f32 (local linear attention, probe solved by fp32 conjugate
+    gradients) on the prefill workload's shape B=4, H=16, N=2048, d=128 with
+    fp32 q, k, v ~ N(0, 1), ridge lambda = 0.1, at most 48 steps per row,
+    relative tolerance 1e-4.  Work: each CG step of row i streams its i + 1
+    keys at 6 d flop per key (q.k, p.k, the update of Sigma p); the softmax
+    pass for kbar costs 4 d and the output pass 8 d per causal pair.  The
+    roofline is the fp32 FMA rate of the CUDA cores (SMs x 128 lanes x 2 flop
+    x the max SM clock).  L2 is flushed before every launch sequence.
+    Prints one JSON line."""
+    import torch
+    import parameterized_local_linear_02_b300 as plx
+
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    B, H, N, d = 4, 16, 2048, 128
+    lam, iters, tol = 0.1, 48, 1e-4
+    g = torch.Generator(device=dev)
+    g.manual_seed(17)
+    q, k, v = (torch.randn((B, H, N, d), generator=g, device=dev) for _ in range(3))
+    ws = torch.empty(plx.plx_lla_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    steps = torch.empty((B, H, N), dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        plx.plx_lla_f32(q, k, v, lam=lam, max_iters=iters, tol=tol, workspace=ws, out=out, lse=lse, steps=steps,
+                        with_rho=False)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    ms = []
+    for _ in range(max(3, args.steps)):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    clocks = sampler.stop()
+    med = float(np.median(ms))
+    st = steps.double()
+    keys = torch.arange(1, N + 1, device=dev, dtype=torch.float64)
+    cg_flops = float((st * keys).sum()) * 6 * d
+    pairs = B * H * N * (N + 1) / 2
+    flops = cg_flops + pairs * 12 * d
+    value = flops / (med * 1e-3) / 1e12
+    props = torch.cuda.get_device_properties(dev)
+    sm_max = clocks.get("sm_max_mhz") or 2032.0
+    alu_peak = props.multi_processor_count * 128 * 2 * sm_max * 1e6 / 1e12
+    line = {"metric": "LLA (probe solved by fp32 CG) TFLOP/s on the CUDA cores, 1 GPU",
+            "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": len(ms), "warmup": max(3, args.warmup),
+            "ms_per_step": med, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "lla_b4_h16_n2048_d128", "B": B, "H": H, "N": N, "d": d, "lambda": lam,
+                       "max_iters": iters, "tol": tol, "l2": "flushed (256 MiB write) before every launch sequence"},
+            "cg_steps": {"max": int(steps.max()), "mean": float(st.mean()),
+                         "rows_at_max": int((steps == iters).sum()), "rows": B * H * N},
+            "roofline": {"bound": "alu", "achieved": value, "peak": alu_peak, "unit": "TFLOP/s",
+                         "frac": value / alu_peak,
+                         "peak_source": f"{props.multi_processor_count} SMs x 128 fp32 lanes x 2 flop x {sm_max:.0f} MHz",
+                         "flop_per_launch_sequence": flops, "cg_flop": cg_flops},
+            "gpu_launches": (iters + 3) * len(ms), "clocks": clocks, "device_status": plx.plx_last_device_error()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -721,6 +867,10 @@ def main():
                     help="time plx_bwd (and plx_bwd_f32) on the prefill workload's shape instead of the step")
     ap.add_argument("--cached", action="store_true",
                     help="time plx_fwd_cached (T new tokens per sequence) on the decode workload's cache")
+    ap.add_argument("--proj", action="store_true",
+                    help="time plx_probe_proj (rho = W_R x) on the prefill workload's probe")
+    ap.add_argument("--lla", action="store_true",
+                    help="time plx_lla_f32 (local linear attention, CG-solved probe) on the prefill workload's shape")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the softmax-attention comparison and the end-to-end leg")
     args = ap.parse_args()
@@ -734,6 +884,10 @@ def main():
         return run_backward_bench(args, world, rank, local)
     if args.cached:
         return run_cached_bench(args, world, rank, local)
+    if args.proj:
+        return run_proj_bench(args, world, rank, local)
+    if args.lla:
+        return run_lla_bench(args, world, rank, local)
     return run_ours(args, world, rank, local)
 
 

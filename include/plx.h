@@ -322,6 +322,72 @@ plx_status plx_decode_noalloc(const void* q, const void* rho, const void* k_cach
                               float scale, int num_splits, plx_dtype out_dtype, void* stream);
 
 /*
+ * plx_lla_f32 -- local linear attention (LLA) with the solved probe, the
+ * method Parallax replaces ("Parallax: Parameterized Local Linear Attention
+ * for Language Modeling", zhichai.net section 1.2; gist.science "Enunciato
+ * del Problema"): each token's probe solves a ridge-regularised linear system
+ * by conjugate gradients, then Parallax's output formula uses it.  For query
+ * i of one head (causal prefix j <= i), with w_ij = softmax_j(scale q_i.k_j):
+ *
+ *   (Sigma_KK^(i) + lambda I) rho_i = mu_i,   mu_i = kbar_i - q_i
+ *   Sigma_KK^(i) = sum_j w_ij (k_j - kbar_i)(k_j - kbar_i)^T,  kbar_i = sum_j w_ij k_j
+ *   o_i = vbar_i - Sigma_KV^(i) rho_i
+ *
+ * (the intercept at k = q_i of the weighted ridge fit of v on k - q_i).
+ * Conjugate gradients start from rho = 0.  Each row runs at most max_iters
+ * steps and stops once |r|^2 <= tol^2 |mu|^2 (tol = 0 runs every step), or
+ * when p . Ap <= 0.  All arithmetic is fp32 on the CUDA cores.
+ *
+ *   q, k, v  : fp32 [B][H][N][d], 16-byte aligned.
+ *   out      : fp32 [B][H][N][d] output, 16-byte aligned.
+ *   rho_out  : fp32 [B][H][N][d], the solved probe, or NULL; 16-byte aligned.
+ *   lse      : fp32 [B][H][N] natural-log softmax normaliser, or NULL.
+ *   steps_out: int32 [B][H][N] conjugate-gradient steps taken per row, or NULL.
+ *   workspace: device scratch of plx_lla_workspace_size(B, H, N, d) bytes,
+ *              256-byte aligned, no initialisation.
+ *   B, H, N >= 1, B * H <= 65535; d a multiple of 32 in [32, 256];
+ *   lambda >= 0 (finite); max_iters >= 0; tol >= 0 (finite).
+ *   lambda = 0 needs every row's Sigma_KK to be non-singular (a prefix of at
+ *   least d + 1 keys in general position); a row with p . Ap <= 0 stops.
+ * max_iters + 3 launches on `stream`, plus a device-to-device copy for each
+ * of rho_out and steps_out that is given.
+ * Errors: PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_MISALIGNED,
+ * PLX_ERR_WORKSPACE, PLX_ERR_CUDA.
+ */
+plx_status plx_lla_f32(const float* q, const float* k, const float* v, float* out, float* rho_out, float* lse,
+                       int32_t* steps_out, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                       float scale, float lambda, int max_iters, float tol, void* stream);
+
+/* Workspace bytes plx_lla_f32 needs: about B*H*N*(4d + 4)*4 (0 for invalid sizes). */
+size_t plx_lla_workspace_size(int B, int H, int N, int d);
+
+/*
+ * plx_probe_proj -- the probe projection rho_i = W_R x_i that feeds every
+ * PLX entry point (zhichai.net section 1.3: the probe is a learned linear
+ * map of the token's hidden state), on the tensor cores (tcgen05, bf16
+ * operands, fp32 accumulation, bf16 result):
+ *
+ *   rho[b][h][n][:] = W_R[h d : (h + 1) d][:] . x[b][n][:]
+ *
+ *   x    : bf16 [B][N][Dx] hidden states, 16-byte aligned.
+ *   w_r  : bf16 [H * d][Dx], head h's d x Dx block in rows h d .. h d + d - 1,
+ *          16-byte aligned.
+ *   rho  : bf16 [B][H][N][d] output (the layout plx_fwd, plx_bwd and
+ *          plx_fwd_cached read), written, 16-byte aligned; must not overlap
+ *          x or w_r.
+ *   B, N, H, Dx >= 1; d in {64, 128}; Dx a multiple of 8 (16-byte rows).
+ * One persistent launch on `stream`; each output element is one fp32 dot
+ * product of length Dx rounded once to bf16, and the result does not depend
+ * on the launch configuration.
+ * Errors: PLX_ERR_INVALID_ARG (null pointer, non-positive size),
+ * PLX_ERR_UNSUPPORTED (d, or Dx not a multiple of 8), PLX_ERR_MISALIGNED,
+ * PLX_ERR_CUDA; device-side wait timeouts are reported by
+ * plx_last_device_error.
+ */
+plx_status plx_probe_proj(const void* x, const void* w_r, void* rho, int B, int N, int H, int d, int Dx,
+                          void* stream);
+
+/*
  * plx_last_device_error -- synchronises `stream`, then reads and clears the
  * current device's status word.  Returns PLX_ERR_TIMEOUT if a kernel gave up
  * a bounded wait, PLX_ERR_INVALID_ARG if a decode length exceeded S_cap,

@@ -80,6 +80,12 @@ def library() -> ctypes.CDLL:
         lib.plx_bwd_bf16_workspace_size.argtypes = [i, i, i, i]
         lib.plx_decode_noalloc.restype = i
         lib.plx_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        lib.plx_probe_proj.restype = i
+        lib.plx_lla_f32.restype = i
+        lib.plx_lla_f32.argtypes = [vp] * 8 + [sz, i, i, i, i, f, f, i, f, vp]
+        lib.plx_lla_workspace_size.restype = sz
+        lib.plx_lla_workspace_size.argtypes = [i, i, i, i]
+        lib.plx_probe_proj.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
         lib.plx_last_device_error.restype = i
         lib.plx_last_device_error.argtypes = [vp]
         _lib = lib
@@ -286,6 +292,70 @@ def plx_bwd(q, k, v, rho, dout, *, scale=None, workspace=None, grads=None):
                            _ptr(drho), _ptr(workspace), ws_bytes, B, H, N, d, scale, _stream(dev))
     _check(st, "plx_bwd")
     return dq, dk, dv, drho
+
+
+def plx_lla_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return library().plx_lla_workspace_size(B, H, N, d)
+
+
+def plx_lla_f32(q, k, v, *, lam, max_iters, tol=0.0, scale=None, workspace=None, out=None, rho_out=None,
+                lse=None, steps=None, with_rho=True, with_steps=True):
+    """Local linear attention with the probe solved by conjugate gradients
+    (fp32 [B, H, N, d] q, k, v; ridge ``lam``; at most ``max_iters`` steps per
+    row, a row stopping once |r| <= tol |mu|).  Returns ``(out, rho, lse,
+    steps)``; rho (the solved probe) and steps (int32 per row) are None when
+    not requested."""
+    B, H, N, d = q.shape
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.float32, (B, H, N, d), dev)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, (B, H, N, d), dev)
+    if with_rho and rho_out is None:
+        rho_out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    if rho_out is not None:
+        _need(rho_out, "rho_out", torch.float32, (B, H, N, d), dev)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    _need(lse, "lse", torch.float32, (B, H, N), dev)
+    if with_steps and steps is None:
+        steps = torch.empty((B, H, N), dtype=torch.int32, device=dev)
+    if steps is not None:
+        _need(steps, "steps", torch.int32, (B, H, N), dev)
+    need = plx_lla_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().plx_lla_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(rho_out), _ptr(lse), _ptr(steps),
+                               _ptr(workspace), ws_bytes, B, H, N, d, scale, float(lam), int(max_iters),
+                               float(tol), _stream(dev))
+    _check(st, "plx_lla_f32")
+    return out, rho_out, lse, steps
+
+
+def plx_probe_proj(x, w_r, *, heads, out=None):
+    """The probe projection rho = W_R x on the tensor cores, written in the
+    [B, H, N, d] layout the PLX entry points read.  x is bf16 [B, N, Dx];
+    w_r is bf16 [H * d, Dx] (head h in rows h d .. h d + d - 1); ``heads`` = H.
+    Returns bf16 rho [B, H, N, d] (``out`` may pass it preallocated)."""
+    if x.dim() != 3 or w_r.dim() != 2:
+        raise ValueError("x must be [B, N, Dx] and w_r [H * d, Dx]")
+    B, N, Dx = x.shape
+    H = int(heads)
+    if H < 1 or w_r.shape[0] % H != 0:
+        raise ValueError(f"w_r has {w_r.shape[0]} rows, not a multiple of heads={H}")
+    d = w_r.shape[0] // H
+    dev = x.device
+    _need(x, "x", torch.bfloat16, (B, N, Dx), dev)
+    _need(w_r, "w_r", torch.bfloat16, (H * d, Dx), dev)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (B, H, N, d), dev)
+    st = library().plx_probe_proj(_ptr(x), _ptr(w_r), _ptr(out), B, N, H, d, Dx, _stream(dev))
+    _check(st, "plx_probe_proj")
+    return out
 
 
 def plx_decode_num_splits(B: int, H: int, d: int, S_cap: int) -> int:

@@ -3,9 +3,11 @@
 // One translation unit: argument validation, launch configuration, TMA
 // tensor-map encoding and the device status word, around the kernels in
 // fwd_tc.cuh (tcgen05 prefill), fwd_f32.cuh (fp32 prefill), bwd_tc.cuh (tcgen05
-// backward), bwd_f32.cuh (fp32 backward) and decode.cuh (split-KV decode +
-// combine).  Every entry point validates its arguments
-// before launching anything and never lets a C++ exception escape.
+// backward), bwd_f32.cuh (fp32 backward), decode.cuh (split-KV decode +
+// combine), proj_tc.cuh (tcgen05 probe projection) and lla_f32.cuh (local
+// linear attention, conjugate gradients in fp32).  Every entry point
+// validates its arguments before launching anything and never lets a C++
+// exception escape.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -18,14 +20,17 @@
 #include "bwd_f32.cuh"
 #include "decode.cuh"
 #include "fwd_f32.cuh"
+#include "lla_f32.cuh"
 #include "fwd_tc.cuh"
 #include "bwd_tc.cuh"
+#include "proj_tc.cuh"
 
 namespace {
 
 using plx::BwdTcCfg;
 using plx::DecodeCfg;
 using plx::FwdTcCfg;
+using plx::ProjCfg;
 
 constexpr int kMaxDevices = 64;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -77,6 +82,8 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, false, plx::BWD_DQ>, BwdTcCfg<64, false, plx::BWD_DQ>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, true, plx::BWD_DKV>, BwdTcCfg<64, true, plx::BWD_DKV>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, false, plx::BWD_DKV>, BwdTcCfg<64, false, plx::BWD_DKV>::SMEM);
+    e = e ? e : set_smem(plx::plx_proj_tc_kernel<128>, ProjCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_proj_tc_kernel<64>, ProjCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_decode_split_kernel<128, true>, DecodeCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_decode_split_kernel<128, false>, DecodeCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_decode_split_kernel<64, true>, DecodeCfg<64>::SMEM);
@@ -196,6 +203,33 @@ plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void
     return launch_status();
 }
 
+// The probe projection on the tensor cores: x is read through a {64, 128}
+// box of its [B][N][Dx] view, W_R through a {64, 256} box of its [H d][Dx]
+// view, rho written through the [B H][N][d] output map.
+template <int D>
+plx_status launch_proj_tc(const void* x, const void* w_r, void* rho, int B, int N, int H, int Dx,
+                          cudaStream_t stream, int sm_count) {
+    using Cfg = ProjCfg<D>;
+    const long long n_mt = (N + Cfg::BM - 1) / Cfg::BM;
+    const long long n_hg = (static_cast<long long>(H) * D + Cfg::BN - 1) / Cfg::BN;
+    const long long n_items = static_cast<long long>(B) * n_mt * n_hg;
+    if (n_items > INT_MAX || static_cast<long long>(H) * D > INT_MAX) return PLX_ERR_UNSUPPORTED;
+    CUtensorMap mx, mw, mo;
+    if (!make_map(&mx, x, Dx, N, B, Cfg::BM) || !make_map(&mw, w_r, Dx, H * D, 1, Cfg::BN) ||
+        !make_out_map(&mo, rho, D, N, static_cast<long long>(B) * H, false))
+        return PLX_ERR_CUDA;
+    plx::ProjParams p;
+    p.N = N;
+    p.H = H;
+    p.n_kb = (Dx + Cfg::BK - 1) / Cfg::BK;
+    p.n_mt = static_cast<int>(n_mt);
+    p.n_hg = static_cast<int>(n_hg);
+    p.n_items = static_cast<int>(n_items);
+    const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
+    plx::plx_proj_tc_kernel<D><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mx, mw, mo, p);
+    return launch_status();
+}
+
 // 3-D map over the backward's per-row statistics [BH][N] x float4, for the dkv
 // pass: a {4, 64, 1} box, rows past N zero-filled.
 bool make_stats_map(CUtensorMap* map, const void* base, int N, long long BH) {
@@ -287,6 +321,46 @@ bool dispatch_f32(const plx::FwdF32Params& p, int d, long long BH, cudaStream_t 
         case 8: launch_f32<8, PLX>(p, BH, s); return true;
         default: return false;
     }
+}
+
+// Workspace of plx_lla_f32 for R = B H N rows: kbar, x, r, p ([R][d] fp32
+// each), lse, rs, rs0 ([R] fp32 each) and the step counts ([R] int32).
+struct LlaWorkspace {
+    float *kbar, *x, *r, *p, *lse, *rs, *rs0;
+    int* steps;
+};
+size_t lla_ws_bytes(long long R, int d) {
+    return 4 * align256(static_cast<size_t>(R) * d * sizeof(float)) + 4 * align256(static_cast<size_t>(R) * 4);
+}
+LlaWorkspace lla_ws_carve(void* base, long long R, int d) {
+    auto* c = static_cast<char*>(base);
+    const size_t vec = align256(static_cast<size_t>(R) * d * sizeof(float)), sc = align256(static_cast<size_t>(R) * 4);
+    LlaWorkspace w;
+    w.kbar = reinterpret_cast<float*>(c);
+    w.x = reinterpret_cast<float*>(c + vec);
+    w.r = reinterpret_cast<float*>(c + 2 * vec);
+    w.p = reinterpret_cast<float*>(c + 3 * vec);
+    w.lse = reinterpret_cast<float*>(c + 4 * vec);
+    w.rs = reinterpret_cast<float*>(c + 4 * vec + sc);
+    w.rs0 = reinterpret_cast<float*>(c + 4 * vec + 2 * sc);
+    w.steps = reinterpret_cast<int*>(c + 4 * vec + 3 * sc);
+    return w;
+}
+
+// plx_lla_f32's launches: kbar and lse (softmax attention of the keys
+// themselves), the CG set-up, max_iters CG steps, and Parallax's output with
+// the solved probe (centred).
+template <int DPL>
+void launch_lla(const float* q, const float* k, const float* v, float* out, float* lse, const LlaWorkspace& w,
+                int N, long long BH, float scale, float lambda, int max_iters, float tol, cudaStream_t s) {
+    plx::FwdF32Params f{q, k, k, nullptr, w.kbar, w.lse, N, scale};
+    launch_f32<DPL, false>(f, BH, s);
+    plx::LlaParams lp{q, k, w.kbar, w.lse, w.x, w.r, w.p, w.rs, w.rs0, w.steps, N, scale, lambda, tol * tol};
+    dim3 grid((N + plx::LLA_ROWS_PER_BLOCK - 1) / plx::LLA_ROWS_PER_BLOCK, static_cast<unsigned>(BH));
+    plx::plx_lla_init_kernel<DPL><<<grid, plx::LLA_WARPS * 32, 0, s>>>(lp);
+    for (int it = 0; it < max_iters; ++it)
+        plx::plx_lla_cg_step_kernel<DPL><<<grid, plx::LLA_WARPS * 32, plx::LlaTile<DPL>::SMEM, s>>>(lp);
+    plx::plx_lla_out_kernel<DPL><<<grid, plx::LLA_WARPS * 32, 0, s>>>(lp, v, out, lse);
 }
 
 template <int DPL, bool PLX>
@@ -729,6 +803,72 @@ plx_status plx_decode_noalloc(const void* q, const void* rho, const void* k_cach
         if (!scratch) return PLX_ERR_CUDA;
         return plx_decode(q, rho, k_cache, v_cache, seqlens, out, lse, B, H, d, S_cap, scale, splits, scratch,
                           kNoallocScratchBytes, out_dtype, stream);
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+size_t plx_lla_workspace_size(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || d < 32 || d > 256 || d % 32 != 0) return 0;
+    return lla_ws_bytes(static_cast<long long>(B) * H * N, d);
+}
+
+plx_status plx_lla_f32(const float* q, const float* k, const float* v, float* out, float* rho_out, float* lse,
+                       int32_t* steps_out, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                       float scale, float lambda, int max_iters, float tol, void* stream) {
+    try {
+        if (!q || !k || !v || !out) return PLX_ERR_INVALID_ARG;
+        if (B < 1 || H < 1 || N < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
+        if (!std::isfinite(lambda) || lambda < 0.f || max_iters < 0 || !std::isfinite(tol) || tol < 0.f)
+            return PLX_ERR_INVALID_ARG;
+        if (d < 32 || d > 256 || d % 32 != 0) return PLX_ERR_UNSUPPORTED;
+        const float* in16[] = {q, k, v, out, rho_out};
+        for (const float* ptr : in16)
+            if (ptr && !aligned(ptr, 16)) return PLX_ERR_MISALIGNED;
+        if ((lse && !aligned(lse, 4)) || (steps_out && !aligned(steps_out, 4)) ||
+            (workspace && !aligned(workspace, 256)))
+            return PLX_ERR_MISALIGNED;
+        const long long BH = static_cast<long long>(B) * H;
+        if (BH > 65535) return PLX_ERR_UNSUPPORTED;
+        const long long R = BH * N;
+        if (!workspace || workspace_bytes < lla_ws_bytes(R, d)) return PLX_ERR_WORKSPACE;
+        const LlaWorkspace w = lla_ws_carve(workspace, R, d);
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        switch (d / 32) {
+            case 1: launch_lla<1>(q, k, v, out, lse, w, N, BH, scale, lambda, max_iters, tol, s); break;
+            case 2: launch_lla<2>(q, k, v, out, lse, w, N, BH, scale, lambda, max_iters, tol, s); break;
+            case 3: launch_lla<3>(q, k, v, out, lse, w, N, BH, scale, lambda, max_iters, tol, s); break;
+            case 4: launch_lla<4>(q, k, v, out, lse, w, N, BH, scale, lambda, max_iters, tol, s); break;
+            case 5: launch_lla<5>(q, k, v, out, lse, w, N, BH, scale, lambda, max_iters, tol, s); break;
+            case 6: launch_lla<6>(q, k, v, out, lse, w, N, BH, scale, lambda, max_iters, tol, s); break;
+            case 7: launch_lla<7>(q, k, v, out, lse, w, N, BH, scale, lambda, max_iters, tol, s); break;
+            case 8: launch_lla<8>(q, k, v, out, lse, w, N, BH, scale, lambda, max_iters, tol, s); break;
+            default: return PLX_ERR_UNSUPPORTED;
+        }
+        if (rho_out && cudaMemcpyAsync(rho_out, w.x, static_cast<size_t>(R) * d * sizeof(float),
+                                       cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return PLX_ERR_CUDA;
+        if (steps_out && cudaMemcpyAsync(steps_out, w.steps, static_cast<size_t>(R) * sizeof(int32_t),
+                                         cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return PLX_ERR_CUDA;
+        return launch_status();
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+plx_status plx_probe_proj(const void* x, const void* w_r, void* rho, int B, int N, int H, int d, int Dx,
+                          void* stream) {
+    try {
+        if (!x || !w_r || !rho) return PLX_ERR_INVALID_ARG;
+        if (B < 1 || N < 1 || H < 1 || Dx < 1) return PLX_ERR_INVALID_ARG;
+        if ((d != 128 && d != 64) || Dx % 8 != 0) return PLX_ERR_UNSUPPORTED;
+        if (!aligned(x, 16) || !aligned(w_r, 16) || !aligned(rho, 16)) return PLX_ERR_MISALIGNED;
+        const DeviceInfo* info = device_info();
+        if (!info) return PLX_ERR_CUDA;
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        return d == 128 ? launch_proj_tc<128>(x, w_r, rho, B, N, H, Dx, s, info->sm_count)
+                        : launch_proj_tc<64>(x, w_r, rho, B, N, H, Dx, s, info->sm_count);
     } catch (...) {
         return PLX_ERR_CUDA;
     }

@@ -195,3 +195,34 @@ def test_fwd_cached_rejects_bad_arguments_before_launch():
     assert lib.plx_fwd_cached(P, P, P, P, SL, P, P, 1, 2, 16, 64, 96, 0.1, F32, None) == 2      # head dim
     assert lib.plx_fwd_cached(P, P, P, P, ctypes.c_void_p(0x30002), P, P, 1, 2, 16, 64, 128, 0.1, F32,
                               None) == 3                                                        # misaligned seqlens
+
+
+def test_probe_proj_rejects_bad_arguments_before_launch():
+    lib = plx.library()
+    P = P16
+    assert lib.plx_probe_proj(None, P, P, 1, 64, 2, 128, 256, None) == 1                      # no x
+    assert lib.plx_probe_proj(P, P, None, 1, 64, 2, 128, 256, None) == 1                      # no rho
+    assert lib.plx_probe_proj(P, P, P, 0, 64, 2, 128, 256, None) == 1                         # B < 1
+    assert lib.plx_probe_proj(P, P, P, 1, 64, 2, 128, 0, None) == 1                           # Dx < 1
+    assert lib.plx_probe_proj(P, P, P, 1, 64, 2, 96, 256, None) == 2                          # head dim
+    assert lib.plx_probe_proj(P, P, P, 1, 64, 2, 128, 250, None) == 2                         # Dx % 8
+    assert lib.plx_probe_proj(P, ctypes.c_void_p(0x40008), P, 1, 64, 2, 128, 256, None) == 3  # misaligned W_R
+
+
+def test_lla_rejects_bad_arguments_before_launch():
+    lib = plx.library()
+    P = P16
+    WS = ctypes.c_void_p(0x100000)
+    need = lib.plx_lla_workspace_size(2, 3, 64, 64)
+    assert need >= 2 * 3 * 64 * (4 * 64 + 4) * 4
+    assert lib.plx_lla_workspace_size(2, 3, 64, 48) == 0
+    args = lambda ws, nbytes, d, lam, iters, tol: (P, P, P, P, None, None, None, ws, nbytes, 2, 3, 64, d, 0.1, lam,
+                                                   iters, tol, None)
+    assert lib.plx_lla_f32(*args(WS, need, 64, -0.1, 8, 0.0)) == 1                  # negative lambda
+    assert lib.plx_lla_f32(*args(WS, need, 64, 0.1, -1, 0.0)) == 1                  # negative iterations
+    assert lib.plx_lla_f32(*args(WS, need, 64, 0.1, 8, float("nan"))) == 1          # tol not finite
+    assert lib.plx_lla_f32(*args(WS, need, 48, 0.1, 8, 0.0)) == 2                   # head dim
+    assert lib.plx_lla_f32(*args(None, 0, 64, 0.1, 8, 0.0)) == 6                    # no workspace
+    assert lib.plx_lla_f32(*args(WS, need - 256, 64, 0.1, 8, 0.0)) == 6             # workspace too small
+    assert lib.plx_lla_f32(*args(ctypes.c_void_p(0x100010), need, 64, 0.1, 8, 0.0)) == 3   # misaligned workspace
+    assert lib.plx_lla_f32(None, P, P, P, None, None, None, WS, need, 2, 3, 64, 64, 0.1, 0.1, 8, 0.0, None) == 1
