@@ -1,0 +1,429 @@
+// lla_f32.cuh -- plx_lla_f32: local linear attention with the solved probe,
+// in fp32 on the CUDA cores.
+//
+// "Parallax: Parameterized Local Linear Attention for Language Modeling"
+// introduces Parallax as a learned replacement for local linear attention
+// (LLA), whose probe is the solution of a per-token linear system found by
+// conjugate gradients (zhichai.net section 1.2; gist.science, "Enunciato del
+// Problema").  For query i of one head (causal prefix j <= i):
+//
+//   w_ij = softmax_j(scale q_i . k_j),  kbar_i = sum_j w_ij k_j
+//   (Sigma_KK^(i) + lambda I) rho_i = mu_i,   mu_i = kbar_i - q_i
+//   Sigma_KK^(i) p = sum_j w_ij ((k_j - kbar_i) . p) (k_j - kbar_i)
+//                  = sum_j w_ij ((k_j . p) - (kbar_i . p)) k_j      (since sum_j w_ij = 1)
+//   o_i = vbar_i - Sigma_KV^(i) rho_i           (Parallax's output formula)
+//
+// The library runs it as a sequence of launches on one stream:
+//   1. plx_fwd_f32_kernel<., false> with v := k: kbar_i and lse_i;
+//   2. plx_lla_init_kernel: x = 0, r = p = mu, rs = rs0 = mu . mu;
+//   3. max_iters x plx_lla_cg_step_kernel: one conjugate-gradient step per
+//      row, Sigma_KK p formed by streaming the keys once per 4 rows (weights
+//      from the stored lse, no online rescaling), the update done in
+//      registers; a row stops once r . r <= tol^2 rs0 (or when p . Ap <= 0);
+//   4. plx_lla_out_kernel: o from Parallax's output formula with rho := x,
+//      in centred form.
+// The pages warn that the solve is unstable in low precision; every step
+// here is fp32.
+#pragma once
+#include "bwd_f32.cuh"   // warp_sum
+#include "status.cuh"
+
+namespace plx {
+
+struct LlaParams {
+    const float* q;      // [BH][N][d]
+    const float* k;      // [BH][N][d]
+    const float* kbar;   // [BH][N][d]
+    const float* lse;    // [BH][N] (natural log)
+    float* x;            // [BH][N][d] the probe iterate
+    float* r;            // [BH][N][d] residual
+    float* p;            // [BH][N][d] search direction
+    float* rs;           // [BH][N] r . r (0 once the row has stopped)
+    float* rs0;          // [BH][N] mu . mu
+    int* steps;          // [BH][N] steps taken
+    int N;
+    float scale;
+    float lambda;
+    float tol2;          // tol^2
+};
+
+constexpr int LLA_WARPS = 4;
+constexpr int LLA_ROWS_PER_BLOCK = 16;
+
+template <int DPL>
+__global__ void __launch_bounds__(LLA_WARPS * 32) plx_lla_init_kernel(const LlaParams p) {
+    constexpr int D = DPL * 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t bh = blockIdx.y;
+    for (int rr = warp; rr < LLA_ROWS_PER_BLOCK; rr += LLA_WARPS) {
+        const int i = blockIdx.x * LLA_ROWS_PER_BLOCK + rr;
+        if (i >= p.N) break;
+        const size_t row = bh * p.N + i;
+        const size_t o = row * D;
+        float part = 0.f;
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) {
+            const float mu = p.kbar[o + lane + 32 * t] - p.q[o + lane + 32 * t];
+            p.x[o + lane + 32 * t] = 0.f;
+            p.r[o + lane + 32 * t] = mu;
+            p.p[o + lane + 32 * t] = mu;
+            part = fmaf(mu, mu, part);
+        }
+        const float rs = warp_sum(part);
+        if (lane == 0) {
+            p.rs[row] = rs;
+            p.rs0[row] = rs;
+            p.steps[row] = 0;
+        }
+    }
+}
+
+// lane L of a warp owns the DPL contiguous dims L*DPL .. L*DPL + DPL - 1 of
+// every vector, so one key row is one 16-byte load per lane when DPL = 4
+template <int DPL>
+__device__ __forceinline__ void load_own(const float* row, int lane, float (&f)[DPL]) {
+    const float* src = row + lane * DPL;
+    if constexpr (DPL % 4 == 0) {
+#pragma unroll
+        for (int t = 0; t < DPL; t += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src + t);
+            f[t] = x.x;
+            f[t + 1] = x.y;
+            f[t + 2] = x.z;
+            f[t + 3] = x.w;
+        }
+    } else if constexpr (DPL % 2 == 0) {
+#pragma unroll
+        for (int t = 0; t < DPL; t += 2) {
+            const float2 x = *reinterpret_cast<const float2*>(src + t);
+            f[t] = x.x;
+            f[t + 1] = x.y;
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) f[t] = src[t];
+    }
+}
+
+// Sums 8 values over the warp and leaves the full sum of value (lane >> 2) & 7
+// in each lane: lane masks 16, 8, 4 each halve the values a lane carries
+// (it keeps one half and adds its partner's copy of that half), masks 2 and 1
+// finish the single remaining sum.  9 shuffles instead of 40.
+__device__ __forceinline__ float reduce_scatter8(const float (&a)[8], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float b[4], c[2];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        const float send = b4 ? a[x] : a[x + 4];
+        const float keep = b4 ? a[x + 4] : a[x];
+        b[x] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        const float send = b3 ? b[x] : b[x + 2];
+        const float keep = b3 ? b[x + 2] : b[x];
+        c[x] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    const float send = b2 ? c[0] : c[1];
+    const float keep = b2 ? c[1] : c[0];
+    float val = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    val += __shfl_xor_sync(0xffffffffu, val, 2);
+    val += __shfl_xor_sync(0xffffffffu, val, 1);
+    return val;
+}
+
+// Keys per shared-memory tile of the CG step (16 KB per tile at d <= 128).
+template <int DPL>
+struct LlaTile {
+    static constexpr int TK = DPL <= 4 ? 32 : 16;
+    static constexpr int FLOATS = TK * DPL * 32;
+    static constexpr int SMEM = 2 * FLOATS * 4 + 64;     // two tiles + 2 mbarriers + flag
+};
+
+// One conjugate-gradient step for 4 consecutive rows per warp, 16 rows per
+// block.  The block's keys 0 .. i_b + 15 stream through two shared-memory
+// tiles of TK keys: thread 0 issues one 1-D bulk copy per tile (the keys of a
+// head are contiguous), the copy of tile t + 1 overlapping the work on tile
+// t, and every wait on a copy is bounded.  Per key j the warp needs 8 dot
+// products (q_r . k_j and p_r . k_j of its 4 rows): reduce_scatter8 leaves s
+// of row (L >> 3) & 3 in the lanes L with bit 2 clear and its p . k in the
+// lanes with bit 2 set; one exchange pairs them, those lanes form
+// g = w (p.k - kbar.p), and four broadcasts hand every lane the 4 rows' g.
+template <int DPL>
+__global__ void __launch_bounds__(LLA_WARPS * 32) plx_lla_cg_step_kernel(const LlaParams p) {
+    constexpr int D = DPL * 32;
+    constexpr int RW = LLA_ROWS_PER_BLOCK / LLA_WARPS;   // rows per warp
+    constexpr int TK = LlaTile<DPL>::TK;
+    static_assert(RW == 4, "the butterfly is written for 4 rows per warp");
+    extern __shared__ __align__(128) float lla_smem[];
+    float* tile0 = lla_smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(lla_smem + 2 * LlaTile<DPL>::FLOATS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t bh = blockIdx.y;
+    const float* K = p.k + bh * p.N * D;
+    const int ib = blockIdx.x * LLA_ROWS_PER_BLOCK;
+    const int i0 = ib + warp * RW;
+
+    bool act[RW];
+    float rs[RW], qv[RW][DPL], pv[RW][DPL], U[RW][DPL], kp[RW], lse[RW];
+    bool any = false;
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+        const int i = i0 + r;
+        const size_t row = bh * p.N + (i < p.N ? i : ib);
+        rs[r] = p.rs[row];
+        act[r] = i < p.N && rs[r] > p.tol2 * p.rs0[row];
+        any |= act[r];
+        lse[r] = p.lse[row];
+        float kb[DPL];
+        load_own<DPL>(p.q + row * D, lane, qv[r]);
+        load_own<DPL>(p.p + row * D, lane, pv[r]);
+        load_own<DPL>(p.kbar + row * D, lane, kb);
+        float part = 0.f;
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) {
+            qv[r][t] *= p.scale;
+            part = fmaf(kb[t], pv[r][t], part);
+            U[r][t] = 0.f;
+        }
+        kp[r] = warp_sum(part);
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (!__syncthreads_or(any)) return;                   // every row of the block has stopped
+
+    const int kmax = min(ib + LLA_ROWS_PER_BLOCK, p.N) - 1;   // last key the block needs
+    const int n_tiles = kmax / TK + 1;
+    auto issue = [&](int t) {
+        const int j0 = t * TK;
+        const int nk = min(TK, kmax + 1 - j0);
+        const uint32_t bytes = static_cast<uint32_t>(nk) * D * 4;
+        mbar_arrive_expect_tx(&full[t & 1], bytes);
+        bulk_g2s(tile0 + (t & 1) * LlaTile<DPL>::FLOATS, K + static_cast<size_t>(j0) * D, bytes, &full[t & 1]);
+    };
+    if (threadIdx.x == 0) issue(0);
+
+    // this lane's row in the butterfly (the row whose s / p.k it ends up holding)
+    const int my = (lane >> 3) & 3;
+    float my_lse = lse[0], my_kp = kp[0];
+    bool my_act = act[0];
+#pragma unroll
+    for (int r = 1; r < RW; ++r)
+        if (my == r) {
+            my_lse = lse[r];
+            my_kp = kp[r];
+            my_act = act[r];
+        }
+    const bool b2 = lane & 4;
+    const bool warp_any = __any_sync(0xffffffffu, any);
+    int last_issued = 0;
+
+    for (int t = 0; t < n_tiles; ++t) {
+        if (threadIdx.x == 0 && t + 1 < n_tiles) {        // the other tile was released at the last barrier
+            issue(t + 1);
+            last_issued = t + 1;
+        }
+        if (!mbar_wait(&full[t & 1], (t >> 1) & 1)) {
+            atomicOr(&g_plx_status, PLX_DEV_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        const float* tk = tile0 + (t & 1) * LlaTile<DPL>::FLOATS;
+        // keys past the warp's last row are not needed, and keys past kmax were not copied
+        const int j_end = min(min(t * TK + TK, i0 + RW), kmax + 1);
+        if (warp_any && !*abort_flag) {
+#pragma unroll 2
+            for (int j = t * TK; j < j_end; ++j) {
+                float kf[DPL];
+                load_own<DPL>(tk + (j - t * TK) * D, lane, kf);
+                float a[2 * RW];                            // a[2r] = s part of row r, a[2r+1] = p.k part
+#pragma unroll
+                for (int r = 0; r < RW; ++r) {
+                    float sd = 0.f, rd = 0.f;
+#pragma unroll
+                    for (int x = 0; x < DPL; ++x) {
+                        sd = fmaf(qv[r][x], kf[x], sd);
+                        rd = fmaf(pv[r][x], kf[x], rd);
+                    }
+                    a[2 * r] = sd;
+                    a[2 * r + 1] = rd;
+                }
+                const float val = reduce_scatter8(a, lane);
+                // lanes with bit 2 clear hold s of row `my`, their partner (lane ^ 4) its p . k
+                const float other = __shfl_xor_sync(0xffffffffu, val, 4);
+                float g = 0.f;
+                if (!b2 && my_act && j <= i0 + my) g = expf(val - my_lse) * (other - my_kp);
+                float gr[RW];
+#pragma unroll
+                for (int r = 0; r < RW; ++r) gr[r] = __shfl_sync(0xffffffffu, g, 8 * r);
+#pragma unroll
+                for (int r = 0; r < RW; ++r)
+#pragma unroll
+                    for (int x = 0; x < DPL; ++x) U[r][x] = fmaf(gr[r], kf[x], U[r][x]);
+            }
+        }
+        __syncthreads();                                  // tile t is free for the copy of tile t + 2
+        if (*abort_flag) break;
+    }
+    // no copy may still be in flight when the block exits (only after an abort)
+    if (threadIdx.x == 0 && *abort_flag) mbar_wait(&full[last_issued & 1], (last_issued >> 1) & 1);
+    if (*abort_flag) return;
+
+    // Ap = Sigma_KK p + lambda p, then one conjugate-gradient step per active row
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+        if (!act[r]) continue;                              // warp-uniform
+        const size_t row = bh * p.N + i0 + r;
+        float pap = 0.f;
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) {
+            U[r][t] = fmaf(p.lambda, pv[r][t], U[r][t]);
+            pap = fmaf(pv[r][t], U[r][t], pap);
+        }
+        pap = warp_sum(pap);
+        if (!(pap > 0.f)) {                                 // breakdown: stop the row
+            if (lane == 0) p.rs[row] = 0.f;
+            continue;
+        }
+        const float alpha = rs[r] / pap;
+        float xv[DPL], rv[DPL];
+        load_own<DPL>(p.x + row * D, lane, xv);
+        load_own<DPL>(p.r + row * D, lane, rv);
+        float rn = 0.f;
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) {
+            xv[t] = fmaf(alpha, pv[r][t], xv[t]);
+            rv[t] = fmaf(-alpha, U[r][t], rv[t]);
+            rn = fmaf(rv[t], rv[t], rn);
+        }
+        rn = warp_sum(rn);
+        const float beta = rn / rs[r];
+        float* xo = p.x + row * D + lane * DPL;
+        float* ro = p.r + row * D + lane * DPL;
+        float* po = p.p + row * D + lane * DPL;
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) {
+            xo[t] = xv[t];
+            ro[t] = rv[t];
+            po[t] = fmaf(beta, pv[r][t], rv[t]);
+        }
+        if (lane == 0) {
+            p.rs[row] = rn;
+            p.steps[row] += 1;
+        }
+    }
+}
+
+// Parallax's output with the solved probe, in centred form (4 rows per warp,
+// the same butterfly): with r'_j = k_j . rho - kbar . rho = (k_j - kbar) . rho,
+//   o = vbar - Sigma_KV rho = sum_j w_j (1 - r'_j) v_j + vbar sum_j w_j r'_j,
+// weights w_j = exp(s_j - lse) / L, L = sum_j exp(s_j - lse) (1 up to
+// rounding).  The uncentred (1 + c) vbar - u cancels two terms of size
+// |k| |rho| |v|, which is large on short prefixes where rho ~ mu / lambda;
+// here r'_j is 0 on a one-key prefix and small elsewhere.
+template <int DPL>
+__global__ void __launch_bounds__(LLA_WARPS * 32) plx_lla_out_kernel(const LlaParams p, const float* v, float* out,
+                                                                  float* lse_out) {
+    constexpr int D = DPL * 32;
+    constexpr int RW = LLA_ROWS_PER_BLOCK / LLA_WARPS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t bh = blockIdx.y;
+    const float* K = p.k + bh * p.N * D;
+    const float* V = v + bh * p.N * D;
+    const int i0 = blockIdx.x * LLA_ROWS_PER_BLOCK + warp * RW;
+    if (i0 >= p.N) return;
+
+    float qv[RW][DPL], xv[RW][DPL], O[RW][DPL], A[RW][DPL], kx[RW], lse[RW];
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+        const int i = i0 + r < p.N ? i0 + r : i0;
+        const size_t row = bh * p.N + i;
+        lse[r] = p.lse[row];
+        float kb[DPL];
+        load_own<DPL>(p.q + row * D, lane, qv[r]);
+        load_own<DPL>(p.x + row * D, lane, xv[r]);
+        load_own<DPL>(p.kbar + row * D, lane, kb);
+        float part = 0.f;
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) {
+            qv[r][t] *= p.scale;
+            part = fmaf(kb[t], xv[r][t], part);
+            O[r][t] = 0.f;
+            A[r][t] = 0.f;
+        }
+        kx[r] = warp_sum(part);
+    }
+    const int my = (lane >> 3) & 3;
+    float my_lse = lse[0], my_kx = kx[0];
+#pragma unroll
+    for (int r = 1; r < RW; ++r)
+        if (my == r) {
+            my_lse = lse[r];
+            my_kx = kx[r];
+        }
+    const bool b2 = lane & 4;
+    const int jmax = min(i0 + RW - 1, p.N - 1);
+    float wsum = 0.f, wr = 0.f;        // lanes 8 r: sum_j w_j and sum_j w_j r'_j of row r
+
+#pragma unroll 2
+    for (int j = 0; j <= jmax; ++j) {
+        float kf[DPL], vf[DPL];
+        load_own<DPL>(K + static_cast<size_t>(j) * D, lane, kf);
+        load_own<DPL>(V + static_cast<size_t>(j) * D, lane, vf);
+        float a[2 * RW];
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            float sd = 0.f, rd = 0.f;
+#pragma unroll
+            for (int t = 0; t < DPL; ++t) {
+                sd = fmaf(qv[r][t], kf[t], sd);
+                rd = fmaf(xv[r][t], kf[t], rd);
+            }
+            a[2 * r] = sd;
+            a[2 * r + 1] = rd;
+        }
+        const float val = reduce_scatter8(a, lane);
+        const float other = __shfl_xor_sync(0xffffffffu, val, 4);
+        float w = 0.f, rc = 0.f;
+        if (!b2 && j <= i0 + my) {
+            w = expf(val - my_lse);
+            rc = other - my_kx;
+        }
+        wsum += w;
+        wr = fmaf(w, rc, wr);
+        const float g = w - w * rc;                         // w (1 - r')
+        float gr[RW], wv[RW];
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            gr[r] = __shfl_sync(0xffffffffu, g, 8 * r);
+            wv[r] = __shfl_sync(0xffffffffu, w, 8 * r);
+        }
+#pragma unroll
+        for (int r = 0; r < RW; ++r)
+#pragma unroll
+            for (int t = 0; t < DPL; ++t) {
+                O[r][t] = fmaf(gr[r], vf[t], O[r][t]);
+                A[r][t] = fmaf(wv[r], vf[t], A[r][t]);
+            }
+    }
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+        const float L = __shfl_sync(0xffffffffu, wsum, 8 * r);
+        const float C = __shfl_sync(0xffffffffu, wr, 8 * r);
+        if (i0 + r >= p.N) continue;                        // warp-uniform
+        const size_t row = bh * p.N + i0 + r;
+        const float inv = 1.f / L;
+        const float cn = C * inv;
+        float* dst = out + row * D + lane * DPL;
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) dst[t] = fmaf(cn, A[r][t] * inv, O[r][t] * inv);
+        if (lane == 0 && lse_out) lse_out[row] = lse[r];
+    }
+}
+
+}  // namespace plx
