@@ -319,6 +319,282 @@ __global__ void __launch_bounds__(LLA_WARPS * 32) plx_lla_cg_step_kernel(const L
     }
 }
 
+// ---------------------------------------------------------------------------
+// The CG step as two block-level SIMT GEMMs per key tile (d = 64 or 128).
+// A block owns BM = 64 query rows i_b .. i_b + 63 and streams keys
+// 0 .. i_b + 63 in tiles of BK = 32:
+//   phase 1   [S; R] = [scale q; p] K^T   (128 stacked rows x 32 keys, K = d)
+//             thread (rg, kg) holds rows {rg, rg + 32} of q and the same two
+//             rows of p (stacked rows rg + 64, rg + 96) against keys
+//             {kg, kg + 8, kg + 16, kg + 24}, so it forms
+//             G = exp(s - lse) ((p.k) - (kbar.p)) for 2 rows x 4 keys in
+//             registers and writes it to shared memory;
+//   phase 2   U += G K                    (64 rows x d, K = 32 keys)
+//             thread (rgrp, dgrp) accumulates rows {rgrp + 16 i} x dims
+//             dgrp * d/16 .. + d/16 in registers across all tiles.
+// The key rows of a tile arrive by one 1-D bulk copy each into a row-padded
+// buffer (row stride d + 4 floats), so 8 consecutive keys read at the same
+// dims fall in 8 different bank groups.  Two tile buffers: the copy of tile
+// t + 1 overlaps the work on tile t.  The CG update of a row reduces over the
+// 16 threads (a half-warp) that hold its dims.
+template <int D>
+struct LlaGemmCfg {
+    static constexpr int BM = 64, BK = 32, THREADS = 256;
+    static constexpr int LD = D + 4;                      // padded row stride (floats)
+    static constexpr int DG = D / 16;                     // phase-2 dims per thread
+    static constexpr int OFF_STAGE = 0;                   // 2 x [BK][LD]
+    static constexpr int OFF_QP = OFF_STAGE + 2 * BK * LD;   // [2 BM][LD]: scale q rows, then p rows
+    static constexpr int GLD = BM + 4;                    // G row stride: key kk, row a at (a % 16) * 4 + a / 16
+    static constexpr int OFF_G = OFF_QP + 2 * BM * LD;    // [BK][GLD]
+    static constexpr int OFF_ROW = OFF_G + BK * GLD;      // lse, kp, rs [BM] each, act [BM] (int)
+    static constexpr int OFF_BAR = OFF_ROW + 4 * BM;      // 2 mbarriers + abort flag
+    static constexpr int SMEM = OFF_BAR * 4 + 32;
+    static_assert(D == 64 || D == 128, "the block GEMM step is built for d in {64, 128}");
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p) {
+    using Cfg = LlaGemmCfg<D>;
+    constexpr int BM = Cfg::BM, BK = Cfg::BK, LD = Cfg::LD, DG = Cfg::DG, GLD = Cfg::GLD;
+    extern __shared__ __align__(128) float lla_gsmem[];
+    float* stage = lla_gsmem + Cfg::OFF_STAGE;
+    float* QP = lla_gsmem + Cfg::OFF_QP;
+    float* Gs = lla_gsmem + Cfg::OFF_G;
+    float* s_lse = lla_gsmem + Cfg::OFF_ROW;
+    float* s_kp = s_lse + BM;
+    float* s_rs = s_kp + BM;
+    int* s_act = reinterpret_cast<int*>(s_rs + BM);
+    uint64_t* full = reinterpret_cast<uint64_t*>(lla_gsmem + Cfg::OFF_BAR);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const size_t bh = blockIdx.y;
+    const int ib = blockIdx.x * BM;
+    const float* K = p.k + bh * p.N * D;
+
+    // ---- prologue: row scalars, q (scaled) and p rows into shared memory
+    if (tid < BM) {
+        const int i = ib + tid;
+        int a = 0;
+        float lse = 0.f, rs = 0.f;
+        if (i < p.N) {
+            const size_t row = bh * p.N + i;
+            rs = p.rs[row];
+            lse = p.lse[row];
+            a = rs > p.tol2 * p.rs0[row] ? 1 : 0;
+        }
+        s_act[tid] = a;
+        s_lse[tid] = lse;
+        s_rs[tid] = rs;
+    }
+    for (int idx = tid; idx < 2 * BM * (D / 4); idx += Cfg::THREADS) {
+        const int r = idx / (D / 4), c = idx % (D / 4);
+        const int i = ib + (r & (BM - 1));
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < p.N) {
+            const size_t off = (bh * p.N + i) * D + c * 4;
+            v = *reinterpret_cast<const float4*>((r < BM ? p.q : p.p) + off);
+            if (r < BM) {
+                v.x *= p.scale;
+                v.y *= p.scale;
+                v.z *= p.scale;
+                v.w *= p.scale;
+            }
+        }
+        *reinterpret_cast<float4*>(QP + r * LD + c * 4) = v;
+    }
+    // kbar . p per row: warp w takes rows w, w + 8, ...
+    for (int r = warp; r < BM; r += Cfg::THREADS / 32) {
+        const int i = ib + r;
+        float part = 0.f;
+        if (i < p.N) {
+            const size_t off = (bh * p.N + i) * D;
+            for (int x = lane; x < D; x += 32) part = fmaf(p.kbar[off + x], p.p[off + x], part);
+        }
+        part = warp_sum(part);
+        if (lane == 0) s_kp[r] = part;
+    }
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    int any_local = tid < BM ? s_act[tid] : 0;
+    if (!__syncthreads_or(any_local)) return;             // every row of the block has stopped
+
+    const int kmax = min(ib + BM, p.N) - 1;
+    const int n_tiles = kmax / BK + 1;
+    auto issue = [&](int t) {                             // warp 0, all lanes
+        const int j0 = t * BK;
+        const int nk = min(BK, kmax + 1 - j0);
+        if (lane == 0) mbar_arrive_expect_tx(&full[t & 1], static_cast<uint32_t>(nk) * D * 4);
+        __syncwarp();
+        if (lane < nk)
+            bulk_g2s(stage + (t & 1) * BK * LD + lane * LD, K + static_cast<size_t>(j0 + lane) * D, D * 4,
+                     &full[t & 1]);
+    };
+    if (warp == 0) issue(0);
+
+    // phase-1 and phase-2 thread coordinates
+    const int rg = tid >> 3, kg = tid & 7;               // rows {rg, rg+32} (+ their p rows), keys kg + 8 jj
+    const int rgrp = tid >> 4, dgrp = tid & 15;          // rows rgrp + 16 i, dims dgrp * DG ..
+    float U[4][DG];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int x = 0; x < DG; ++x) U[i][x] = 0.f;
+    const float lse0 = s_lse[rg], lse1 = s_lse[rg + 32];
+    const float kp0 = s_kp[rg], kp1 = s_kp[rg + 32];
+    const bool act0 = s_act[rg] != 0, act1 = s_act[rg + 32] != 0;
+    int last_issued = 0;
+
+    for (int t = 0; t < n_tiles; ++t) {
+        if (warp == 0 && t + 1 < n_tiles) {              // that buffer was released at the last barrier
+            issue(t + 1);
+            last_issued = t + 1;
+        }
+        if (!mbar_wait(&full[t & 1], (t >> 1) & 1)) {
+            atomicOr(&g_plx_status, PLX_DEV_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        const float* kt = stage + (t & 1) * BK * LD;
+        const int j0 = t * BK;
+        const int nk = min(BK, kmax + 1 - j0);
+        // phase 1: acc[m][jj], m = 0, 1: s of rows rg, rg+32; m = 2, 3: p.k of the same rows
+        float acc[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) acc[m][jj] = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < D; c += 4) {
+            float4 a[4], b[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) a[m] = *reinterpret_cast<const float4*>(QP + (rg + 32 * m) * LD + c);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) b[jj] = *reinterpret_cast<const float4*>(kt + (kg + 8 * jj) * LD + c);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    acc[m][jj] = fmaf(a[m].x, b[jj].x, acc[m][jj]);
+                    acc[m][jj] = fmaf(a[m].y, b[jj].y, acc[m][jj]);
+                    acc[m][jj] = fmaf(a[m].z, b[jj].z, acc[m][jj]);
+                    acc[m][jj] = fmaf(a[m].w, b[jj].w, acc[m][jj]);
+                }
+        }
+        // G for rows rg, rg + 32 and keys kg + 8 jj (0 for stopped rows, keys past the row or the tile)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int kk = kg + 8 * jj, j = j0 + kk;
+            const bool in = kk < nk;
+            const float g0 = (in && act0 && j <= ib + rg) ? expf(acc[0][jj] - lse0) * (acc[2][jj] - kp0) : 0.f;
+            const float g1 = (in && act1 && j <= ib + rg + 32) ? expf(acc[1][jj] - lse1) * (acc[3][jj] - kp1) : 0.f;
+            Gs[kk * GLD + (rg & 15) * 4 + (rg >> 4)] = g0;
+            Gs[kk * GLD + (rg & 15) * 4 + ((rg + 32) >> 4)] = g1;
+        }
+        __syncthreads();
+        // phase 2: U[rows rgrp + 16 i][dims dgrp * DG ..] += G K
+        if (!*abort_flag) {
+#pragma unroll 2
+            for (int kk = 0; kk < nk; ++kk) {
+                const float4 g = *reinterpret_cast<const float4*>(Gs + kk * GLD + rgrp * 4);
+                float kv[DG];
+#pragma unroll
+                for (int x = 0; x < DG; x += 4) {
+                    const float4 k4 = *reinterpret_cast<const float4*>(kt + kk * LD + dgrp * DG + x);
+                    kv[x] = k4.x;
+                    kv[x + 1] = k4.y;
+                    kv[x + 2] = k4.z;
+                    kv[x + 3] = k4.w;
+                }
+#pragma unroll
+                for (int x = 0; x < DG; ++x) {
+                    U[0][x] = fmaf(g.x, kv[x], U[0][x]);
+                    U[1][x] = fmaf(g.y, kv[x], U[1][x]);
+                    U[2][x] = fmaf(g.z, kv[x], U[2][x]);
+                    U[3][x] = fmaf(g.w, kv[x], U[3][x]);
+                }
+            }
+        }
+        __syncthreads();                                  // G and this tile buffer may be reused
+        if (*abort_flag) break;
+    }
+    // no copy may still be in flight when the block exits (only after an abort)
+    if (warp == 0 && lane == 0 && *abort_flag) mbar_wait(&full[last_issued & 1], (last_issued >> 1) & 1);
+    if (*abort_flag) return;
+
+    // ---- Ap = U + lambda p and one conjugate-gradient step per active row.  A
+    // row's 16 threads are one half-warp and the two half-warps of a warp may
+    // hold rows in different states, so every lane runs the shuffles and only
+    // the loads and stores depend on the row's state.
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int a = rgrp + 16 * i;
+        const bool act = s_act[a] != 0;                   // implies ib + a < N
+        const size_t row = bh * p.N + ib + a;
+        const float* prow = QP + (BM + a) * LD + dgrp * DG;
+        float pv[DG], pap = 0.f;
+#pragma unroll
+        for (int x = 0; x < DG; ++x) {
+            pv[x] = prow[x];
+            U[i][x] = fmaf(p.lambda, pv[x], U[i][x]);
+            pap = fmaf(pv[x], U[i][x], pap);
+        }
+#pragma unroll
+        for (int m = 8; m >= 1; m >>= 1) pap += __shfl_xor_sync(0xffffffffu, pap, m);
+        const bool ok = act && pap > 0.f;
+        if (act && !ok && dgrp == 0) p.rs[row] = 0.f;      // breakdown: stop the row
+        const float rs = s_rs[a];
+        const float alpha = ok ? rs / pap : 0.f;
+        float xv[DG], rv[DG], rn = 0.f;
+#pragma unroll
+        for (int x = 0; x < DG; ++x) {
+            xv[x] = 0.f;
+            rv[x] = 0.f;
+        }
+        if (ok) {
+            const float* xo = p.x + row * D + dgrp * DG;
+            const float* ro = p.r + row * D + dgrp * DG;
+#pragma unroll
+            for (int x = 0; x < DG; x += 4) {
+                const float4 x4 = *reinterpret_cast<const float4*>(xo + x);
+                const float4 r4 = *reinterpret_cast<const float4*>(ro + x);
+                xv[x] = x4.x; xv[x + 1] = x4.y; xv[x + 2] = x4.z; xv[x + 3] = x4.w;
+                rv[x] = r4.x; rv[x + 1] = r4.y; rv[x + 2] = r4.z; rv[x + 3] = r4.w;
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < DG; ++x) {
+            xv[x] = fmaf(alpha, pv[x], xv[x]);
+            rv[x] = fmaf(-alpha, U[i][x], rv[x]);
+            rn = fmaf(rv[x], rv[x], rn);
+        }
+#pragma unroll
+        for (int m = 8; m >= 1; m >>= 1) rn += __shfl_xor_sync(0xffffffffu, rn, m);
+        if (ok) {
+            const float beta = rn / rs;
+            float* xo = p.x + row * D + dgrp * DG;
+            float* ro = p.r + row * D + dgrp * DG;
+            float* po = p.p + row * D + dgrp * DG;
+#pragma unroll
+            for (int x = 0; x < DG; x += 4) {
+                *reinterpret_cast<float4*>(xo + x) = make_float4(xv[x], xv[x + 1], xv[x + 2], xv[x + 3]);
+                *reinterpret_cast<float4*>(ro + x) = make_float4(rv[x], rv[x + 1], rv[x + 2], rv[x + 3]);
+                *reinterpret_cast<float4*>(po + x) =
+                    make_float4(fmaf(beta, pv[x], rv[x]), fmaf(beta, pv[x + 1], rv[x + 1]),
+                                fmaf(beta, pv[x + 2], rv[x + 2]), fmaf(beta, pv[x + 3], rv[x + 3]));
+            }
+            if (dgrp == 0) {
+                p.rs[row] = rn;
+                p.steps[row] += 1;
+            }
+        }
+    }
+}
+
 // Parallax's output with the solved probe, in centred form (4 rows per warp,
 // the same butterfly): with r'_j = k_j . rho - kbar . rho = (k_j - kbar) . rho,
 //   o = vbar - Sigma_KV rho = sum_j w_j (1 - r'_j) v_j + vbar sum_j w_j r'_j,

@@ -82,6 +82,8 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, false, plx::BWD_DQ>, BwdTcCfg<64, false, plx::BWD_DQ>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, true, plx::BWD_DKV>, BwdTcCfg<64, true, plx::BWD_DKV>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, false, plx::BWD_DKV>, BwdTcCfg<64, false, plx::BWD_DKV>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<128>, plx::LlaGemmCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<64>, plx::LlaGemmCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_proj_tc_kernel<128>, ProjCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_proj_tc_kernel<64>, ProjCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_decode_split_kernel<128, true>, DecodeCfg<128>::SMEM);
@@ -358,8 +360,16 @@ void launch_lla(const float* q, const float* k, const float* v, float* out, floa
     plx::LlaParams lp{q, k, w.kbar, w.lse, w.x, w.r, w.p, w.rs, w.rs0, w.steps, N, scale, lambda, tol * tol};
     dim3 grid((N + plx::LLA_ROWS_PER_BLOCK - 1) / plx::LLA_ROWS_PER_BLOCK, static_cast<unsigned>(BH));
     plx::plx_lla_init_kernel<DPL><<<grid, plx::LLA_WARPS * 32, 0, s>>>(lp);
-    for (int it = 0; it < max_iters; ++it)
-        plx::plx_lla_cg_step_kernel<DPL><<<grid, plx::LLA_WARPS * 32, plx::LlaTile<DPL>::SMEM, s>>>(lp);
+    if constexpr (DPL == 2 || DPL == 4) {
+        // d = 64, 128: the step as two block GEMMs per key tile
+        using G = plx::LlaGemmCfg<DPL * 32>;
+        dim3 ggrid((N + G::BM - 1) / G::BM, static_cast<unsigned>(BH));
+        for (int it = 0; it < max_iters; ++it)
+            plx::plx_lla_cg_gemm_kernel<DPL * 32><<<ggrid, G::THREADS, G::SMEM, s>>>(lp);
+    } else {
+        for (int it = 0; it < max_iters; ++it)
+            plx::plx_lla_cg_step_kernel<DPL><<<grid, plx::LLA_WARPS * 32, plx::LlaTile<DPL>::SMEM, s>>>(lp);
+    }
     plx::plx_lla_out_kernel<DPL><<<grid, plx::LLA_WARPS * 32, 0, s>>>(lp, v, out, lse);
 }
 
@@ -832,6 +842,7 @@ plx_status plx_lla_f32(const float* q, const float* k, const float* v, float* ou
         if (BH > 65535) return PLX_ERR_UNSUPPORTED;
         const long long R = BH * N;
         if (!workspace || workspace_bytes < lla_ws_bytes(R, d)) return PLX_ERR_WORKSPACE;
+        if (!device_info()) return PLX_ERR_CUDA;          // kernel attributes (shared-memory sizes)
         const LlaWorkspace w = lla_ws_carve(workspace, R, d);
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         switch (d / 32) {
