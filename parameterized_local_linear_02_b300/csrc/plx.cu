@@ -215,20 +215,25 @@ plx_status launch_proj_tc(const void* x, const void* w_r, void* rho, int B, int 
     const long long n_mt = (N + Cfg::BM - 1) / Cfg::BM;
     const long long n_hg = (static_cast<long long>(H) * D + Cfg::BN - 1) / Cfg::BN;
     const long long n_items = static_cast<long long>(B) * n_mt * n_hg;
-    if (n_items > INT_MAX || static_cast<long long>(H) * D > INT_MAX) return PLX_ERR_UNSUPPORTED;
-    CUtensorMap mx, mw, mo;
+    if (2 * n_items > INT_MAX || static_cast<long long>(H) * D > INT_MAX) return PLX_ERR_UNSUPPORTED;
+    CUtensorMap mx, mw, mw2, mo;
     if (!make_map(&mx, x, Dx, N, B, Cfg::BM) || !make_map(&mw, w_r, Dx, H * D, 1, Cfg::BN) ||
+        !make_map(&mw2, w_r, Dx, H * D, 1, Cfg::BN / 2) ||
         !make_out_map(&mo, rho, D, N, static_cast<long long>(B) * H, false))
         return PLX_ERR_CUDA;
+    const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
+    // the last wave's items run as two half items when they fill at most half the grid
+    const long long tail = n_items % grid;
+    const bool split = n_items > grid && tail > 0 && 2 * tail <= grid;
     plx::ProjParams p;
     p.N = N;
     p.H = H;
     p.n_kb = (Dx + Cfg::BK - 1) / Cfg::BK;
     p.n_mt = static_cast<int>(n_mt);
     p.n_hg = static_cast<int>(n_hg);
-    p.n_items = static_cast<int>(n_items);
-    const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
-    plx::plx_proj_tc_kernel<D><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mx, mw, mo, p);
+    p.n_full = static_cast<int>(split ? n_items - tail : n_items);
+    p.n_items = static_cast<int>(split ? n_items + tail : n_items);
+    plx::plx_proj_tc_kernel<D><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mx, mw, mw2, mo, p);
     return launch_status();
 }
 

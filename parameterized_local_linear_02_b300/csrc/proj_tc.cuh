@@ -15,6 +15,11 @@
 // tile, so the CTAs running at one time read each X tile from L2 several
 // times and from HBM once; W_R stays in L2.
 //
+// Tail split: when the items left for the last wave would fill at most half
+// of the CTAs, each of them runs as two half items of 128 columns (W_R
+// through a 128-row box), so the last wave takes about two thirds of an item
+// time instead of one and no CTA idles for a whole item.
+//
 // Roles (192 threads, one CTA per SM):
 //   warp 0      TMA producer (one lane): X and W tiles through an NSTAGE ring.
 //   warp 1      TMEM owner and MMA issuer (whole warp, elected lane).  Two
@@ -54,13 +59,16 @@ struct ProjCfg {
 };
 
 struct ProjParams {
-    int N, H, n_kb, n_mt, n_hg, n_items;
+    int N, H, n_kb, n_mt, n_hg;
+    int n_full;      // items 0 .. n_full - 1 are whole (256 columns)
+    int n_items;     // n_full + 2 x (split items): item n_full + 2 s + h is half h of item n_full + s
 };
 
 template <int D>
 __global__ void __launch_bounds__(ProjCfg<D>::THREADS, 1)
 plx_proj_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
-                   const __grid_constant__ CUtensorMap mapO, const ProjParams p) {
+                   const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapO,
+                   const ProjParams p) {
     using Cfg = ProjCfg<D>;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, NSTAGE = Cfg::NSTAGE;
     extern __shared__ uint8_t smem_raw[];
@@ -94,6 +102,7 @@ plx_proj_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_consta
         fence_mbar_init();
         tma_prefetch_desc(&mapX);
         tma_prefetch_desc(&mapW);
+        tma_prefetch_desc(&mapW2);
         tma_prefetch_desc(&mapO);
     }
     tc_fence_before();
@@ -105,8 +114,14 @@ plx_proj_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_consta
         atomicOr(&g_plx_status, PLX_DEV_ERR_TIMEOUT);
         *abort_flag = 1;
     };
-    // item u -> column group hg (fastest), token tile mt, batch b
-    auto item = [&](int u, int& b, int& mt, int& hg) {
+    // item u -> column group hg (fastest), token tile mt, batch b, and which
+    // columns of the group: half = -1 for all 256, else 128 * half .. + 127
+    auto item = [&](int u, int& b, int& mt, int& hg, int& half) {
+        half = -1;
+        if (u >= p.n_full) {
+            half = (u - p.n_full) & 1;
+            u = p.n_full + ((u - p.n_full) >> 1);
+        }
         hg = u % p.n_hg;
         const int bm = u / p.n_hg;
         mt = bm % p.n_mt;
@@ -123,15 +138,19 @@ plx_proj_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_consta
             bool ok = true;
             for (int u = c; u < p.n_items && ok; u += G) {
                 if (*abort_flag) break;
-                int b, mt, hg;
-                item(u, b, mt, hg);
+                int b, mt, hg, half;
+                item(u, b, mt, hg, half);
+                const uint32_t bytes = half < 0 ? Cfg::STAGE_BYTES : Cfg::X_TILE + Cfg::W_TILE / 2;
                 for (int kb = 0; kb < p.n_kb; ++kb, ++it) {
                     const int s = it % NSTAGE;
                     if (it >= NSTAGE && !mbar_wait(&empty[s], ((it / NSTAGE) - 1) & 1)) { ok = false; break; }
                     uint8_t* st = smem + Cfg::OFF_STAGE + s * Cfg::STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+                    mbar_arrive_expect_tx(&full[s], bytes);
                     tma_load_3d(st, &mapX, &full[s], kb * Cfg::BK, mt * BM, b);
-                    tma_load_3d(st + Cfg::X_TILE, &mapW, &full[s], kb * Cfg::BK, hg * BN, 0);
+                    if (half < 0)
+                        tma_load_3d(st + Cfg::X_TILE, &mapW, &full[s], kb * Cfg::BK, hg * BN, 0);
+                    else
+                        tma_load_3d(st + Cfg::X_TILE, &mapW2, &full[s], kb * Cfg::BK, hg * BN + half * (BN / 2), 0);
                 }
             }
             if (!ok) fail();
@@ -141,12 +160,14 @@ plx_proj_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_consta
         }
     } else if (warp == 1) {
         // ===================================================== MMA issuer (whole warp)
-        constexpr uint32_t ID = idesc_bf16_f32(BM, BN, false, false);
+        constexpr uint32_t ID_FULL = idesc_bf16_f32(BM, BN, false, false);
+        constexpr uint32_t ID_HALF = idesc_bf16_f32(BM, BN / 2, false, false);
         const uint32_t sBase = smem_u32(smem + Cfg::OFF_STAGE);
         int it = 0, n = 0;
         bool ok = true;
         for (int u = c; u < p.n_items && ok; u += G, ++n) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            const uint32_t ID = u < p.n_full ? ID_FULL : ID_HALF;
             const int ab = n & 1;
             // the epilogue has read this accumulator's previous item (item n - 2)
             if (n >= 2 && !wait_warp(&acc_empty[ab], ((n >> 1) - 1) & 1)) { ok = false; break; }
@@ -179,16 +200,18 @@ plx_proj_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_consta
         bool ok = true;
         for (int u = c; u < p.n_items; u += G, ++n) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            int b, mt, hg;
-            item(u, b, mt, hg);
+            int b, mt, hg, half;
+            item(u, b, mt, hg, half);
             const int ab = n & 1;
             if (!wait_warp(&acc_full[ab], (n >> 1) & 1)) { ok = false; break; }
             tc_fence_after();
             const int y = mt * BM + quad * 32;
+            const int col0 = half < 0 ? 0 : half * (BN / 2);     // first group column of this item
+            const int ncol = half < 0 ? BN : BN / 2;
             if (y < p.N) {
 #pragma unroll 1
-                for (int cb = 0; cb < BN; cb += 32) {
-                    const int head = hg * Cfg::HPI + cb / D;
+                for (int cb = 0; cb < ncol; cb += 32) {
+                    const int head = hg * Cfg::HPI + (col0 + cb) / D;
                     if (head >= p.H) break;
                     uint32_t v[32];
                     tmem_ld32x32b_x32(lane_addr + ab * BN + cb, v);
@@ -208,7 +231,7 @@ plx_proj_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_consta
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_3d(&mapO, slot, cb % D, y, b * p.H + head);
+                        tma_store_3d(&mapO, slot, (col0 + cb) % D, y, b * p.H + head);
                         bulk_commit_group();
                     }
                     ++issued;

@@ -50,6 +50,11 @@ def check(got, ref, absdot, Dx, what, min_exact=0.98):
     (1, 1, 1, 64, 8),          # one token, one head, Dx = 8
     (2, 2048, 16, 128, 256),   # 256 items: several items per CTA, both accumulators reused
     (3, 77, 2, 64, 1032),      # Dx of 17 stages (one of 8 columns), tiny N
+    # more items than CTAs with a last wave of at most half the grid: those items run as two
+    # 128-column halves (148 SMs: 160 items -> 148 whole + 24 halves; 152 -> 148 + 8)
+    (2, 1280, 16, 128, 128),
+    (2, 2048, 20, 64, 64),     # d = 64: each half holds two heads
+    (4, 2432, 3, 128, 64),     # H d = 384: the second half of the last group lies past H
 ])
 def test_proj_matches_oracle(shape):
     B, N, H, d, Dx = shape
