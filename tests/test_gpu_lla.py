@@ -35,7 +35,9 @@ def inputs(B, H, N, d, seed):
 
 
 @pytest.mark.parametrize("shape,lam", [((1, 2, 70, 64), 0.1), ((2, 1, 129, 128), 0.05), ((1, 1, 1, 32), 0.1),
-                                       ((1, 1, 40, 96), 0.5)])
+                                       ((1, 1, 40, 96), 0.5),
+                                       # the block-GEMM step (d = 64, 128) on one partial tile
+                                       ((1, 1, 1, 128), 0.1), ((2, 3, 5, 64), 0.2), ((1, 2, 64, 128), 0.1)])
 def test_lla_iteration_matched(shape, lam):
     """tol = 0, 3 steps.  Rows with a prefix of at least 9 keys take all 3
     steps in both precisions and must match the fp64 CG to fp32 accuracy.
