@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(LLA_WARPS * 32) plx_lla_cg_step_kernel(const L
 //             registers and writes it to shared memory;
 //   phase 2   U += G K                    (64 rows x d, K = 32 keys)
 //             thread (rgrp, dgrp) accumulates rows {rgrp + 16 i} x dims
-//             dgrp * d/16 .. + d/16 in registers across all tiles.
+//             {dgrp * 4 + 64 h + e} in registers across all tiles.
 // The key rows of a tile arrive by one 1-D bulk copy each into a row-padded
 // buffer (row stride d + 4 floats), so 8 consecutive keys read at the same
 // dims fall in 8 different bank groups.  Two tile buffers: the copy of tile
@@ -439,7 +439,9 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
 
     // phase-1 and phase-2 thread coordinates
     const int rg = tid >> 3, kg = tid & 7;               // rows {rg, rg+32} (+ their p rows), keys kg + 8 jj
-    const int rgrp = tid >> 4, dgrp = tid & 15;          // rows rgrp + 16 i, dims dgrp * DG ..
+    // rows rgrp + 16 i; dims dgrp * 4 + 64 h + e: the 8 lanes of a quarter-warp read
+    // 128 contiguous bytes of a key row, so phase 2's loads are free of bank conflicts
+    const int rgrp = tid >> 4, dgrp = tid & 15;
     float U[4][DG];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -496,7 +498,7 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
             Gs[kk * GLD + (rg & 15) * 4 + ((rg + 32) >> 4)] = g1;
         }
         __syncthreads();
-        // phase 2: U[rows rgrp + 16 i][dims dgrp * DG ..] += G K
+        // phase 2: U[rows rgrp + 16 i][dims dgrp * 4 + 64 h + e] += G K
         if (!*abort_flag) {
 #pragma unroll 2
             for (int kk = 0; kk < nk; ++kk) {
@@ -504,7 +506,7 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
                 float kv[DG];
 #pragma unroll
                 for (int x = 0; x < DG; x += 4) {
-                    const float4 k4 = *reinterpret_cast<const float4*>(kt + kk * LD + dgrp * DG + x);
+                    const float4 k4 = *reinterpret_cast<const float4*>(kt + kk * LD + dgrp * 4 + 16 * x);
                     kv[x] = k4.x;
                     kv[x + 1] = k4.y;
                     kv[x + 2] = k4.z;
@@ -535,11 +537,18 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
         const int a = rgrp + 16 * i;
         const bool act = s_act[a] != 0;                   // implies ib + a < N
         const size_t row = bh * p.N + ib + a;
-        const float* prow = QP + (BM + a) * LD + dgrp * DG;
+        const float* prow = QP + (BM + a) * LD + dgrp * 4;
         float pv[DG], pap = 0.f;
 #pragma unroll
+        for (int x = 0; x < DG; x += 4) {
+            const float4 p4 = *reinterpret_cast<const float4*>(prow + 16 * x);
+            pv[x] = p4.x;
+            pv[x + 1] = p4.y;
+            pv[x + 2] = p4.z;
+            pv[x + 3] = p4.w;
+        }
+#pragma unroll
         for (int x = 0; x < DG; ++x) {
-            pv[x] = prow[x];
             U[i][x] = fmaf(p.lambda, pv[x], U[i][x]);
             pap = fmaf(pv[x], U[i][x], pap);
         }
@@ -556,12 +565,12 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
             rv[x] = 0.f;
         }
         if (ok) {
-            const float* xo = p.x + row * D + dgrp * DG;
-            const float* ro = p.r + row * D + dgrp * DG;
+            const float* xo = p.x + row * D + dgrp * 4;
+            const float* ro = p.r + row * D + dgrp * 4;
 #pragma unroll
             for (int x = 0; x < DG; x += 4) {
-                const float4 x4 = *reinterpret_cast<const float4*>(xo + x);
-                const float4 r4 = *reinterpret_cast<const float4*>(ro + x);
+                const float4 x4 = *reinterpret_cast<const float4*>(xo + 16 * x);
+                const float4 r4 = *reinterpret_cast<const float4*>(ro + 16 * x);
                 xv[x] = x4.x; xv[x + 1] = x4.y; xv[x + 2] = x4.z; xv[x + 3] = x4.w;
                 rv[x] = r4.x; rv[x + 1] = r4.y; rv[x + 2] = r4.z; rv[x + 3] = r4.w;
             }
@@ -576,14 +585,14 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
         for (int m = 8; m >= 1; m >>= 1) rn += __shfl_xor_sync(0xffffffffu, rn, m);
         if (ok) {
             const float beta = rn / rs;
-            float* xo = p.x + row * D + dgrp * DG;
-            float* ro = p.r + row * D + dgrp * DG;
-            float* po = p.p + row * D + dgrp * DG;
+            float* xo = p.x + row * D + dgrp * 4;
+            float* ro = p.r + row * D + dgrp * 4;
+            float* po = p.p + row * D + dgrp * 4;
 #pragma unroll
             for (int x = 0; x < DG; x += 4) {
-                *reinterpret_cast<float4*>(xo + x) = make_float4(xv[x], xv[x + 1], xv[x + 2], xv[x + 3]);
-                *reinterpret_cast<float4*>(ro + x) = make_float4(rv[x], rv[x + 1], rv[x + 2], rv[x + 3]);
-                *reinterpret_cast<float4*>(po + x) =
+                *reinterpret_cast<float4*>(xo + 16 * x) = make_float4(xv[x], xv[x + 1], xv[x + 2], xv[x + 3]);
+                *reinterpret_cast<float4*>(ro + 16 * x) = make_float4(rv[x], rv[x + 1], rv[x + 2], rv[x + 3]);
+                *reinterpret_cast<float4*>(po + 16 * x) =
                     make_float4(fmaf(beta, pv[x], rv[x]), fmaf(beta, pv[x + 1], rv[x + 1]),
                                 fmaf(beta, pv[x + 2], rv[x + 2]), fmaf(beta, pv[x + 3], rv[x + 3]));
             }
