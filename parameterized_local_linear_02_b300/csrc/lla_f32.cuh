@@ -16,10 +16,12 @@
 // The library runs it as a sequence of launches on one stream:
 //   1. plx_fwd_f32_kernel<., false> with v := k: kbar_i and lse_i;
 //   2. plx_lla_init_kernel: x = 0, r = p = mu, rs = rs0 = mu . mu;
-//   3. max_iters x plx_lla_cg_step_kernel: one conjugate-gradient step per
-//      row, Sigma_KK p formed by streaming the keys once per 4 rows (weights
-//      from the stored lse, no online rescaling), the update done in
-//      registers; a row stops once r . r <= tol^2 rs0 (or when p . Ap <= 0);
+//   3. max_iters conjugate-gradient steps, one launch each: Sigma_KK p formed
+//      by streaming the keys once per block of rows (weights from the stored
+//      lse, no online rescaling), the update done in registers; a row stops
+//      once r . r <= tol^2 rs0 (or when p . Ap <= 0).  d = 64, 128:
+//      plx_lla_cg_gemm_kernel (two block-level GEMMs per key tile, 64 rows a
+//      block); other d: plx_lla_cg_step_kernel (4 rows a warp);
 //   4. plx_lla_out_kernel: o from Parallax's output formula with rho := x,
 //      in centred form.
 // The pages warn that the solve is unstable in low precision; every step
