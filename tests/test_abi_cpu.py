@@ -226,3 +226,24 @@ def test_lla_rejects_bad_arguments_before_launch():
     assert lib.plx_lla_f32(*args(WS, need - 256, 64, 0.1, 8, 0.0)) == 6             # workspace too small
     assert lib.plx_lla_f32(*args(ctypes.c_void_p(0x100010), need, 64, 0.1, 8, 0.0)) == 3   # misaligned workspace
     assert lib.plx_lla_f32(None, P, P, P, None, None, None, WS, need, 2, 3, 64, 64, 0.1, 0.1, 8, 0.0, None) == 1
+
+
+def test_no_cpu_fallback_without_a_device():
+    """With no CUDA device every entry point raises; none computes on the host.
+    (Skipped on a GPU host: CPU tensors must never reach the library there.)"""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("checks the behaviour without a CUDA device")
+    x = torch.zeros((1, 64, 64), dtype=torch.bfloat16)
+    w = torch.zeros((128, 64), dtype=torch.bfloat16)
+    qb = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16)
+    qf = torch.zeros((1, 1, 8, 64), dtype=torch.float32)
+    calls = [
+        lambda: plx.plx_probe_proj(x, w, heads=1),
+        lambda: plx.plx_lla_f32(qf, qf, qf, lam=0.1, max_iters=1),
+        lambda: plx.plx_fwd(qb, qb, qb, qb),
+        lambda: plx.plx_bwd(qb, qb, qb, qb, qb),
+    ]
+    for call in calls:
+        with pytest.raises((RuntimeError, plx.PlxError)):
+            call()
