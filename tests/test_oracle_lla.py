@@ -11,10 +11,12 @@ Pins, each fixed independently of the oracle's code:
 - exact recovery of linear data v = a + M k;
 - the softmax limit at large lambda (scipy softmax);
 - the independent C oracle's explicit Parallax form fed the solved probe;
-- conjugate gradients after d steps equal the direct solve.
+- conjugate gradients after d steps equal the direct solve;
+- affinity in v: shifting every value by a shifts o by a.
 
-Planted mistakes (a flipped mu, an uncentred key moment, the ridge on the
-wrong side, an unweighted moment, a CG sign slip) each fail one of them."""
+Planted mistakes each fail one of them: a flipped mu, an uncentred key
+moment, the ridge on the wrong side, an unweighted moment, a CG sign slip, a
+transposed value-key covariance, an output without its vbar term."""
 import types
 
 import numpy as np
@@ -101,8 +103,20 @@ def pin_cg_reaches_the_solve(mod):
     assert int(cg[3].max()) <= 4
 
 
+def pin_value_shift(mod):
+    """The fit's intercept is affine in the values: v_j + a gives o + a, and
+    rho* (a function of q and k only) does not change."""
+    rng = np.random.default_rng(37)
+    q, k, v = _inputs(rng, 1, 1, 9, 3)
+    a = rng.standard_normal(3)
+    o1, r1, _ = mod.lla_direct(q, k, v, 0.7, 0.2)[(0, 0)]
+    o2, r2, _ = mod.lla_direct(q, k, v + a, 0.7, 0.2)[(0, 0)]
+    np.testing.assert_allclose(o2, o1 + a, rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(r2, r1, rtol=1e-12, atol=1e-12)
+
+
 PINS = [pin_ridge_least_squares, pin_linear_data, pin_softmax_limit, pin_parallax_with_solved_probe,
-        pin_cg_reaches_the_solve]
+        pin_cg_reaches_the_solve, pin_value_shift]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -129,6 +143,7 @@ MUTANTS = {
     "unweighted_key_moment": ("S = (kc * w[:, None]).T @ kc", "S = kc.T @ kc / len(w)"),
     "cg_residual_sign": ("r = r - alpha * Ap", "r = r + alpha * Ap"),
     "value_covariance_transposed": ("C = (vc * w[:, None]).T @ kc", "C = (kc * w[:, None]).T @ vc"),
+    "output_drops_vbar": ("o[n] = vbar - C @ rho[n]", "o[n] = -(C @ rho[n])"),
 }
 
 
