@@ -5,6 +5,9 @@ One step = one pass of the whole hot path on HBM-resident synthetic inputs:
   * plx_fwd on the prefill workload B=4, H=16, N=2048, d=128 (bf16, causal,
     rho = W_R x), outputs o and lse in fp32 (bf16 storage of o would add
     rounding beyond the parity tolerance on rows where |o| is far above its RMS);
+  * plx_fwd on the long-sequence prefill B=2, H=16, N=8192, d=128 (bf16,
+    planted keys, rho ~ N(0, 0.1^2)), fp32 o and lse, reported in its own
+    block with its own roofline;
   * plx_decode on the decode workload B=64, H=16, d=128, bf16 KV cache with
     every length 4096 (split-KV + LSE combine).
 The headline value is prefill TFLOP/s, counting 8*d flop per causal
@@ -42,6 +45,7 @@ if ROOT not in sys.path:
 
 METRIC = "PLX prefill TFLOP/s and decode KV GB/s vs B300 roofline, 1 GPU"
 PREFILL = "prefill_b4_h16_n2048_d128"
+PREFILL_LONG = "prefill_b2_h16_n8192_d128_planted"
 DECODE = "decode_b64_h16_ctx4096_d128"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
@@ -272,6 +276,7 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     peaks = read_peaks()
     do_pf = args.only in ("both", "prefill")
+    do_long = args.only in ("both", "long") and not args.no_long
     do_dec = args.only in ("both", "decode")
     extras = not args.no_extras
 
@@ -286,6 +291,15 @@ def run_ours(args, world, rank, local):
         t = x.device_tensors(dev)
         out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    lc = plx_inputs.CONFIGS[PREFILL_LONG]
+    Bl, Hl, Nl, dl = lc["B"], lc["H"], lc["N"], lc["d"]
+    if do_long:
+        xl = plx_inputs.prefill(Bl, Hl, Nl, dl, seed=rank_seed(lc["seed"], rank), dtype="bf16", rho=lc["rho"],
+                                rho_std=lc["rho_std"], keys=lc["keys"])
+        tl = xl.device_tensors(dev)
+        del xl
+        out_l = torch.empty((Bl, Hl, Nl, dl), dtype=torch.float32, device=dev)
+        lse_l = torch.empty((Bl, Hl, Nl), dtype=torch.float32, device=dev)
     if do_dec:
         dd = plx_inputs.decode_device(Bd, Hd, dc["d"], S_cap, seed=rank_seed(dc["seed"], rank), seqlens=dc["seqlens"],
                                       rho_std=dc["rho_std"], device=dev)
@@ -299,11 +313,14 @@ def run_ours(args, world, rank, local):
     def fwd(rho=True):
         plx.plx_fwd(t["q"], t["k"], t["v"], t["rho"] if rho else None, out=out, lse=lse)
 
+    def fwd_long(rho=True):
+        plx.plx_fwd(tl["q"], tl["k"], tl["v"], tl["rho"] if rho else None, out=out_l, lse=lse_l)
+
     def dec(rho=True):
         plx.plx_decode(dd["q"], dd["rho"] if rho else None, dd["k_cache"], dd["v_cache"], dd["seqlens"],
                        num_splits=splits, workspace=ws, out=dout, lse=dlse)
 
-    launches_per_step = (1 if do_pf else 0) + ((2 if splits > 1 else 1) if do_dec else 0)
+    launches_per_step = (1 if do_pf else 0) + (1 if do_long else 0) + ((2 if splits > 1 else 1) if do_dec else 0)
 
     def timed(fn, k):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
@@ -318,6 +335,8 @@ def run_ours(args, world, rank, local):
         flush.zero_()
         if do_pf:
             fwd()
+        if do_long:
+            fwd_long()
         if do_dec:
             dec()
     torch.cuda.synchronize()
@@ -330,13 +349,15 @@ def run_ours(args, world, rank, local):
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    ev_f, ev_d = [], []
+    ev_f, ev_l, ev_d = [], [], []
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for _ in range(args.steps):
         if do_pf:
             ev_f += timed(fwd, 1)
+        if do_long:
+            ev_l += timed(fwd_long, 1)
         if do_dec:
             ev_d += timed(dec, 1)
     t_end.record(stream)
@@ -362,6 +383,22 @@ def run_ours(args, world, rank, local):
             "peak_source": f"{peaks['source']} bf16 dense (burst)",
             "frac_of_sustained": value / world / peaks["bf16_tflops_sustained"],
             "kernel": "plx_fwd_tc_kernel<128,true>", "flop_per_launch": flops, "avg_launch_ms": f_avg}
+    if do_long:
+        l_avg = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev_l])), world)
+        l_flops = prefill_flops(Bl, Hl, Nl, dl)
+        l_val = world * l_flops / (l_avg * 1e-3) / 1e12
+        lroof = {"bound": "tensor", "achieved": l_val / world, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                 "frac": l_val / world / peaks["bf16_tflops"],
+                 "traffic": traffic.get("plx_fwd_long", {}).get("bytes_per_launch"),
+                 "peak_source": f"{peaks['source']} bf16 dense (burst)",
+                 "frac_of_sustained": l_val / world / peaks["bf16_tflops_sustained"],
+                 "kernel": "plx_fwd_tc_kernel<128,true>", "flop_per_launch": l_flops, "avg_launch_ms": l_avg}
+        line["prefill_long"] = {"workload": PREFILL_LONG, "value": l_val, "unit": "TFLOP/s", "ms": l_avg,
+                                "B": Bl, "H": Hl, "N": Nl, "d": dl, "keys": "planted (64 centres + N(0, 0.05^2))",
+                                "rho": "N(0, 0.1^2)", "out": "fp32 o + fp32 lse",
+                                "l2": "flushed (256 MiB write) before every launch", "roofline": lroof}
+        if not do_pf:
+            line.update({"value": l_val, "unit": "TFLOP/s", "roofline": lroof})
     if do_dec:
         d_avg = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev_d])), world)
         dbytes = decode_bytes(dd["seqlens_host"], Hd, dc["d"])
@@ -374,12 +411,15 @@ def run_ours(args, world, rank, local):
                  "kernel": "plx_decode_split_kernel<128,true>" + (" + combine" if splits > 1 else "")}
         line["decode"] = {"value": d_gbs, "unit": "GB/s", "ms": d_avg, "batch": Bd, "splits": splits,
                           "tokens_per_s": world * Bd / (d_avg * 1e-3), "roofline": droof}
-        if not do_pf:
+        if not do_pf and not do_long:
             line.update({"value": d_gbs, "unit": "GB/s", "roofline": droof})
-    line["ms_per_step"] = (f_avg if do_pf else 0.0) + (d_avg if do_dec else 0.0)
-    line["config"] = {"workload": PREFILL if do_pf else DECODE, "B": B, "H": H, "N": N, "d": d, "causal": True,
+    line["ms_per_step"] = ((f_avg if do_pf else 0.0) + (l_avg if do_long else 0.0)
+                           + (d_avg if do_dec else 0.0))
+    line["config"] = {"workload": PREFILL if do_pf else (PREFILL_LONG if do_long else DECODE), "B": B, "H": H, "N": N, "d": d, "causal": True,
                       "rho": "W_R x", "out": "fp32 o + fp32 lse",
                       "l2": "flushed (256 MiB write) before every launch"}
+    if do_long:
+        line["config"].update({"long_prefill_workload": PREFILL_LONG})
     if do_dec:
         line["config"].update({"decode_workload": DECODE, "decode_batch": Bd, "decode_splits": splits})
 
@@ -401,6 +441,8 @@ def run_ours(args, world, rank, local):
         sa = {}
         if do_pf:
             sa_f = timed(lambda: fwd(False), max(5, args.steps // 2))
+        if do_long:
+            sa_l = timed(lambda: fwd_long(False), max(3, args.steps // 4))
         if do_dec:
             sa_d = timed(lambda: dec(False), max(5, args.steps // 2))
         torch.cuda.synchronize()
@@ -409,6 +451,11 @@ def run_ours(args, world, rank, local):
             sa.update({"prefill_ms": sa_f_ms,
                        "prefill_tflops_4d": prefill_flops(B, H, N, d, False) / sa_f_ms / 1e9,
                        "plx_over_sa_time": f_avg / sa_f_ms})
+        if do_long:
+            sa_l_ms = float(np.mean([a.elapsed_time(b) for a, b in sa_l]))
+            sa.update({"prefill_long_ms": sa_l_ms,
+                       "prefill_long_tflops_4d": prefill_flops(Bl, Hl, Nl, dl, False) / sa_l_ms / 1e9,
+                       "prefill_long_plx_over_sa_time": l_avg / sa_l_ms})
         if do_dec:
             sa_d_ms = float(np.mean([a.elapsed_time(b) for a, b in sa_d]))
             sa.update({"decode_ms": sa_d_ms,
@@ -856,8 +903,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=("both", "prefill", "decode"), default="both",
-                    help="run one kernel only (profiling of a single kernel)")
+    ap.add_argument("--only", choices=("both", "prefill", "long", "decode"), default="both",
+                    help="run one leg only (profiling of a single kernel); 'both' runs every leg")
+    ap.add_argument("--no-long", action="store_true", help="leave the long-sequence prefill out of the step")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="decode batch (default: the decode workload's 64); smaller for profiling")
     ap.add_argument("--decode-sweep", action="store_true",
