@@ -289,10 +289,10 @@ plx_status plx_decode_family(const void* q, const void* rho, const void* k_cache
 
 /*
  * plx_decode_noalloc -- plx_decode for callers that cannot allocate device
- * memory: code running where cudaMalloc is off limits (inside a host
- * callback, under an allocator that owns all device memory, or in a process
- * that must not grow its footprint after start-up) cannot provide the
- * workspace that plx_decode asks for.  This entry point takes no workspace
+ * memory: code running where cudaMalloc is off limits (under an allocator
+ * that owns all device memory, or in a process that must not grow its
+ * footprint after start-up) cannot provide the workspace that plx_decode
+ * asks for.  This entry point takes no workspace
  * and allocates nothing; the split partials go to a scratch array that the
  * library holds in static device memory, PLX_DECODE_NOALLOC_SCRATCH_BYTES
  * (4 MiB) on every GPU that loads the library, until the process exits.
@@ -302,13 +302,16 @@ plx_status plx_decode_family(const void* q, const void* rho, const void* k_cache
  * it calls with the scratch array as the workspace.
  *   num_splits : 0 picks plx_decode's split count, lowered if needed to the
  *                largest count whose partials fit in the scratch
- *                (B * H * splits * (2 d + 4) * 4 bytes); with more than one
- *                split that needs B * H <= 4032 at d = 128.  An explicit
- *                count whose partials do not fit is rejected with
- *                PLX_ERR_UNSUPPORTED before anything is launched.
+ *                (B * H * splits * (2 d + 4) * 4 bytes <= 4 MiB); two or
+ *                more splits need B * H <= 2016 at d = 128 (B * H <= 3971 at
+ *                d = 64), and above that one split runs, which needs no
+ *                scratch.  An explicit count whose partials do not fit is
+ *                rejected with PLX_ERR_UNSUPPORTED before anything is
+ *                launched.
  * The first call on a device looks up the scratch array's device address
- * (cudaGetSymbolAddress, once per device, with that device current); make
- * that first call before any stream capture.  Every call on a device shares
+ * (cudaGetSymbolAddress, once per device and context, with that device
+ * current); make that first call before any stream capture.  After
+ * cudaDeviceReset the next call looks the address up again.  Every call on a device shares
  * the one array, so calls that may overlap on the GPU (on different streams,
  * or from several host threads) race with each other: order them on one
  * stream.  The array keeps the previous call's partials; nothing in it needs

@@ -26,11 +26,12 @@
 //                frees when its S/R GEMMs finish, a V slot when its PV GEMMs do.
 //   warp 1       TMEM owner and MMA issuer.  The whole warp runs the issue
 //                loop and one elected lane issues each tcgen05 instruction,
-//                so descriptors stay in warp-uniform registers.  The issue
-//                order runs across items without a break: SR_{g+1} before PV_g
-//                for the CTA's global tile index g, so the tensor pipe computes
-//                S/R of the next tile (of this item or the next) while the
-//                softmax works on the current one.
+//                so descriptors stay in warp-uniform registers (one elect.sync
+//                per batch of MMAs).  The issue order runs across items: SR_{g+1}
+//                before PV_g for the CTA's global tile index g, so the tensor
+//                pipe computes S/R of the next tile while the softmax works on
+//                the current one; at an item boundary the item's last PV goes
+//                first, then the next item's S/R as soon as its Q has landed.
 //   warps 2-9    softmax + epilogue, two warps per TMEM lane quadrant
 //                (quadrant = warp % 4, so both sit on the same scheduler):
 //                thread r of the pair owns query row r of the quadrant, the
@@ -39,12 +40,12 @@
 //                per-quadrant mbarrier (bounded waits), once per tile; the
 //                exponentials are taken against the running max while that
 //                handshake is in flight (again only if a row max jumps).
-//                An item's epilogue runs inside the first tile of the CTA's
-//                next item, after that tile's P/PR are stored and before they
-//                are released to the PV GEMM (whose first MMA overwrites O/U):
-//                the item's last PV has long finished by then, and (l, C)
-//                ride on that tile's max handshake.  The output goes through
-//                a swizzled shared-memory chunk per warp and a TMA store.
+//                An item's epilogue runs right after its last tile: the pair
+//                adds its (l, C) through the same handshake, waits for the
+//                item's last PV (issued ahead of the next item's first S/R
+//                GEMMs, which run meanwhile) and writes o through a swizzled
+//                shared-memory chunk per warp and a TMA store, before the next
+//                item's first P (whose PV overwrites O/U) is released.
 //   warps 10-11  V re-encode (bf16 -> fp16, in place) of each V stage as
 //                soon as it lands, off the softmax's critical path; the PV
 //                GEMMs wait for it.
@@ -295,7 +296,10 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         // ===================================================== MMA issuer (whole warp)
         constexpr uint32_t ID_S = idesc_bf16_f32(128, BN, false, false);
         constexpr uint32_t ID_PV = idesc_f16_f32(128, D, false, true);
-        const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sR), sKa = smem_u32(sK), sVa = smem_u32(sV);
+        const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV);
+        // base descriptors of the K-major Q and rho tiles (fixed for the kernel)
+        const uint64_t a_q = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t a_r = sdesc_sw128(smem_u32(sR), 16, 1024);
         auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity));
         };
@@ -307,17 +311,11 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             if (!wait_warp(&v_ready[stage], (pg / NSTAGE) & 1)) return false;
             tc_fence_after();
             const uint32_t tS = tmem + (b ? Cfg::TM_S1 : Cfg::TM_S0);
-            const uint32_t tR = tmem + (b ? Cfg::TM_R1 : Cfg::TM_R0);
-            const uint32_t vbase = sVa + stage * Cfg::KV_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-                const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, Cfg::KV_PANEL, 1024);
-                const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
-                // keys [32h, 32h + 32) of the tile sit, as fp16 pairs, in columns [32h, 32h + 16)
-                const uint32_t acol = (kk >> 1) * 32 + (kk & 1) * 8;
-                mma_ts_warp(tmem + Cfg::TM_O, tS + acol, bdesc, ID_PV, acc);
-                if (PLX) mma_ts_warp(tmem + Cfg::TM_U, tR + acol, bdesc, ID_PV, acc);
-            }
+            static_assert(Cfg::TM_R0 == Cfg::TM_S0 + 64 && Cfg::TM_R1 == Cfg::TM_S1 + 64, "R sits 64 columns after S");
+            // keys [32h, 32h + 32) of the tile sit, as fp16 pairs, in columns [32h, 32h + 16)
+            // of S_b (P) and R_b (PR); V is the MN-major B operand
+            const uint64_t b_v = sdesc_sw128(sVa + stage * Cfg::KV_BYTES, Cfg::KV_PANEL, 1024);
+            mma_pv_batch<PLX, 0, PLX ? 64 : 0>(tmem + Cfg::TM_O, tmem + Cfg::TM_U, tS, b_v, ID_PV, first ? 0u : 1u);
             mma_commit_warp(&v_empty[stage]);
             mma_commit_warp(&pv_done[b]);
             return true;
@@ -329,6 +327,10 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             // one read of the flag for the whole warp: every lane takes the same branch
             if (u >= p.n_items || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
             const int n_kv = item_span<CACHED>(p, u, BM, BN).n_kv;
+            // the previous item's last PV goes first: its epilogue then runs while
+            // the S/R GEMMs of this item's first tiles do
+            if (pend && !issue_pv(g - 1, pend_first)) { ok = false; break; }
+            pend = false;
             if (!wait_warp(q_full, items & 1)) { ok = false; break; }
             tc_fence_after();
             for (int j = 0; j < n_kv; ++j, ++g) {
@@ -338,19 +340,12 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 const int b = g & 1;
                 const uint32_t tS = tmem + (b ? Cfg::TM_S1 : Cfg::TM_S0);
                 const uint32_t tR = tmem + (b ? Cfg::TM_R1 : Cfg::TM_R0);
-                const uint32_t kbase = sKa + ks * Cfg::KV_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * Cfg::Q_PANEL + (kk & 3) * 32;
-                    const uint32_t koff = (kk >> 2) * Cfg::KV_PANEL + (kk & 3) * 32;
-                    const uint64_t bdesc = sdesc_sw128(kbase + koff, 16, 1024);
-                    mma_ss_warp(tS, sdesc_sw128(sQa + off, 16, 1024), bdesc, ID_S, kk > 0);
-                    if (PLX) mma_ss_warp(tR, sdesc_sw128(sRa + off, 16, 1024), bdesc, ID_S, kk > 0);
-                }
+                static_assert(Cfg::Q_PANEL == 1024 * 16 && Cfg::KV_PANEL == 512 * 16, "panel strides of the S/R batch");
+                mma_sr_batch<D, PLX>(tS, tR, a_q, a_r, sdesc_sw128(sKa + ks * Cfg::KV_BYTES, 16, 1024), ID_S);
                 mma_commit_warp(&k_empty[ks]);
                 mma_commit_warp(&s_full[b]);
                 if (j == n_kv - 1) mma_commit_warp(q_empty);
-                // then the PV of the tile before this one, of this item or the previous one
+                // then the PV of the tile before this one
                 if (pend && !issue_pv(g - 1, pend_first)) { ok = false; break; }
                 pend = true;
                 pend_first = j == 0;
@@ -477,11 +472,6 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 atomicOr(&g_plx_status, PLX_DEV_ERR_NONFINITE);
             return true;
         };
-        // the item whose epilogue is still to run: its index, last global tile,
-        // and this warp's running max and partial sums
-        bool prev = false;
-        int prev_u = 0, prev_g = 0;
-        float prev_m = 0.f, prev_l = 0.f, prev_C = 0.f;
         bool ok = true;
         for (int r = 0; ok; ++r) {
             const int u = snake_item(r, c, G);
@@ -492,15 +482,14 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             const int pos = it.off + i;             // its position: keys 0 .. pos
             float m = -INFINITY, l = 0.f, C = 0.f;
             // cached mode: a quadrant none of whose 32 rows is a query row (T < 128)
-            // stores nothing, so after the first tile (which runs the previous
-            // item's epilogue and the pair handshakes) it only keeps the barrier
-            // phases in step; the garbage left in its lanes stays in its own rows
+            // stores nothing; its two warps only keep the barrier phases in step,
+            // and the garbage left in its lanes stays in its own rows
             const bool idle = CACHED && q0 + quad * 32 >= p.Tq;
             for (int j = 0; j < n_kv; ++j, ++g) {
                 const int b = g & 1;
                 if (!wait_warp(&s_full[b], (g >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                if (idle && j > 0) {
+                if (idle) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&p_full[b]);
@@ -539,12 +528,8 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 // 2^4, m stays, and they are final.  The first tile of an item, and a
                 // tile that does raise a row max that far (a warp-uniform decision,
                 // the same in both warps), take them again against the new m.
-                // The first tile of an item also carries the previous item's (l, C).
                 float* xm = xmax + (b * 2) * BM;
                 xm[half * BM + row] = mloc;
-                const bool epi = j == 0 && prev;
-                float2* xe = xlc + (((items - 1) & 1) * 2) * BM;
-                if (epi) xe[half * BM + row] = make_float2(prev_l, prev_C);
                 pair_arrive();
                 if constexpr (PLX) tmem_ld32x32b_x32_nowait(tR + half * HALF, rraw);
                 float pe[HALF];
@@ -640,29 +625,24 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                         tmem_st32x32b_x32(lane_addr + Cfg::TM_O + cb, o32);
                     }
                 }
-                // the previous item's O and U are read out before this tile's P is
-                // released: the first PV of this item overwrites them
-                if (epi && !epilogue(prev_u, prev_g, prev_m, xe)) { ok = false; break; }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[b]);
             }
             if (!ok) break;
-            prev = true;
-            prev_u = u;
-            prev_g = g - 1;
-            prev_m = m;
-            prev_l = l;
-            prev_C = C;
+            // The item's epilogue, right after its last tile: the pair adds its
+            // (l, C), then waits for the last PV.  The MMA warp issues that PV
+            // before the next item's first S/R GEMMs, which run meanwhile; the
+            // next item's first PV, which overwrites O and U, needs this warp's P
+            // of that item and so comes after the epilogue.
+            if (!idle) {
+                float2* xe = xlc + ((items & 1) * 2) * BM;
+                xe[half * BM + row] = make_float2(l, C);
+                pair_arrive();
+                if (!pair_wait() || !epilogue(u, g - 1, m, xe)) { ok = false; break; }
+            }
             ++items;
-        }
-        // the CTA's last item: its own (l, C) handshake, then its epilogue
-        if (ok && prev) {
-            float2* xe = xlc + (((items - 1) & 1) * 2) * BM;
-            xe[half * BM + row] = make_float2(prev_l, prev_C);
-            pair_arrive();
-            ok = pair_wait() && epilogue(prev_u, prev_g, prev_m, xe);
         }
         if (!ok) fail();
         // the output stores have finished (and stopped reading shared memory)

@@ -447,6 +447,7 @@ void launch_decode(const plx::DecodeParams& p, long long BH, cudaStream_t s) {
 constexpr size_t kNoallocScratchBytes = PLX_DECODE_NOALLOC_SCRATCH_BYTES;
 static_assert(kNoallocScratchBytes % 256 == 0, "scratch size");
 float* g_noalloc_scratch[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};   // the context the address above belongs to
 
 }  // namespace
 
@@ -454,17 +455,47 @@ static __device__ __align__(256) float plx_decode_scratch[kNoallocScratchBytes /
 
 namespace {
 
-// Device address of plx_decode_scratch on the current device, looked up once
-// per device (host code cannot take the array's address directly: its name
-// there is a host-side stand-in).  nullptr on a CUDA error.
+// Unique id of the calling thread's current CUDA context, 0 if there is none
+// (or the driver cannot tell).
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    }
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of plx_decode_scratch on the current device (host code cannot
+// take the array's address directly: its name there is a host-side stand-in).
+// It is looked up once per device and context: cudaDeviceReset gives the
+// device a new context, in which the module and its array may sit elsewhere,
+// so a call that finds another context than the one of the cached address
+// looks it up again.  nullptr on a CUDA error.
 float* noalloc_scratch() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_noalloc_scratch[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_noalloc_scratch[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, plx_decode_scratch) != cudaSuccess || !ptr) return nullptr;
         g_noalloc_scratch[dev] = static_cast<float*>(ptr);
+        g_noalloc_ctx[dev] = current_context_id();   // now current, if it was not before
     }
     return g_noalloc_scratch[dev];
 }

@@ -366,4 +366,82 @@ __device__ __forceinline__ void tmem_st32x32b_x32(uint32_t taddr, const uint32_t
                  :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
 }
 
+// ------------------------------------------------- batched tcgen05 issue
+// One warp-wide asm block per batch of MMAs: a single elect.sync picks the
+// issuing lane, and each MMA's shared-memory descriptors are the batch's base
+// descriptors plus a compile-time offset added to their low word (the start
+// address field, bits 0-13, in 16-byte units: adding an offset that keeps the
+// address below 256 KB cannot carry into the next field).  So a batch costs
+// about three instructions per MMA.
+//
+// The S/R batch of the prefill: D(S) (+)= Q K^T and, for PLX, D(R) (+)= rho K^T
+// over D/16 k-steps of 16; Q, rho and K tiles are K-major, 128B-swizzled
+// 64-column panels (the k-step's 32 bytes at (k % 4) * 32 within a panel,
+// panels a_panel / b_panel bytes apart).  The first k-step overwrites D.
+template <int D, bool PLX>
+__device__ __forceinline__ void mma_sr_batch(uint32_t t_s, uint32_t t_r, uint64_t a_q, uint64_t a_r, uint64_t b_k,
+                                             uint32_t idesc);
+template <>
+__device__ __forceinline__ void mma_sr_batch<64, true>(uint32_t t_s, uint32_t t_r, uint64_t a_q, uint64_t a_r,
+                                                        uint64_t b_k, uint32_t idesc) {
+    asm volatile("{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 lo;\n\t.reg .b64 da, db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\tadd.u32 lo, %6, 0; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 0; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pf;\n\tadd.u32 lo, %4, 0; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pf;\n\tadd.u32 lo, %6, 2; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 2; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 2; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 4; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 4; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 4; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 6; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 6; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 6; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\t}"
+                 ::"r"(t_s), "r"(t_r), "r"(static_cast<uint32_t>(a_q)), "r"(static_cast<uint32_t>(a_q >> 32)),
+                   "r"(static_cast<uint32_t>(a_r)), "r"(static_cast<uint32_t>(a_r >> 32)),
+                   "r"(static_cast<uint32_t>(b_k)), "r"(static_cast<uint32_t>(b_k >> 32)), "r"(idesc)
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void mma_sr_batch<64, false>(uint32_t t_s, uint32_t t_r, uint64_t a_q, uint64_t a_r,
+                                                        uint64_t b_k, uint32_t idesc) {
+    asm volatile("{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 lo;\n\t.reg .b64 da, db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\tadd.u32 lo, %6, 0; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 0; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pf;\n\tadd.u32 lo, %6, 2; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 2; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 4; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 4; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 6; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 6; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\t}"
+                 ::"r"(t_s), "r"(t_r), "r"(static_cast<uint32_t>(a_q)), "r"(static_cast<uint32_t>(a_q >> 32)),
+                   "r"(static_cast<uint32_t>(a_r)), "r"(static_cast<uint32_t>(a_r >> 32)),
+                   "r"(static_cast<uint32_t>(b_k)), "r"(static_cast<uint32_t>(b_k >> 32)), "r"(idesc)
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void mma_sr_batch<128, true>(uint32_t t_s, uint32_t t_r, uint64_t a_q, uint64_t a_r,
+                                                        uint64_t b_k, uint32_t idesc) {
+    asm volatile("{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 lo;\n\t.reg .b64 da, db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\tadd.u32 lo, %6, 0; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 0; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pf;\n\tadd.u32 lo, %4, 0; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pf;\n\tadd.u32 lo, %6, 2; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 2; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 2; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 4; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 4; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 4; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 6; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 6; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 6; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 512; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1024; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 1024; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 514; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1026; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 1026; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 516; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1028; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 1028; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 518; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1030; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 1030; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\t}"
+                 ::"r"(t_s), "r"(t_r), "r"(static_cast<uint32_t>(a_q)), "r"(static_cast<uint32_t>(a_q >> 32)),
+                   "r"(static_cast<uint32_t>(a_r)), "r"(static_cast<uint32_t>(a_r >> 32)),
+                   "r"(static_cast<uint32_t>(b_k)), "r"(static_cast<uint32_t>(b_k >> 32)), "r"(idesc)
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void mma_sr_batch<128, false>(uint32_t t_s, uint32_t t_r, uint64_t a_q, uint64_t a_r,
+                                                        uint64_t b_k, uint32_t idesc) {
+    asm volatile("{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 lo;\n\t.reg .b64 da, db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\tadd.u32 lo, %6, 0; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 0; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pf;\n\tadd.u32 lo, %6, 2; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 2; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 4; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 4; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 6; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 6; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 512; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1024; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 514; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1026; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 516; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1028; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 518; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1030; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\t}"
+                 ::"r"(t_s), "r"(t_r), "r"(static_cast<uint32_t>(a_q)), "r"(static_cast<uint32_t>(a_q >> 32)),
+                   "r"(static_cast<uint32_t>(a_r)), "r"(static_cast<uint32_t>(a_r >> 32)),
+                   "r"(static_cast<uint32_t>(b_k)), "r"(static_cast<uint32_t>(b_k >> 32)), "r"(idesc)
+                 : "memory");
+}
+
+// The PV batch of the prefill: O (+)= P V and, for PLX, U (+)= (P o R) V over
+// the tile's 64 keys in 4 k-steps of 16.  P and PR are fp16 pairs in TMEM:
+// keys [32h, 32h + 32) at columns [32h, 32h + 16) of the buffer t_p + P_OFF
+// (P) and t_p + PR_OFF (PR); V is the MN-major B operand, k-step kk at
+// kk * 2048 bytes (b_v its base descriptor).  acc0 = 0: the first k-step
+// overwrites O and U.
+template <bool PLX, int P_OFF, int PR_OFF>
+__device__ __forceinline__ void mma_pv_batch(uint32_t t_o, uint32_t t_u, uint32_t t_p, uint64_t b_v, uint32_t idesc,
+                                             uint32_t acc0);
+template <>
+__device__ __forceinline__ void mma_pv_batch<true, 0, 64>(uint32_t t_o, uint32_t t_u, uint32_t t_p, uint64_t b_v,
+                                                        uint32_t idesc, uint32_t acc0) {
+    asm volatile("{\n\t.reg .pred e, pa, pt;\n\t.reg .b32 lo, ta;\n\t.reg .b64 db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pa, %6, 0;\n\tsetp.eq.b32 pt, %6, %6;\n\tadd.u32 lo, %3, 0; mov.b64 db, {lo, %4};\n\tadd.u32 ta, %2, 0;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %5, pa;\n\tadd.u32 ta, %2, 64;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], db, %5, pa;\n\tadd.u32 lo, %3, 128; mov.b64 db, {lo, %4};\n\tadd.u32 ta, %2, 8;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %5, pt;\n\tadd.u32 ta, %2, 72;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], db, %5, pt;\n\tadd.u32 lo, %3, 256; mov.b64 db, {lo, %4};\n\tadd.u32 ta, %2, 32;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %5, pt;\n\tadd.u32 ta, %2, 96;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], db, %5, pt;\n\tadd.u32 lo, %3, 384; mov.b64 db, {lo, %4};\n\tadd.u32 ta, %2, 40;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %5, pt;\n\tadd.u32 ta, %2, 104;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], db, %5, pt;\n\t}"
+                 ::"r"(t_o), "r"(t_u), "r"(t_p), "r"(static_cast<uint32_t>(b_v)), "r"(static_cast<uint32_t>(b_v >> 32)),
+                   "r"(idesc), "r"(acc0)
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void mma_pv_batch<false, 0, 0>(uint32_t t_o, uint32_t t_u, uint32_t t_p, uint64_t b_v,
+                                                        uint32_t idesc, uint32_t acc0) {
+    asm volatile("{\n\t.reg .pred e, pa, pt;\n\t.reg .b32 lo, ta;\n\t.reg .b64 db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pa, %6, 0;\n\tsetp.eq.b32 pt, %6, %6;\n\tadd.u32 lo, %3, 0; mov.b64 db, {lo, %4};\n\tadd.u32 ta, %2, 0;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %5, pa;\n\tadd.u32 lo, %3, 128; mov.b64 db, {lo, %4};\n\tadd.u32 ta, %2, 8;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %5, pt;\n\tadd.u32 lo, %3, 256; mov.b64 db, {lo, %4};\n\tadd.u32 ta, %2, 32;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %5, pt;\n\tadd.u32 lo, %3, 384; mov.b64 db, {lo, %4};\n\tadd.u32 ta, %2, 40;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %5, pt;\n\t}"
+                 ::"r"(t_o), "r"(t_u), "r"(t_p), "r"(static_cast<uint32_t>(b_v)), "r"(static_cast<uint32_t>(b_v >> 32)),
+                   "r"(idesc), "r"(acc0)
+                 : "memory");
+}
+
 }  // namespace plx
