@@ -325,6 +325,52 @@ plx_status plx_decode_noalloc(const void* q, const void* rho, const void* k_cach
                               float scale, int num_splits, plx_dtype out_dtype, void* stream);
 
 /*
+ * plx_decode_partials / plx_decode_combine -- plx_decode with its key range
+ * split over several caches (for instance over GPUs, each holding a slice of
+ * every sequence's positions), merged afterwards.  The decode streams K and V
+ * once with an online softmax ("Parallax: Parameterized Local Linear
+ * Attention for Language Modeling", gist.science, "Algoritmo Consapevole
+ * dell'Hardware"); over any set of disjoint key ranges it keeps the state
+ *   m = max s_j,  l = sum e^{s_j - m},  C = sum e^{s_j - m} r_j,
+ *   A = sum e^{s_j - m} v_j,  U = sum e^{s_j - m} r_j v_j
+ * (s_j = scale q.k_j in log2 units, r_j = rho.k_j), and states of disjoint
+ * ranges merge exactly by the log-sum-exp weighting the split combine of
+ * plx_decode uses: M = max m_g, w_g = 2^(m_g - M), L = sum w_g l_g, C, A, U
+ * likewise, then o = (1 + C/L) A/L - U/L and lse = (M + log2 L) ln 2.
+ *
+ * plx_decode_partials: the states of one shard.
+ *   k_shard, v_shard : bf16 [B][H][S_shard][d]; row r of sequence b is
+ *                      position key_begin + r.  Sequence b has
+ *                      clamp(seqlens[b] - key_begin, 0, S_shard) keys here
+ *                      (its query at position seqlens[b] - 1 sees every
+ *                      position below seqlens[b]); a shard with none of a
+ *                      sequence's keys writes the empty state (m = -inf,
+ *                      l = 0).  A length past the shard is not an error.
+ *   q, rho, seqlens  : as plx_decode (rho NULL: softmax attention).
+ *   partials         : fp32 [B*H][num_splits][2 d + 4] = (m, l, C, 0, A[d],
+ *                      U[d]) per split of the shard's range, m in log2 units;
+ *                      plx_decode_partials_size(B, H, d, num_splits) bytes,
+ *                      16-byte aligned.
+ *   key_begin >= 0, S_shard >= 1, num_splits in [1, 1024] (explicit: every
+ *   shard must use the count the combine is told).
+ * plx_decode_combine: merges `groups` such buffers, concatenated in shard
+ * order ([groups][B*H][num_splits][2 d + 4], e.g. an all-gather of every
+ * shard's partials), into out (bf16 or fp32 [B][H][d]) and lse (fp32 [B][H],
+ * natural log, may be NULL).  with_rho: the shards ran with rho (PLX) or
+ * without (softmax attention); flags: 0 or PLX_FAMILY_NO_INTERCEPT (needs
+ * with_rho).  The result equals plx_decode over the whole range up to fp32
+ * rounding of the merge order.  One launch each on `stream`.
+ * Errors: PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED (d), PLX_ERR_MISALIGNED,
+ * PLX_ERR_WORKSPACE (partials buffer too small), PLX_ERR_CUDA.
+ */
+size_t plx_decode_partials_size(int B, int H, int d, int num_splits);
+plx_status plx_decode_partials(const void* q, const void* rho, const void* k_shard, const void* v_shard,
+                               const int32_t* seqlens, int key_begin, void* partials, size_t partials_bytes, int B,
+                               int H, int d, int S_shard, float scale, int num_splits, void* stream);
+plx_status plx_decode_combine(const void* partials, int groups, int num_splits, void* out, float* lse, int B, int H,
+                              int d, int with_rho, unsigned flags, plx_dtype out_dtype, void* stream);
+
+/*
  * plx_lla_f32 -- local linear attention (LLA) with the solved probe, the
  * method Parallax replaces ("Parallax: Parameterized Local Linear Attention
  * for Language Modeling", zhichai.net section 1.2; gist.science "Enunciato
@@ -398,6 +444,24 @@ plx_status plx_probe_proj(const void* x, const void* w_r, void* rho, int B, int 
  * synchronisation failed, else PLX_OK.
  */
 plx_status plx_last_device_error(void* stream);
+
+/*
+ * plx_selftest_wait -- a diagnostic of the device-side failure detection.
+ * Every kernel of the library waits on shared-memory barriers with a bounded
+ * wait: after a wall-time limit (4 s in the kernels) it gives up, records
+ * PLX_ERR_TIMEOUT in the device status word and returns instead of hanging.
+ * This call runs that same wait once, in a one-thread kernel, on a barrier
+ * with nothing asynchronous in flight, with the limit given here.
+ *   limit_us : 1 .. 1000000 (microseconds).
+ *   arrive   : nonzero arrives on the barrier first, so the wait completes
+ *              and the status word is left alone; zero leaves the barrier
+ *              alone, so the wait gives up after limit_us and the next
+ *              plx_last_device_error returns PLX_ERR_TIMEOUT.
+ * The device stays usable afterwards.  The pages have no counterpart: this
+ * checks the library's own bounded waits.
+ * Errors: PLX_ERR_INVALID_ARG (limit out of range), PLX_ERR_CUDA.
+ */
+plx_status plx_selftest_wait(unsigned int limit_us, int arrive, void* stream);
 
 #ifdef __cplusplus
 }

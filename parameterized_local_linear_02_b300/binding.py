@@ -88,6 +88,14 @@ def library() -> ctypes.CDLL:
         lib.plx_probe_proj.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
         lib.plx_last_device_error.restype = i
         lib.plx_last_device_error.argtypes = [vp]
+        lib.plx_selftest_wait.restype = i
+        lib.plx_selftest_wait.argtypes = [ctypes.c_uint, i, vp]
+        lib.plx_decode_partials_size.restype = sz
+        lib.plx_decode_partials_size.argtypes = [i, i, i, i]
+        lib.plx_decode_partials.restype = i
+        lib.plx_decode_partials.argtypes = [vp, vp, vp, vp, vp, i, vp, sz, i, i, i, i, f, i, vp]
+        lib.plx_decode_combine.restype = i
+        lib.plx_decode_combine.argtypes = [vp, i, i, vp, vp, i, i, i, i, ctypes.c_uint, i, vp]
         _lib = lib
         return lib
 
@@ -456,6 +464,57 @@ def _decode(q, rho, k_cache, v_cache, seqlens, flags, scale, num_splits, workspa
     return out, lse
 
 
+def plx_decode_partials_size(B: int, H: int, d: int, num_splits: int) -> int:
+    return library().plx_decode_partials_size(B, H, d, num_splits)
+
+
+def plx_decode_partials(q, rho, k_shard, v_shard, seqlens, *, key_begin, num_splits, scale=None, out=None):
+    """The online-softmax states of one shard of the key range: ``k_shard``,
+    ``v_shard`` bf16 [B, H, S_shard, d] hold positions key_begin ..
+    key_begin + S_shard - 1.  Returns (or fills) fp32 partials, a flat buffer
+    of [B*H][num_splits][2 d + 4] states (include/plx.h)."""
+    B, H, S, d = k_shard.shape
+    dev = k_shard.device
+    _need(q, "q", torch.bfloat16, (B, H, d), dev)
+    if rho is not None:
+        _need(rho, "rho", torch.bfloat16, (B, H, d), dev)
+    _need(k_shard, "k_shard", torch.bfloat16, (B, H, S, d), dev)
+    _need(v_shard, "v_shard", torch.bfloat16, (B, H, S, d), dev)
+    _need(seqlens, "seqlens", torch.int32, (B,), dev)
+    n = plx_decode_partials_size(B, H, d, int(num_splits)) // 4
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=dev)
+    else:
+        _need(out, "partials", torch.float32, (n,), dev)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().plx_decode_partials(_ptr(q), _ptr(rho), _ptr(k_shard), _ptr(v_shard), _ptr(seqlens),
+                                       int(key_begin), _ptr(out), out.numel() * 4, B, H, d, S, scale,
+                                       int(num_splits), _stream(dev))
+    _check(st, "plx_decode_partials")
+    return out
+
+
+def plx_decode_combine(partials, *, groups, num_splits, B, H, d, with_rho=True, flags=0, out=None, lse=None,
+                       out_dtype=torch.bfloat16, with_lse=True):
+    """Merge ``groups`` shards' partials, concatenated in shard order in the
+    flat fp32 tensor ``partials``, into ``(out [B, H, d], lse [B, H])``."""
+    dev = partials.device
+    n = groups * (plx_decode_partials_size(B, H, d, int(num_splits)) // 4)
+    _need(partials, "partials", torch.float32, (n,), dev)
+    if out is None:
+        out = torch.empty((B, H, d), dtype=out_dtype, device=dev)
+    else:
+        _need(out, "out", out.dtype, (B, H, d), dev)
+    if lse is None and with_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, (B, H), dev)
+    st = library().plx_decode_combine(_ptr(partials), int(groups), int(num_splits), _ptr(out), _ptr(lse), B, H, d,
+                                      1 if with_rho else 0, int(flags), _out_code(out.dtype), _stream(dev))
+    _check(st, "plx_decode_combine")
+    return out, lse
+
+
 def plx_decode_noalloc(q, rho, k_cache, v_cache, seqlens, *, scale=None, num_splits=0, out=None, lse=None,
                        out_dtype=torch.bfloat16, with_lse=True):
     """plx_decode through the entry point that takes no workspace: the split
@@ -486,6 +545,17 @@ def plx_decode_noalloc(q, rho, k_cache, v_cache, seqlens, *, scale=None, num_spl
                                       _out_code(out.dtype), _stream(dev))
     _check(st, "plx_decode_noalloc")
     return out, lse
+
+
+def plx_selftest_wait(limit_us: int, arrive: bool, device=None) -> None:
+    """Run the library's bounded device wait once (plx_selftest_wait in
+    include/plx.h): with ``arrive=False`` nothing arrives and the wait gives up
+    after ``limit_us`` microseconds, which the next plx_last_device_error
+    reports as 5 (PLX_ERR_TIMEOUT)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    st = library().plx_selftest_wait(int(limit_us), 1 if arrive else 0, _stream(dev))
+    if st != 0:
+        raise PlxError(st, "plx_selftest_wait")
 
 
 def plx_last_device_error(device=None) -> int:

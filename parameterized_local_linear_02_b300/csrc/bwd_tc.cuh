@@ -635,6 +635,8 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
             tc_fence_before();
         }
         if (!ok) fail();
+        // no TMEM store of this warp is still pending, and the output stores have finished
+        tmem_st_wait();
         if (lane == 0) bulk_wait_all();
     }
 

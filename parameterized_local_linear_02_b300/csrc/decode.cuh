@@ -68,6 +68,16 @@ struct DecodeParams {
     int max_blocks;
     int page;
     int num_blocks;
+    // A shard of the key range (plx_decode_partials): the cache holds the
+    // positions key_begin .. key_begin + S_cap - 1, so sequence b has
+    // clamp(seqlens[b] - key_begin, 0, S_cap) of its keys here; the split
+    // partials are always written (never the output), and a length past this
+    // shard is not an error (those keys live in a later shard).
+    int key_begin = 0;
+    int partials_only = 0;
+    // the combine merges groups x splits partials per (b, h), laid out
+    // [groups][B*H][splits][PART] (groups = 1: the split kernel's own layout)
+    int groups = 1;
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -110,7 +120,10 @@ plx_decode_split_kernel(const DecodeParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     int L = p.seqlens[b];
-    if (L > p.S_cap) {
+    if (p.partials_only) {
+        L -= p.key_begin;
+        L = L > p.S_cap ? p.S_cap : L;
+    } else if (L > p.S_cap) {
         if (threadIdx.x == 0 && split == 0 && (bh % p.H) == 0) atomicOr(&g_plx_status, PLX_DEV_ERR_SEQLEN);
         L = p.S_cap;
     }
@@ -301,7 +314,7 @@ plx_decode_split_kernel(const DecodeParams p) {
                 Us = fmaf(sc, pw[4 + D + t], Us);
             }
         }
-        if (p.splits == 1) {
+        if (p.splits == 1 && !p.partials_only) {
             float o = 0.f;
             if (Lsum > 0.f) {
                 const float inv = 1.f / Lsum;
@@ -320,25 +333,32 @@ plx_decode_split_kernel(const DecodeParams p) {
     }
 }
 
-// Merge the split partials of one (b, h): M = max m_s, w_s = 2^(m_s - M),
+// Merge the partials of one (b, h) -- every split of every group (shard of
+// the key range), in group-major order: M = max m_s, w_s = 2^(m_s - M),
 // L = sum w_s l_s, then the weighted sums of C, A, U, and the PLX output.
 template <int D, bool PLX>
 __global__ void __launch_bounds__(D) plx_decode_combine_kernel(const DecodeParams p) {
     constexpr int PART = DecodeCfg<D>::PART;
     const int bh = blockIdx.x, t = threadIdx.x;
-    const float* base = p.ws + static_cast<size_t>(bh) * p.splits * PART;
+    const size_t group_stride = static_cast<size_t>(gridDim.x) * p.splits * PART;
     float M = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, base[s * PART]);
+    for (int g = 0; g < p.groups; ++g) {
+        const float* base = p.ws + g * group_stride + static_cast<size_t>(bh) * p.splits * PART;
+        for (int s = 0; s < p.splits; ++s) M = fmaxf(M, base[s * PART]);
+    }
     float Lsum = 0.f, Cs = 0.f, As = 0.f, Us = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < p.splits; ++s) {
-            const float* ps = base + s * PART;
-            if (ps[0] == -INFINITY) continue;
-            const float sc = exp2f(ps[0] - M);
-            Lsum = fmaf(sc, ps[1], Lsum);
-            Cs = fmaf(sc, ps[2], Cs);
-            As = fmaf(sc, ps[4 + t], As);
-            if constexpr (PLX) Us = fmaf(sc, ps[4 + D + t], Us);
+        for (int g = 0; g < p.groups; ++g) {
+            const float* base = p.ws + g * group_stride + static_cast<size_t>(bh) * p.splits * PART;
+            for (int s = 0; s < p.splits; ++s) {
+                const float* ps = base + s * PART;
+                if (ps[0] == -INFINITY) continue;
+                const float sc = exp2f(ps[0] - M);
+                Lsum = fmaf(sc, ps[1], Lsum);
+                Cs = fmaf(sc, ps[2], Cs);
+                As = fmaf(sc, ps[4 + t], As);
+                if constexpr (PLX) Us = fmaf(sc, ps[4 + D + t], Us);
+            }
         }
     }
     float o = 0.f;

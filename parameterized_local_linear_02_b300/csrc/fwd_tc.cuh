@@ -645,7 +645,10 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             ++items;
         }
         if (!ok) fail();
-        // the output stores have finished (and stopped reading shared memory)
+        // no TMEM store of this warp is still pending (a wait that gave up may
+        // have left the tile after its stores), and the output stores have
+        // finished (and stopped reading shared memory)
+        tmem_st_wait();
         if (lane == 0) bulk_wait_all();
         tc_fence_before();
     } else if (warp >= 2 + Cfg::SM_WARPS) {

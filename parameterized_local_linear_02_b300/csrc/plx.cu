@@ -435,6 +435,18 @@ size_t decode_ws_bytes(long long BH, int d, int splits) {
 }
 
 template <int D, bool PLX>
+void launch_decode_split(const plx::DecodeParams& p, long long BH, cudaStream_t s) {
+    using Cfg = DecodeCfg<D>;
+    dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(p.splits));
+    plx::plx_decode_split_kernel<D, PLX><<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(p);
+}
+
+template <int D, bool PLX>
+void launch_decode_combine(const plx::DecodeParams& p, long long BH, cudaStream_t s) {
+    plx::plx_decode_combine_kernel<D, PLX><<<static_cast<unsigned>(BH), D, 0, s>>>(p);
+}
+
+template <int D, bool PLX>
 void launch_decode(const plx::DecodeParams& p, long long BH, cudaStream_t s) {
     using Cfg = DecodeCfg<D>;
     dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(p.splits));
@@ -498,6 +510,17 @@ float* noalloc_scratch() {
         g_noalloc_ctx[dev] = current_context_id();   // now current, if it was not before
     }
     return g_noalloc_scratch[dev];
+}
+
+// One bounded wait on a fresh barrier (the diagnostic behind
+// plx_selftest_wait): a wait that gives up records PLX_DEV_ERR_TIMEOUT.
+__global__ void plx_wait_selftest_kernel(unsigned long long limit_ns, int arrive) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    plx::mbar_init(&bar, 1);
+    plx::fence_mbar_init();
+    if (arrive) plx::mbar_arrive(&bar);
+    if (!plx::mbar_wait_for(&bar, 0, limit_ns)) atomicOr(&plx::g_plx_status, plx::PLX_DEV_ERR_TIMEOUT);
 }
 
 }  // namespace
@@ -766,6 +789,9 @@ plx_status decode_impl(const void* q, const void* rho, const void* k_cache, cons
         p.max_blocks = paged.max_blocks;
         p.page = paged.page;
         p.num_blocks = paged.num_blocks;
+        p.key_begin = 0;
+        p.partials_only = 0;
+        p.groups = 1;
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         if (d == 128) {
             if (rho) launch_decode<128, true>(p, BH, s);
@@ -854,6 +880,111 @@ plx_status plx_decode_noalloc(const void* q, const void* rho, const void* k_cach
     }
 }
 
+size_t plx_decode_partials_size(int B, int H, int d, int num_splits) {
+    if (B < 1 || H < 1 || (d != 64 && d != 128) || num_splits < 1 || num_splits > 1024) return 0;
+    return static_cast<size_t>(B) * H * num_splits * (2 * d + 4) * sizeof(float);
+}
+
+plx_status plx_decode_partials(const void* q, const void* rho, const void* k_shard, const void* v_shard,
+                               const int32_t* seqlens, int key_begin, void* partials, size_t partials_bytes, int B,
+                               int H, int d, int S_shard, float scale, int num_splits, void* stream) {
+    try {
+        if (!q || !k_shard || !v_shard || !seqlens || !partials) return PLX_ERR_INVALID_ARG;
+        if (B < 1 || H < 1 || S_shard < 1 || key_begin < 0 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
+        if (num_splits < 1 || num_splits > 1024) return PLX_ERR_INVALID_ARG;
+        if (d != 64 && d != 128) return PLX_ERR_UNSUPPORTED;
+        if (!aligned(q, 16) || !aligned(k_shard, 16) || !aligned(v_shard, 16) || (rho && !aligned(rho, 16)) ||
+            !aligned(seqlens, 4) || !aligned(partials, 16))
+            return PLX_ERR_MISALIGNED;
+        const long long BH = static_cast<long long>(B) * H;
+        if (BH > INT_MAX) return PLX_ERR_UNSUPPORTED;
+        if (partials_bytes < plx_decode_partials_size(B, H, d, num_splits)) return PLX_ERR_WORKSPACE;
+        const DeviceInfo* info = device_info();
+        if (!info) return PLX_ERR_CUDA;
+        plx::DecodeParams p;
+        p.q = static_cast<const __nv_bfloat16*>(q);
+        p.rho = static_cast<const __nv_bfloat16*>(rho);
+        p.kc = static_cast<const __nv_bfloat16*>(k_shard);
+        p.vc = static_cast<const __nv_bfloat16*>(v_shard);
+        p.seqlens = seqlens;
+        p.out = nullptr;
+        p.lse = nullptr;
+        p.ws = static_cast<float*>(partials);
+        p.H = H;
+        p.S_cap = S_shard;
+        p.splits = num_splits;
+        p.scale_log2 = scale * kLog2e;
+        p.out_f32 = 1;
+        p.no_intercept = 0;
+        p.block_table = nullptr;
+        p.max_blocks = 0;
+        p.page = 0;
+        p.num_blocks = 0;
+        p.key_begin = key_begin;
+        p.partials_only = 1;
+        p.groups = 1;
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        if (d == 128) {
+            if (rho) launch_decode_split<128, true>(p, BH, s);
+            else launch_decode_split<128, false>(p, BH, s);
+        } else {
+            if (rho) launch_decode_split<64, true>(p, BH, s);
+            else launch_decode_split<64, false>(p, BH, s);
+        }
+        return launch_status();
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+plx_status plx_decode_combine(const void* partials, int groups, int num_splits, void* out, float* lse, int B, int H,
+                              int d, int with_rho, unsigned flags, plx_dtype out_dtype, void* stream) {
+    try {
+        if (!partials || !out) return PLX_ERR_INVALID_ARG;
+        if (B < 1 || H < 1 || groups < 1 || num_splits < 1 || num_splits > 1024) return PLX_ERR_INVALID_ARG;
+        if (out_dtype != PLX_BF16 && out_dtype != PLX_F32) return PLX_ERR_INVALID_ARG;
+        if ((flags & ~static_cast<unsigned>(PLX_FAMILY_NO_INTERCEPT)) != 0) return PLX_ERR_INVALID_ARG;
+        if ((flags & PLX_FAMILY_NO_INTERCEPT) && !with_rho) return PLX_ERR_INVALID_ARG;
+        if (d != 64 && d != 128) return PLX_ERR_UNSUPPORTED;
+        if (!aligned(partials, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return PLX_ERR_MISALIGNED;
+        const long long BH = static_cast<long long>(B) * H;
+        if (BH > INT_MAX || static_cast<long long>(groups) * num_splits > (1LL << 24)) return PLX_ERR_UNSUPPORTED;
+        plx::DecodeParams p;
+        p.q = nullptr;
+        p.rho = nullptr;
+        p.kc = nullptr;
+        p.vc = nullptr;
+        p.seqlens = nullptr;
+        p.out = out;
+        p.lse = lse;
+        p.ws = static_cast<float*>(const_cast<void*>(partials));
+        p.H = H;
+        p.S_cap = 0;
+        p.splits = num_splits;
+        p.scale_log2 = 0.f;
+        p.out_f32 = out_dtype == PLX_F32;
+        p.no_intercept = (flags & PLX_FAMILY_NO_INTERCEPT) ? 1 : 0;
+        p.block_table = nullptr;
+        p.max_blocks = 0;
+        p.page = 0;
+        p.num_blocks = 0;
+        p.key_begin = 0;
+        p.partials_only = 0;
+        p.groups = groups;
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        if (d == 128) {
+            if (with_rho) launch_decode_combine<128, true>(p, BH, s);
+            else launch_decode_combine<128, false>(p, BH, s);
+        } else {
+            if (with_rho) launch_decode_combine<64, true>(p, BH, s);
+            else launch_decode_combine<64, false>(p, BH, s);
+        }
+        return launch_status();
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
 size_t plx_lla_workspace_size(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 1 || d < 32 || d > 256 || d % 32 != 0) return 0;
     return lla_ws_bytes(static_cast<long long>(B) * H * N, d);
@@ -916,6 +1047,17 @@ plx_status plx_probe_proj(const void* x, const void* w_r, void* rho, int B, int 
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         return d == 128 ? launch_proj_tc<128>(x, w_r, rho, B, N, H, Dx, s, info->sm_count)
                         : launch_proj_tc<64>(x, w_r, rho, B, N, H, Dx, s, info->sm_count);
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+plx_status plx_selftest_wait(unsigned int limit_us, int arrive, void* stream) {
+    try {
+        if (limit_us < 1 || limit_us > 1000000) return PLX_ERR_INVALID_ARG;
+        plx_wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+            static_cast<unsigned long long>(limit_us) * 1000ull, arrive ? 1 : 0);
+        return launch_status();
     } catch (...) {
         return PLX_ERR_CUDA;
     }

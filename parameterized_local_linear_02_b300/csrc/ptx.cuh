@@ -74,14 +74,18 @@ constexpr uint32_t PLX_WAIT_SUSPEND_NS = 1000;
 // are suspended between polls, so they leave the issue slots to the warps that
 // work.  Bounded: returns false after PLX_WAIT_TIMEOUT_NS of wall time or
 // PLX_WAIT_MAX_POLLS polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// The same wait with the wall-time limit given in nanoseconds.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t polls = 0; polls < PLX_WAIT_MAX_POLLS; ++polls) {
         if (mbar_try_wait_suspend(bar, parity, PLX_WAIT_SUSPEND_NS)) return true;
-        if (globaltimer_ns() - t0 > PLX_WAIT_TIMEOUT_NS) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, PLX_WAIT_TIMEOUT_NS);
 }
 
 // ------------------------------------------------------------- bulk copies

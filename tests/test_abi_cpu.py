@@ -228,6 +228,41 @@ def test_lla_rejects_bad_arguments_before_launch():
     assert lib.plx_lla_f32(None, P, P, P, None, None, None, WS, need, 2, 3, 64, 64, 0.1, 0.1, 8, 0.0, None) == 1
 
 
+def test_decode_partials_and_combine_reject_bad_arguments_before_launch():
+    lib = plx.library()
+    P = P16
+    assert lib.plx_decode_partials_size(2, 3, 128, 2) == 2 * 3 * 2 * (2 * 128 + 4) * 4
+    assert lib.plx_decode_partials_size(2, 3, 96, 2) == 0
+    assert lib.plx_decode_partials_size(2, 3, 128, 0) == 0
+    need = lib.plx_decode_partials_size(2, 3, 128, 2)
+    ok = (P, P, P, P, P, 0, P, need, 2, 3, 128, 64, 0.1, 2, None)
+
+    def call(**kw):
+        names = ("q", "rho", "k", "v", "sl", "kb", "parts", "bytes", "B", "H", "d", "S", "scale", "n", "st")
+        a = dict(zip(names, ok))
+        a.update(kw)
+        return lib.plx_decode_partials(*[a[n] for n in names])
+    assert call(q=None) == 1
+    assert call(kb=-1) == 1
+    assert call(n=0) == 1
+    assert call(S=0) == 1
+    assert call(d=96) == 2
+    assert call(parts=P_ODD) == 3
+    assert call(bytes=need - 4) == 6
+    assert lib.plx_decode_combine(None, 2, 2, P, None, 2, 3, 128, 1, 0, 0, None) == 1
+    assert lib.plx_decode_combine(P, 0, 2, P, None, 2, 3, 128, 1, 0, 0, None) == 1
+    assert lib.plx_decode_combine(P, 2, 2, P, None, 2, 3, 128, 0, 2, 0, None) == 1     # no intercept without rho
+    assert lib.plx_decode_combine(P, 2, 2, P, None, 2, 3, 128, 1, 1, 0, None) == 1     # uniform weights is not a combine flag
+    assert lib.plx_decode_combine(P, 2, 2, P, None, 2, 3, 96, 1, 0, 0, None) == 2
+    assert lib.plx_decode_combine(P_ODD, 2, 2, P, None, 2, 3, 128, 1, 0, 0, None) == 3
+
+
+def test_selftest_wait_rejects_a_limit_out_of_range_before_launch():
+    lib = plx.library()
+    assert lib.plx_selftest_wait(0, 0, None) == 1
+    assert lib.plx_selftest_wait(1000001, 1, None) == 1
+
+
 def test_no_cpu_fallback_without_a_device():
     """With no CUDA device every entry point raises; none computes on the host.
     (Skipped on a GPU host: CPU tensors must never reach the library there.)"""
