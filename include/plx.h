@@ -60,7 +60,9 @@ typedef enum {
     PLX_ERR_CUDA = 4,        /* a CUDA call or kernel launch failed */
     PLX_ERR_TIMEOUT = 5,     /* a device-side wait gave up (see plx_last_device_error) */
     PLX_ERR_WORKSPACE = 6,   /* decode workspace missing or too small */
-    PLX_ERR_RANGE = 7        /* plx_fwd produced a non-finite output (see plx_last_device_error) */
+    PLX_ERR_RANGE = 7,       /* plx_fwd produced a non-finite output (see plx_last_device_error) */
+    PLX_ERR_BOUNDS = 8       /* the debug build (PLX_DEBUG) caught an index outside its buffer and skipped
+                                the access (see plx_last_device_error) */
 } plx_status;
 
 typedef enum { PLX_BF16 = 0, PLX_F32 = 1 } plx_dtype;
@@ -440,7 +442,8 @@ plx_status plx_probe_proj(const void* x, const void* w_r, void* rho, int B, int 
  * plx_last_device_error -- synchronises `stream`, then reads and clears the
  * current device's status word.  Returns PLX_ERR_TIMEOUT if a kernel gave up
  * a bounded wait, PLX_ERR_INVALID_ARG if a decode length exceeded S_cap,
- * PLX_ERR_RANGE if plx_fwd wrote a non-finite output, PLX_ERR_CUDA if
+ * PLX_ERR_RANGE if plx_fwd wrote a non-finite output, PLX_ERR_BOUNDS if a
+ * library built with PLX_DEBUG caught an index outside its buffer, PLX_ERR_CUDA if
  * synchronisation failed, else PLX_OK.
  */
 plx_status plx_last_device_error(void* stream);

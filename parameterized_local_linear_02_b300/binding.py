@@ -46,58 +46,64 @@ def library() -> ctypes.CDLL:
             return _lib
         if _build.stale():
             _build.build()
-        lib = ctypes.CDLL(_build.LIB)
-        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-        lib.plx_version.restype = i
-        lib.plx_version.argtypes = []
-        lib.plx_strerror.restype = ctypes.c_char_p
-        lib.plx_strerror.argtypes = [i]
-        lib.plx_fwd.restype = i
-        lib.plx_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
-        lib.plx_fwd_cached.restype = i
-        lib.plx_fwd_cached.argtypes = [vp] * 7 + [i] * 5 + [f, i, vp]
-        lib.plx_fwd_family.restype = i
-        lib.plx_fwd_family.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, ctypes.c_uint, i, vp]
-        lib.plx_fwd_f32.restype = i
-        lib.plx_fwd_f32.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, vp]
-        lib.plx_decode.restype = i
-        lib.plx_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, i, vp]
-        lib.plx_decode_paged.restype = i
-        lib.plx_decode_paged.argtypes = [vp] * 8 + [i] * 6 + [f, i, vp, sz, i, vp]
-        lib.plx_decode_family.restype = i
-        lib.plx_decode_family.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, ctypes.c_uint, i, vp]
-        lib.plx_decode_num_splits.restype = i
-        lib.plx_decode_num_splits.argtypes = [i, i, i, i]
-        lib.plx_decode_workspace_size.restype = sz
-        lib.plx_decode_workspace_size.argtypes = [i, i, i, i, i]
-        lib.plx_bwd_f32.restype = i
-        lib.plx_bwd_f32.argtypes = [vp] * 12 + [sz, i, i, i, i, f, vp]
-        lib.plx_bwd_workspace_size.restype = sz
-        lib.plx_bwd_workspace_size.argtypes = [i, i, i, i]
-        lib.plx_bwd.restype = i
-        lib.plx_bwd.argtypes = [vp] * 10 + [sz, i, i, i, i, f, vp]
-        lib.plx_bwd_bf16_workspace_size.restype = sz
-        lib.plx_bwd_bf16_workspace_size.argtypes = [i, i, i, i]
-        lib.plx_decode_noalloc.restype = i
-        lib.plx_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
-        lib.plx_probe_proj.restype = i
-        lib.plx_lla_f32.restype = i
-        lib.plx_lla_f32.argtypes = [vp] * 8 + [sz, i, i, i, i, f, f, i, f, vp]
-        lib.plx_lla_workspace_size.restype = sz
-        lib.plx_lla_workspace_size.argtypes = [i, i, i, i]
-        lib.plx_probe_proj.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
-        lib.plx_last_device_error.restype = i
-        lib.plx_last_device_error.argtypes = [vp]
-        lib.plx_selftest_wait.restype = i
-        lib.plx_selftest_wait.argtypes = [ctypes.c_uint, i, vp]
-        lib.plx_decode_partials_size.restype = sz
-        lib.plx_decode_partials_size.argtypes = [i, i, i, i]
-        lib.plx_decode_partials.restype = i
-        lib.plx_decode_partials.argtypes = [vp, vp, vp, vp, vp, i, vp, sz, i, i, i, i, f, i, vp]
-        lib.plx_decode_combine.restype = i
-        lib.plx_decode_combine.argtypes = [vp, i, i, vp, vp, i, i, i, i, ctypes.c_uint, i, vp]
-        _lib = lib
-        return lib
+        _lib = load(_build.LIB)
+        return _lib
+
+
+def load(path: str) -> ctypes.CDLL:
+    """Open a build of the library (libplx.so, or the bounds-checking debug
+    build) and declare the argument types of its entry points."""
+    lib = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.plx_version.restype = i
+    lib.plx_version.argtypes = []
+    lib.plx_strerror.restype = ctypes.c_char_p
+    lib.plx_strerror.argtypes = [i]
+    lib.plx_fwd.restype = i
+    lib.plx_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.plx_fwd_cached.restype = i
+    lib.plx_fwd_cached.argtypes = [vp] * 7 + [i] * 5 + [f, i, vp]
+    lib.plx_fwd_family.restype = i
+    lib.plx_fwd_family.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, ctypes.c_uint, i, vp]
+    lib.plx_fwd_f32.restype = i
+    lib.plx_fwd_f32.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, vp]
+    lib.plx_decode.restype = i
+    lib.plx_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, i, vp]
+    lib.plx_decode_paged.restype = i
+    lib.plx_decode_paged.argtypes = [vp] * 8 + [i] * 6 + [f, i, vp, sz, i, vp]
+    lib.plx_decode_family.restype = i
+    lib.plx_decode_family.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, ctypes.c_uint, i, vp]
+    lib.plx_decode_num_splits.restype = i
+    lib.plx_decode_num_splits.argtypes = [i, i, i, i]
+    lib.plx_decode_workspace_size.restype = sz
+    lib.plx_decode_workspace_size.argtypes = [i, i, i, i, i]
+    lib.plx_bwd_f32.restype = i
+    lib.plx_bwd_f32.argtypes = [vp] * 12 + [sz, i, i, i, i, f, vp]
+    lib.plx_bwd_workspace_size.restype = sz
+    lib.plx_bwd_workspace_size.argtypes = [i, i, i, i]
+    lib.plx_bwd.restype = i
+    lib.plx_bwd.argtypes = [vp] * 10 + [sz, i, i, i, i, f, vp]
+    lib.plx_bwd_bf16_workspace_size.restype = sz
+    lib.plx_bwd_bf16_workspace_size.argtypes = [i, i, i, i]
+    lib.plx_decode_noalloc.restype = i
+    lib.plx_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+    lib.plx_probe_proj.restype = i
+    lib.plx_lla_f32.restype = i
+    lib.plx_lla_f32.argtypes = [vp] * 8 + [sz, i, i, i, i, f, f, i, f, vp]
+    lib.plx_lla_workspace_size.restype = sz
+    lib.plx_lla_workspace_size.argtypes = [i, i, i, i]
+    lib.plx_probe_proj.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+    lib.plx_last_device_error.restype = i
+    lib.plx_last_device_error.argtypes = [vp]
+    lib.plx_selftest_wait.restype = i
+    lib.plx_selftest_wait.argtypes = [ctypes.c_uint, i, vp]
+    lib.plx_decode_partials_size.restype = sz
+    lib.plx_decode_partials_size.argtypes = [i, i, i, i]
+    lib.plx_decode_partials.restype = i
+    lib.plx_decode_partials.argtypes = [vp, vp, vp, vp, vp, i, vp, sz, i, i, i, i, f, i, vp]
+    lib.plx_decode_combine.restype = i
+    lib.plx_decode_combine.argtypes = [vp, i, i, vp, vp, i, i, i, i, ctypes.c_uint, i, vp]
+    return lib
 
 
 def plx_version() -> int:

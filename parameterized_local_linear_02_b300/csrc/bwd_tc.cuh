@@ -507,7 +507,7 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
             const float ci = (C * f0 + other[2 * ROWS + row] * f1) / L;
             const float ai = (A * f0 + other[3 * ROWS + row] * f1) / L;
             const float ei = (E * f0 + other[4 * ROWS + row] * f1) / L;
-            if (half == 0 && rw < p.N)
+            if (half == 0 && rw < p.N && in_bounds(bh < p.BH))
                 p.stats_out[static_cast<size_t>(bh) * p.N + rw] =
                     make_float4(M + __log2f(L), ci, ai, fmaf(2.f * ci, ai, ai) - ei);
             ++items;

@@ -177,9 +177,16 @@ plx_decode_split_kernel(const DecodeParams p) {
                     }
                     g = ((static_cast<size_t>(blk) * p.H + (bh % p.H)) * p.page + (r0 - pg * p.page)) * D;
                 }
-                mbar_arrive_expect_tx(&full[s], 2 * bytes);
-                bulk_g2s_hint(kbuf + s * T * D, p.kc + g, bytes, &full[s], pol);
-                bulk_g2s_hint(vbuf + s * T * D, p.vc + g, bytes, &full[s], pol);
+                const size_t cache_elems = p.block_table
+                                               ? static_cast<size_t>(p.num_blocks) * p.H * p.page * D
+                                               : static_cast<size_t>(gridDim.x) * p.S_cap * D;
+                if (in_bounds(rows > 0 && g + static_cast<size_t>(rows) * D <= cache_elems)) {
+                    mbar_arrive_expect_tx(&full[s], 2 * bytes);
+                    bulk_g2s_hint(kbuf + s * T * D, p.kc + g, bytes, &full[s], pol);
+                    bulk_g2s_hint(vbuf + s * T * D, p.vc + g, bytes, &full[s], pol);
+                } else {
+                    mbar_arrive(&full[s]);   // debug build: the copies are skipped, the phase still completes
+                }
                 ++issued;
             }
             // never leave with copies in flight into this block's shared memory

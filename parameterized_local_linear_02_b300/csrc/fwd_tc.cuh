@@ -156,6 +156,13 @@ __device__ __forceinline__ ItemSpan item_span(const FwdTcParams& p, int u, int B
     }
     it.off = CACHED ? L - p.Tq : 0;       // the self-attention prefill: query row i is position i
     it.n_kv = (it.off + min(p.Tq, it.q0 + BM) + BN - 1) / BN;
+    // debug build: the head, the query tile and the K/V tiles lie inside the
+    // tensors (every role clamps alike, so the barrier phases stay in step)
+    if (!in_bounds(it.bh < p.BH && it.q0 < p.Tq && it.n_kv >= 1 && it.n_kv <= (p.N + BN - 1) / BN)) {
+        it.bh = min(it.bh, p.BH - 1);
+        it.q0 = 0;
+        it.n_kv = 1;
+    }
     return it;
 }
 // u for round r of CTA c in a snake over the grid
@@ -466,7 +473,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             }
             const int ei = eq0 + row;
             const bool store = ei < p.Tq;
-            if (store && half == 0 && p.lse)
+            if (store && half == 0 && p.lse && in_bounds(ebh < p.BH))
                 p.lse[static_cast<size_t>(ebh) * p.Tq + ei] = (em + __log2f(l_all)) * 0.69314718055994531f;
             if (__any_sync(0xffffffffu, store && !(bad == 0.f)) && lane == 0)
                 atomicOr(&g_plx_status, PLX_DEV_ERR_NONFINITE);

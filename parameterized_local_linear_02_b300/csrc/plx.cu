@@ -539,6 +539,7 @@ const char* plx_strerror(plx_status status) {
         case PLX_ERR_TIMEOUT: return "device-side wait timed out";
         case PLX_ERR_WORKSPACE: return "decode workspace missing or too small";
         case PLX_ERR_RANGE: return "non-finite output (inputs outside the supported range)";
+        case PLX_ERR_BOUNDS: return "index outside its buffer (debug build)";
         default: return "unknown status";
     }
 }
@@ -1071,6 +1072,7 @@ plx_status plx_last_device_error(void* stream) {
         if (v && cudaMemcpyToSymbol(plx::g_plx_status, &zero, sizeof(zero)) != cudaSuccess) return PLX_ERR_CUDA;
         if (v & plx::PLX_DEV_ERR_TIMEOUT) return PLX_ERR_TIMEOUT;
         if (v & plx::PLX_DEV_ERR_SEQLEN) return PLX_ERR_INVALID_ARG;
+        if (v & plx::PLX_DEV_ERR_BOUNDS) return PLX_ERR_BOUNDS;
         if (v & plx::PLX_DEV_ERR_NONFINITE) return PLX_ERR_RANGE;
         return PLX_OK;
     } catch (...) {

@@ -16,6 +16,7 @@ namespace plx {
 constexpr unsigned PLX_DEV_ERR_TIMEOUT = 1u;
 constexpr unsigned PLX_DEV_ERR_SEQLEN = 2u;
 constexpr unsigned PLX_DEV_ERR_NONFINITE = 4u;
+constexpr unsigned PLX_DEV_ERR_BOUNDS = 8u;       // debug builds: an index outside its buffer
 
 // a wait gives up after this much wall time (ns) or this many polls
 constexpr unsigned long long PLX_WAIT_TIMEOUT_NS = 4000000000ull;

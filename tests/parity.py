@@ -53,3 +53,30 @@ def assert_lse(got, ref, tol, what=""):
     with np.errstate(invalid="ignore"):          # -inf - -inf where both rows are empty
         err = np.where(both_inf, 0.0, np.abs(got - ref))
     assert float(err.max()) <= tol, f"{what}: lse max abs err {float(err.max()):.2e}"
+
+
+SENTINEL = -768.0      # exact in fp32, bf16 and fp16; no kernel output here takes it
+
+
+def canary(shape, dtype, guard=1024):
+    """A device tensor of ``shape`` filled with NaN (so an element the kernel
+    does not write shows up in the comparison), inside a buffer whose
+    ``guard`` elements before and after hold SENTINEL.  Returns
+    ``(tensor, intact)``; ``intact()`` is True while no write has left the
+    tensor.  Integer dtypes (workspaces) are filled with 0xFF bytes instead of
+    NaN."""
+    import torch
+    n = int(np.prod(shape))
+    if dtype.is_floating_point:
+        buf = torch.full((n + 2 * guard,), float("nan"), dtype=dtype, device="cuda")
+        sent = torch.tensor(SENTINEL, dtype=dtype, device="cuda")
+    else:
+        buf = torch.full((n + 2 * guard,), 0xFF, dtype=dtype, device="cuda")
+        sent = torch.tensor(0x5A, dtype=dtype, device="cuda")
+    buf[:guard] = sent
+    buf[guard + n:] = sent
+    view = buf[guard:guard + n].view(shape)
+
+    def intact():
+        return bool(torch.all(buf[:guard] == sent)) and bool(torch.all(buf[guard + n:] == sent))
+    return view, intact

@@ -9,7 +9,7 @@ import pytest
 
 import plx_inputs
 from oracle.backward import plx_backward
-from parity import assert_bf16
+from parity import assert_bf16, canary
 
 pytestmark = pytest.mark.gpu
 
@@ -27,9 +27,17 @@ def run_bwd(x, dout, rho=True):
     t = x.device_tensors()
     r = t["rho"] if rho else None
     do = torch.from_numpy(dout).to("cuda").to(torch.bfloat16)
-    g = plx.plx_bwd(t["q"], t["k"], t["v"], r, do, scale=x.scale)
+    # NaN-filled gradients and a 0xFF-filled workspace inside sentinel guards:
+    # every gradient element must be written, and nothing around them
+    shape = (x.B, x.H, x.N, x.d)
+    bufs = [canary(shape, torch.float32) for _ in range(4 if rho else 3)]
+    grads = tuple(b[0] for b in bufs) + ((None,) if not rho else ())
+    ws, ws_ok = canary((plx.plx_bwd_bf16_workspace_size(x.B, x.H, x.N, x.d),), torch.uint8)
+    g = plx.plx_bwd(t["q"], t["k"], t["v"], r, do, scale=x.scale, workspace=ws, grads=grads)
     torch.cuda.synchronize()
     assert plx.plx_last_device_error() == 0
+    assert all(ok() for _, ok in bufs) and ws_ok(), "plx_bwd wrote outside its gradients or workspace"
+    assert not any(bool(torch.isnan(a).any()) for a in g if a is not None), "a gradient element was not written"
     return [None if a is None else a.cpu().numpy() for a in g]
 
 

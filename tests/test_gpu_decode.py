@@ -4,7 +4,7 @@ import pytest
 
 import oracle
 import plx_inputs
-from parity import LSE_BF16, assert_bf16, assert_f32, assert_lse
+from parity import LSE_BF16, assert_bf16, assert_f32, assert_lse, canary
 
 pytestmark = pytest.mark.gpu
 
@@ -14,11 +14,24 @@ def device(x):
 
 
 def run(t, rho=True, **kw):
+    """plx_decode into NaN-filled outputs and a 0xFF-filled workspace, each
+    inside sentinel guards: every output element must be written, every
+    partial read must have been written first, and nothing outside is touched."""
     import torch
     import parameterized_local_linear_02_b300 as plx
-    out, lse = plx.plx_decode(t["q"], t["rho"] if rho else None, t["k_cache"], t["v_cache"],
-                              t["seqlens"], **kw)
+    B, H, S_cap, d = t["k_cache"].shape
+    od = kw.pop("out_dtype", torch.bfloat16)
+    out, out_ok = canary((B, H, d), od)
+    lse, lse_ok = canary((B, H), torch.float32)
+    ws_ok = lambda: True
+    need = plx.plx_decode_workspace_size(B, H, d, S_cap, kw.get("num_splits", 0))
+    if need > 0 and "workspace" not in kw:
+        kw["workspace"], ws_ok = canary((need,), torch.uint8)
+    plx.plx_decode(t["q"], t["rho"] if rho else None, t["k_cache"], t["v_cache"], t["seqlens"], out=out, lse=lse,
+                   **kw)
     torch.cuda.synchronize()
+    assert out_ok() and lse_ok() and ws_ok(), "plx_decode wrote outside its outputs or workspace"
+    assert not bool(torch.isnan(out).any()) and not bool(torch.isnan(lse).any()), "an output element was not written"
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 

@@ -4,20 +4,25 @@ import pytest
 
 import oracle
 import plx_inputs
-from parity import LSE_BF16, assert_bf16, assert_bf16_output, assert_lse
+from parity import LSE_BF16, assert_bf16, assert_bf16_output, assert_lse, canary
 
 pytestmark = pytest.mark.gpu
 
 
 def run(x, rho=True, out_dtype="f32"):
+    """plx_fwd into NaN-filled outputs inside sentinel guards: every output
+    element must be written, and nothing around them."""
     import torch
     import parameterized_local_linear_02_b300 as plx
     t = x.device_tensors()
     od = torch.float32 if out_dtype == "f32" else torch.bfloat16
-    out, lse = plx.plx_fwd(t["q"], t["k"], t["v"], t["rho"] if rho else None, scale=x.scale,
-                           out_dtype=od)
+    out, out_ok = canary((x.B, x.H, x.N, x.d), od)
+    lse, lse_ok = canary((x.B, x.H, x.N), torch.float32)
+    plx.plx_fwd(t["q"], t["k"], t["v"], t["rho"] if rho else None, scale=x.scale, out=out, lse=lse)
     torch.cuda.synchronize()
     assert plx.plx_last_device_error() == 0
+    assert out_ok() and lse_ok(), "plx_fwd wrote outside its outputs"
+    assert not bool(torch.isnan(out).any()) and not bool(torch.isnan(lse).any()), "an output element was not written"
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 
