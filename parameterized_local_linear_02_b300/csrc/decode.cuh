@@ -39,7 +39,9 @@ struct DecodeCfg {
     static constexpr int OFF_V = NSTAGE * TILE_BYTES;
     static constexpr int OFF_MERGE = 2 * NSTAGE * TILE_BYTES;
     static constexpr int MERGE_FLOATS = CWARPS * PART;
-    static constexpr int OFF_BAR = OFF_MERGE + MERGE_FLOATS * 4;
+    // the block's own state, read by the cluster's rank 0 in the fused combine
+    static constexpr int OFF_CPART = OFF_MERGE + MERGE_FLOATS * 4;
+    static constexpr int OFF_BAR = OFF_CPART + PART * 4;
     static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + 16;
     static_assert(D == 64 || D == 128, "decode supports d in {64, 128}");
     static_assert(ROWS_PER_WARP == 8, "transposed reduction assumes 8 rows per warp");
@@ -101,7 +103,27 @@ __device__ __forceinline__ void store_out(void* out, int out_f32, size_t idx, fl
     else reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
 }
 
-template <int D, bool PLX>
+// The cluster combine: every split of one (b, h) is a CTA of one thread-block
+// cluster (splits <= 16), each CTA leaves its state in its shared memory,
+// and the cluster's rank 0 reads them through distributed shared memory and
+// writes the output.  One launch instead of split kernel + combine kernel.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+template <int D, bool PLX, bool FUSED = false>
 __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
 plx_decode_split_kernel(const DecodeParams p) {
     using Cfg = DecodeCfg<D>;
@@ -110,6 +132,7 @@ plx_decode_split_kernel(const DecodeParams p) {
     __nv_bfloat16* kbuf = reinterpret_cast<__nv_bfloat16*>(smem + Cfg::OFF_K);
     __nv_bfloat16* vbuf = reinterpret_cast<__nv_bfloat16*>(smem + Cfg::OFF_V);
     float* merge = reinterpret_cast<float*>(smem + Cfg::OFF_MERGE);
+    float* cpart = reinterpret_cast<float*>(smem + Cfg::OFF_CPART);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     uint64_t* empty = full + NSTAGE;
     int* abort_flag = reinterpret_cast<int*>(empty + NSTAGE);
@@ -193,8 +216,8 @@ plx_decode_split_kernel(const DecodeParams p) {
             for (int i = max(0, issued - NSTAGE); i < issued; ++i)
                 if (!mbar_wait(&full[i % NSTAGE], (i / NSTAGE) & 1)) atomicOr(&g_plx_status, PLX_DEV_ERR_TIMEOUT);
         }
-        return;
-    }
+        if constexpr (!FUSED) return;
+    } else {
 
     // ---------------- consumers (warps 0..3)
     float qr[DPL], rr[DPL];
@@ -331,12 +354,49 @@ plx_decode_split_kernel(const DecodeParams p) {
             store_out(p.out, p.out_f32, static_cast<size_t>(bh) * D + t, o);
             if (t == 0 && p.lse)
                 p.lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+        } else if (FUSED) {
+            if (t == 0) { cpart[0] = M; cpart[1] = Lsum; cpart[2] = Cs; cpart[3] = 0.f; }
+            cpart[4 + t] = As;
+            cpart[4 + D + t] = Us;
         } else {
             float* part = p.ws + (static_cast<size_t>(bh) * p.splits + split) * Cfg::PART;
             if (t == 0) { part[0] = M; part[1] = Lsum; part[2] = Cs; part[3] = 0.f; }
             part[4 + t] = As;
             part[4 + D + t] = Us;
         }
+    }
+    }   // consumers
+    if constexpr (FUSED) {
+        // every thread of every CTA of the cluster reaches both barriers: the
+        // first publishes the CTAs' states, the second keeps them alive until
+        // rank 0 has read them.  The merge is the combine kernel's, in rank order.
+        cluster_sync_all();
+        if (cluster_rank() == 0 && threadIdx.x < D) {
+            const int t = threadIdx.x;
+            float M = -INFINITY;
+            for (int r = 0; r < p.splits; ++r) M = fmaxf(M, ld_cluster_f32(cpart, r));
+            float Lsum = 0.f, Cs = 0.f, As = 0.f, Us = 0.f;
+            if (M != -INFINITY) {
+                for (int r = 0; r < p.splits; ++r) {
+                    const float mr = ld_cluster_f32(cpart, r);
+                    if (mr == -INFINITY) continue;
+                    const float sc = exp2f(mr - M);
+                    Lsum = fmaf(sc, ld_cluster_f32(cpart + 1, r), Lsum);
+                    Cs = fmaf(sc, ld_cluster_f32(cpart + 2, r), Cs);
+                    As = fmaf(sc, ld_cluster_f32(cpart + 4 + t, r), As);
+                    if constexpr (PLX) Us = fmaf(sc, ld_cluster_f32(cpart + 4 + D + t, r), Us);
+                }
+            }
+            float o = 0.f;
+            if (Lsum > 0.f) {
+                const float inv = 1.f / Lsum;
+                const float vbar = As * inv;
+                o = PLX ? (p.no_intercept ? -Us * inv : fmaf(Cs * inv, vbar, vbar) - Us * inv) : vbar;
+            }
+            store_out(p.out, p.out_f32, static_cast<size_t>(bh) * D + t, o);
+            if (t == 0 && p.lse) p.lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+        }
+        cluster_sync_all();
     }
 }
 

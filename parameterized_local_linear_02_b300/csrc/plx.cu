@@ -40,7 +40,12 @@ inline bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uin
 struct DeviceInfo {
     int sm_count = 0;
     int decode_blocks_per_sm[2] = {0, 0};   // d = 64, d = 128
+    // the decode's split combine runs inside one thread-block cluster of up to
+    // kMaxFusedSplits CTAs (false if no such cluster can be resident)
+    bool decode_cluster_ok = false;
 };
+
+constexpr int kMaxFusedSplits = 16;
 
 std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
@@ -90,7 +95,42 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_decode_split_kernel<128, false>, DecodeCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_decode_split_kernel<64, true>, DecodeCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_decode_split_kernel<64, false>, DecodeCfg<64>::SMEM);
+    e = e ? e : set_smem(plx::plx_decode_split_kernel<128, true, true>, DecodeCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_decode_split_kernel<128, false, true>, DecodeCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_decode_split_kernel<64, true, true>, DecodeCfg<64>::SMEM);
+    e = e ? e : set_smem(plx::plx_decode_split_kernel<64, false, true>, DecodeCfg<64>::SMEM);
     if (e != cudaSuccess) return nullptr;
+    // clusters of more than 8 CTAs are opt-in; without the opt-in, or if no
+    // cluster of kMaxFusedSplits decode CTAs fits, the combine stays a kernel
+    {
+        bool ok = true;
+        auto allow = [&](auto kernel) {
+            ok = ok && cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        };
+        allow(plx::plx_decode_split_kernel<128, true, true>);
+        allow(plx::plx_decode_split_kernel<128, false, true>);
+        allow(plx::plx_decode_split_kernel<64, true, true>);
+        allow(plx::plx_decode_split_kernel<64, false, true>);
+        if (ok) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 1;
+            attr[0].val.clusterDim.y = kMaxFusedSplits;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(1, kMaxFusedSplits, 1);
+            cfg.blockDim = dim3(DecodeCfg<128>::THREADS, 1, 1);
+            cfg.dynamicSmemBytes = DecodeCfg<128>::SMEM;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            ok = cudaOccupancyMaxActiveClusters(&clusters, plx::plx_decode_split_kernel<128, true, true>, &cfg) ==
+                     cudaSuccess &&
+                 clusters > 0;
+        }
+        cudaGetLastError();   // a refused opt-in is not an error of the library
+        info.decode_cluster_ok = ok;
+    }
     int nb = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, plx::plx_decode_split_kernel<64, true>,
                                                       DecodeCfg<64>::THREADS, DecodeCfg<64>::SMEM) != cudaSuccess)
@@ -407,25 +447,66 @@ bool dispatch_bwd(const plx::BwdF32Params& p, int d, long long BH, cudaStream_t 
 //   ceil(BH s / slots) x (tiles per block + fixed cost per block)
 // plus the combine pass when s > 1; pick the s that minimises it, with at least
 // 8 tiles (256 cache rows) per block.
+struct DecodePlan {
+    int splits = 1;
+    bool fused = false;   // the combine inside a thread-block cluster (one launch)
+};
+
+// Split count and combine form of the decode.  A split combine costs a second
+// launch (kCombineCost, in tile units) unless it runs inside a cluster, which
+// holds at most kMaxFusedSplits CTAs.
+DecodePlan decode_plan(const DeviceInfo& info, long long BH, int d, int S_cap);
+
 int decode_splits(const DeviceInfo& info, long long BH, int d, int S_cap) {
+    return decode_plan(info, BH, d, S_cap).splits;
+}
+
+// The combine form for a given split count: inside a cluster when the grid is
+// a single wave (measured: it saves the combine launch on small grids, about
+// 2 us, but co-scheduling the CTAs of a cluster costs 10-20 % of bandwidth on
+// grids of several waves).
+bool decode_fused(const DeviceInfo& info, long long BH, int splits) {
+    const long long slots = static_cast<long long>(info.sm_count) * info.decode_blocks_per_sm[1];
+    return info.decode_cluster_ok && splits >= 2 && splits <= kMaxFusedSplits && BH * splits <= slots;
+}
+
+DecodePlan decode_plan(const DeviceInfo& info, long long BH, int d, int S_cap) {
     constexpr int T = 32;
     const long long slots = static_cast<long long>(info.sm_count) * info.decode_blocks_per_sm[d == 128 ? 1 : 0];
     const double tiles = static_cast<double>((static_cast<long long>(S_cap) + T - 1) / T);
-    long long smax = (static_cast<long long>(S_cap) + 8 * T - 1) / (8 * T);
-    if (smax > 1024) smax = 1024;
-    if (smax < 1) smax = 1;
     constexpr double kBlockCost = 2.0;     // per-block setup and merge, in tile units
     constexpr double kCombineCost = 4.0;   // the combine launch, in tile units
-    int best = 1;
-    double best_t = 0.0;
-    for (long long s = 1; s <= smax; ++s) {
+    auto cost = [&](long long s, bool fused) {
         const double waves = static_cast<double>((BH * s + slots - 1) / slots);
-        const double t = waves * (tiles / static_cast<double>(s) + kBlockCost) + (s > 1 ? kCombineCost : 0.0);
-        if (s == 1 || t < best_t) {
+        return waves * (tiles / static_cast<double>(s) + kBlockCost) + (s > 1 && !fused ? kCombineCost : 0.0);
+    };
+    // a split of at least 8 tiles with the combine kernel, of at least 4 in a cluster
+    long long smax = (static_cast<long long>(S_cap) + 8 * T - 1) / (8 * T);
+    smax = smax > 1024 ? 1024 : (smax < 1 ? 1 : smax);
+    DecodePlan best;
+    double best_t = cost(1, false);
+    for (long long s = 2; s <= smax; ++s) {
+        const double t = cost(s, false);
+        if (t < best_t) {
             best_t = t;
-            best = static_cast<int>(s);
+            best.splits = static_cast<int>(s);
+            best.fused = false;
         }
     }
+    if (info.decode_cluster_ok) {
+        long long fmax = (static_cast<long long>(S_cap) + 4 * T - 1) / (4 * T);
+        fmax = fmax > kMaxFusedSplits ? kMaxFusedSplits : fmax;
+        for (long long s = 2; s <= fmax && BH * s <= slots; ++s) {
+            const double t = cost(s, true);
+            if (t < best_t) {
+                best_t = t;
+                best.splits = static_cast<int>(s);
+                best.fused = true;
+            }
+        }
+    }
+    // a split count that a cluster holds always runs fused (same result, one launch)
+    best.fused = decode_fused(info, BH, best.splits);
     return best;
 }
 
@@ -447,9 +528,26 @@ void launch_decode_combine(const plx::DecodeParams& p, long long BH, cudaStream_
 }
 
 template <int D, bool PLX>
-void launch_decode(const plx::DecodeParams& p, long long BH, cudaStream_t s) {
+void launch_decode(const plx::DecodeParams& p, long long BH, cudaStream_t s, bool fused) {
     using Cfg = DecodeCfg<D>;
     dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(p.splits));
+    if (fused) {
+        // the splits of one (b, h) form one cluster; its rank 0 merges them
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = static_cast<unsigned>(p.splits);
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::SMEM;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, plx::plx_decode_split_kernel<D, PLX, true>, p);
+        return;
+    }
     plx::plx_decode_split_kernel<D, PLX><<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(p);
     if (p.splits > 1) plx::plx_decode_combine_kernel<D, PLX><<<static_cast<unsigned>(BH), D, 0, s>>>(p);
 }
@@ -769,7 +867,9 @@ plx_status decode_impl(const void* q, const void* rho, const void* k_cache, cons
         const DeviceInfo* info = device_info();
         if (!info) return PLX_ERR_CUDA;
         const int splits = num_splits > 0 ? num_splits : decode_splits(*info, BH, d, S_cap);
-        const size_t need = decode_ws_bytes(BH, d, splits);
+        // a cluster-fused combine keeps the partials on chip: no workspace needed
+        const bool fused = decode_fused(*info, BH, splits);
+        const size_t need = fused ? 0 : decode_ws_bytes(BH, d, splits);
         if (need > 0 && (!workspace || workspace_bytes < need)) return PLX_ERR_WORKSPACE;
         plx::DecodeParams p;
         p.q = static_cast<const __nv_bfloat16*>(q);
@@ -795,11 +895,11 @@ plx_status decode_impl(const void* q, const void* rho, const void* k_cache, cons
         p.groups = 1;
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         if (d == 128) {
-            if (rho) launch_decode<128, true>(p, BH, s);
-            else launch_decode<128, false>(p, BH, s);
+            if (rho) launch_decode<128, true>(p, BH, s, fused);
+            else launch_decode<128, false>(p, BH, s, fused);
         } else {
-            if (rho) launch_decode<64, true>(p, BH, s);
-            else launch_decode<64, false>(p, BH, s);
+            if (rho) launch_decode<64, true>(p, BH, s, fused);
+            else launch_decode<64, false>(p, BH, s, fused);
         }
         return launch_status();
     } catch (...) {
