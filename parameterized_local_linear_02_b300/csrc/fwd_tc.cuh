@@ -347,8 +347,9 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                 const int b = g & 1;
                 const uint32_t tS = tmem + (b ? Cfg::TM_S1 : Cfg::TM_S0);
                 const uint32_t tR = tmem + (b ? Cfg::TM_R1 : Cfg::TM_R0);
-                static_assert(Cfg::Q_PANEL == 1024 * 16 && Cfg::KV_PANEL == 512 * 16, "panel strides of the S/R batch");
-                mma_sr_batch<D, PLX>(tS, tR, a_q, a_r, sdesc_sw128(sKa + ks * Cfg::KV_BYTES, 16, 1024), ID_S);
+                static_assert(Cfg::KV_PANEL == 512 * 16, "panel stride of the S/R batch");
+                mma_sr_batch<D, PLX, Cfg::Q_PANEL / 16>(tS, tR, a_q, a_r, sdesc_sw128(sKa + ks * Cfg::KV_BYTES, 16, 1024),
+                                                        ID_S);
                 mma_commit_warp(&k_empty[ks]);
                 mma_commit_warp(&s_full[b]);
                 if (j == n_kv - 1) mma_commit_warp(q_empty);

@@ -381,14 +381,15 @@ __device__ __forceinline__ void tmem_st32x32b_x32(uint32_t taddr, const uint32_t
 //
 // The S/R batch of the prefill: D(S) (+)= Q K^T and, for PLX, D(R) (+)= rho K^T
 // over D/16 k-steps of 16; Q, rho and K tiles are K-major, 128B-swizzled
-// 64-column panels (the k-step's 32 bytes at (k % 4) * 32 within a panel,
-// panels a_panel / b_panel bytes apart).  The first k-step overwrites D.
-template <int D, bool PLX>
+// 64-column panels (the k-step's 32 bytes at (k % 4) * 32 within a panel),
+// Q/rho panels A16 x 16 bytes apart (BM rows of 128 bytes) and K panels
+// 512 x 16 bytes apart (64 rows).  The first k-step overwrites D.
+template <int D, bool PLX, int A16>
 __device__ __forceinline__ void mma_sr_batch(uint32_t t_s, uint32_t t_r, uint64_t a_q, uint64_t a_r, uint64_t b_k,
                                              uint32_t idesc);
 template <>
-__device__ __forceinline__ void mma_sr_batch<64, true>(uint32_t t_s, uint32_t t_r, uint64_t a_q, uint64_t a_r,
-                                                        uint64_t b_k, uint32_t idesc) {
+__device__ __forceinline__ void mma_sr_batch<64, true, 1024>(uint32_t t_s, uint32_t t_r, uint64_t a_q,
+                                                              uint64_t a_r, uint64_t b_k, uint32_t idesc) {
     asm volatile("{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 lo;\n\t.reg .b64 da, db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\tadd.u32 lo, %6, 0; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 0; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pf;\n\tadd.u32 lo, %4, 0; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pf;\n\tadd.u32 lo, %6, 2; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 2; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 2; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 4; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 4; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 4; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 6; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 6; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 6; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\t}"
                  ::"r"(t_s), "r"(t_r), "r"(static_cast<uint32_t>(a_q)), "r"(static_cast<uint32_t>(a_q >> 32)),
                    "r"(static_cast<uint32_t>(a_r)), "r"(static_cast<uint32_t>(a_r >> 32)),
@@ -396,8 +397,8 @@ __device__ __forceinline__ void mma_sr_batch<64, true>(uint32_t t_s, uint32_t t_
                  : "memory");
 }
 template <>
-__device__ __forceinline__ void mma_sr_batch<64, false>(uint32_t t_s, uint32_t t_r, uint64_t a_q, uint64_t a_r,
-                                                        uint64_t b_k, uint32_t idesc) {
+__device__ __forceinline__ void mma_sr_batch<64, false, 1024>(uint32_t t_s, uint32_t t_r, uint64_t a_q,
+                                                              uint64_t a_r, uint64_t b_k, uint32_t idesc) {
     asm volatile("{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 lo;\n\t.reg .b64 da, db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\tadd.u32 lo, %6, 0; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 0; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pf;\n\tadd.u32 lo, %6, 2; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 2; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 4; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 4; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 6; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 6; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\t}"
                  ::"r"(t_s), "r"(t_r), "r"(static_cast<uint32_t>(a_q)), "r"(static_cast<uint32_t>(a_q >> 32)),
                    "r"(static_cast<uint32_t>(a_r)), "r"(static_cast<uint32_t>(a_r >> 32)),
@@ -405,8 +406,8 @@ __device__ __forceinline__ void mma_sr_batch<64, false>(uint32_t t_s, uint32_t t
                  : "memory");
 }
 template <>
-__device__ __forceinline__ void mma_sr_batch<128, true>(uint32_t t_s, uint32_t t_r, uint64_t a_q, uint64_t a_r,
-                                                        uint64_t b_k, uint32_t idesc) {
+__device__ __forceinline__ void mma_sr_batch<128, true, 1024>(uint32_t t_s, uint32_t t_r, uint64_t a_q,
+                                                              uint64_t a_r, uint64_t b_k, uint32_t idesc) {
     asm volatile("{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 lo;\n\t.reg .b64 da, db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\tadd.u32 lo, %6, 0; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 0; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pf;\n\tadd.u32 lo, %4, 0; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pf;\n\tadd.u32 lo, %6, 2; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 2; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 2; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 4; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 4; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 4; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 6; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 6; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 6; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 512; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1024; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 1024; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 514; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1026; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 1026; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 516; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1028; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 1028; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\tadd.u32 lo, %6, 518; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1030; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %4, 1030; mov.b64 da, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %8, pt;\n\t}"
                  ::"r"(t_s), "r"(t_r), "r"(static_cast<uint32_t>(a_q)), "r"(static_cast<uint32_t>(a_q >> 32)),
                    "r"(static_cast<uint32_t>(a_r)), "r"(static_cast<uint32_t>(a_r >> 32)),
@@ -414,24 +415,14 @@ __device__ __forceinline__ void mma_sr_batch<128, true>(uint32_t t_s, uint32_t t
                  : "memory");
 }
 template <>
-__device__ __forceinline__ void mma_sr_batch<128, false>(uint32_t t_s, uint32_t t_r, uint64_t a_q, uint64_t a_r,
-                                                        uint64_t b_k, uint32_t idesc) {
+__device__ __forceinline__ void mma_sr_batch<128, false, 1024>(uint32_t t_s, uint32_t t_r, uint64_t a_q,
+                                                              uint64_t a_r, uint64_t b_k, uint32_t idesc) {
     asm volatile("{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 lo;\n\t.reg .b64 da, db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\tadd.u32 lo, %6, 0; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 0; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pf;\n\tadd.u32 lo, %6, 2; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 2; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 4; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 4; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 6; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 6; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 512; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1024; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 514; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1026; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 516; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1028; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\tadd.u32 lo, %6, 518; mov.b64 db, {lo, %7};\n\tadd.u32 lo, %2, 1030; mov.b64 da, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %8, pt;\n\t}"
                  ::"r"(t_s), "r"(t_r), "r"(static_cast<uint32_t>(a_q)), "r"(static_cast<uint32_t>(a_q >> 32)),
                    "r"(static_cast<uint32_t>(a_r)), "r"(static_cast<uint32_t>(a_r >> 32)),
                    "r"(static_cast<uint32_t>(b_k)), "r"(static_cast<uint32_t>(b_k >> 32)), "r"(idesc)
                  : "memory");
 }
-
-// The PV batch of the prefill: O (+)= P V and, for PLX, U (+)= (P o R) V over
-// the tile's 64 keys in 4 k-steps of 16.  P and PR are fp16 pairs in TMEM:
-// keys [32h, 32h + 32) at columns [32h, 32h + 16) of the buffer t_p + P_OFF
-// (P) and t_p + PR_OFF (PR); V is the MN-major B operand, k-step kk at
-// kk * 2048 bytes (b_v its base descriptor).  acc0 = 0: the first k-step
-// overwrites O and U.
-template <bool PLX, int P_OFF, int PR_OFF>
-__device__ __forceinline__ void mma_pv_batch(uint32_t t_o, uint32_t t_u, uint32_t t_p, uint64_t b_v, uint32_t idesc,
-                                             uint32_t acc0);
 template <>
 __device__ __forceinline__ void mma_pv_batch<true, 0, 64>(uint32_t t_o, uint32_t t_u, uint32_t t_p, uint64_t b_v,
                                                         uint32_t idesc, uint32_t acc0) {

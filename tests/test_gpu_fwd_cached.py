@@ -54,7 +54,9 @@ def run(B, H, T, S_cap, d, seqlens, seed, rho=True):
 
 
 @pytest.mark.parametrize("T,S_cap,seqlens", [(16, 512, [512, 300, 16]), (200, 640, [600, 200, 457]),
-                                             (1, 256, [256, 1, 77]), (128, 384, [383, 128, 129])])
+                                             (1, 256, [256, 1, 77]), (128, 384, [383, 128, 129]),
+                                             (64, 512, [512, 64, 100]), (65, 512, [512, 65, 400]),
+                                             (33, 300, [300, 33, 250])])
 def test_cached_matches_oracle(T, S_cap, seqlens):
     got, exp, lg, le = run(3, 2, T, S_cap, 128, seqlens, seed=T + S_cap)
     assert_bf16(got, exp, f"cached T={T}")
