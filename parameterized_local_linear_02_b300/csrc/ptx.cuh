@@ -423,6 +423,16 @@ __device__ __forceinline__ void mma_sr_batch<128, false, 1024>(uint32_t t_s, uin
                    "r"(static_cast<uint32_t>(b_k)), "r"(static_cast<uint32_t>(b_k >> 32)), "r"(idesc)
                  : "memory");
 }
+
+// The PV batch of the prefill: O (+)= P V and, for PLX, U (+)= (P o R) V over
+// the tile's 64 keys in 4 k-steps of 16.  P and PR are fp16 pairs in TMEM:
+// keys [32h, 32h + 32) at columns [32h, 32h + 16) of the buffer t_p + P_OFF
+// (P) and t_p + PR_OFF (PR); V is the MN-major B operand, k-step kk at
+// kk * 2048 bytes (b_v its base descriptor).  acc0 = 0: the first k-step
+// overwrites O and U.
+template <bool PLX, int P_OFF, int PR_OFF>
+__device__ __forceinline__ void mma_pv_batch(uint32_t t_o, uint32_t t_u, uint32_t t_p, uint64_t b_v, uint32_t idesc,
+                                             uint32_t acc0);
 template <>
 __device__ __forceinline__ void mma_pv_batch<true, 0, 64>(uint32_t t_o, uint32_t t_u, uint32_t t_p, uint64_t b_v,
                                                         uint32_t idesc, uint32_t acc0) {
