@@ -118,6 +118,21 @@ def test_lla_converged_matches_direct_solve(shape, lam):
         assert_f32(out[b, h], o_ref, f"{shape} o vs direct solve", tol=1e-3)
 
 
+@pytest.mark.parametrize("shape,lam", [((1, 2, 200, 64), 1.0), ((1, 1, 160, 128), 0.5)])
+def test_lla_well_conditioned_matches_direct_solve_at_fp32_tolerance(shape, lam):
+    """With a ridge that keeps (Sigma_KK + lambda I) well conditioned (lambda
+    of the order of the key variance), the converged fp32 CG output meets the
+    fp32 path's tolerance, 1e-4 of the RMS, against the dense fp64 solve."""
+    B, H, N, d = shape
+    x = inputs(B, H, N, d, seed=5 * N + d)
+    tol, iters = 1e-6, 4 * d
+    out, rho, _, steps = run_lla(x, lam, iters, tol)
+    ref = lla.lla_direct(x.q, x.k, x.v, x.scale, lam)
+    for (b, h), (o_ref, rho_ref, rows) in ref.items():
+        mx, mn = assert_f32(out[b, h], o_ref, f"{shape} lambda {lam} o vs direct solve", tol=1e-4)
+        print(f"well-conditioned LLA {shape} lambda {lam}: max {mx:.2e} mean {mn:.2e}")
+
+
 def test_lla_full_size_sampled_rows():
     """The bench's LLA workload in the launch configuration the bench times:
     B=4, H=16, N=2048, d=128 fp32, lambda = 0.1, at most 48 steps, tol 1e-4
