@@ -331,6 +331,13 @@ def run_ours(args, world, rank, local):
             b.record(stream)
         return evs
 
+    # the clock sampler starts (and gets its first sample) before the warm-up,
+    # so the GPU does not idle between the warm-up and the timed region (an
+    # idle GPU drops its clocks, and the first timed launches would run while
+    # they ramp back up)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
     for _ in range(args.warmup):
         flush.zero_()
         if do_pf:
@@ -344,9 +351,6 @@ def run_ours(args, world, rank, local):
         raise RuntimeError("device status set during warm-up")
 
     # ---- timed region: K steps of (prefill, decode)
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
     ev_f, ev_l, ev_d = [], [], []
