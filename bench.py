@@ -681,7 +681,33 @@ def run_backward_bench(args, world, rank, local):
                          "roofline": {"bound": "alu", "peak": alu_peak,
                                       "frac": flops / (f32_ms * 1e-3) / 1e12 / alu_peak}},
             "speedup_over_f32_path": f32_ms / med,
-            "gpu_launches": 3 * nsteps, "clocks": clocks, "device_status": plx.plx_last_device_error()}
+            "gpu_launches": 3 * nsteps, "clocks": clocks}
+    # the training pair: plx_fwd_train saves vbar and c beside o and lse, and
+    # plx_bwd_saved forms the row statistics from them (a bandwidth-bound
+    # kernel) instead of the statistics pass
+    o_t = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    lse_t = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    vbar_t = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    c_t = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    fwd_train = lambda: plx.plx_fwd_train(tb["q"], tb["k"], tb["v"], tb["rho"], scale=x.scale, out=o_t, lse=lse_t,
+                                          vbar=vbar_t, c=c_t)
+    fwd_plain = lambda: plx.plx_fwd(tb["q"], tb["k"], tb["v"], tb["rho"], scale=x.scale, out=o_t, lse=lse_t)
+    fp_ms, _ = timed(fwd_plain, max(3, args.steps), 3)
+    ft_ms, _ = timed(fwd_train, max(3, args.steps), 3)
+    sv_ms, sv_steps = timed(lambda: plx.plx_bwd_saved(tb["q"], tb["k"], tb["v"], tb["rho"], dout, o_t, lse_t, vbar_t,
+                                                      c_t, scale=x.scale, workspace=ws, grads=grads),
+                            max(3, args.steps), 3)
+    sv_val = flops / (sv_ms * 1e-3) / 1e12
+    fwd_flops = pairs * 8 * d
+    line["saved_path"] = {
+        "bwd_ms": sv_ms, "value": sv_val, "unit": "TFLOP/s", "frac": sv_val / peak,
+        "implementation_flop_per_pair": 20 * d,
+        "fwd_train_ms": ft_ms, "fwd_ms": fp_ms, "fwd_train_tflops": fwd_flops / (ft_ms * 1e-3) / 1e12,
+        "train_step_ms": ft_ms + sv_ms, "recompute_train_step_ms": fp_ms + med,
+        "inputs": "plx_fwd_train's o (fp32), lse, vbar (fp32), c; bf16 q, k, v, rho, dout",
+        "l2": "flushed (256 MiB write) before every launch"}
+    line["gpu_launches"] += 3 * sv_steps
+    line["device_status"] = plx.plx_last_device_error()
     print(json.dumps(line), flush=True)
     return 0
 

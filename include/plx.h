@@ -222,6 +222,53 @@ plx_status plx_bwd(const void* q, const void* k, const void* v, const void* rho,
 size_t plx_bwd_bf16_workspace_size(int B, int H, int N, int d);
 
 /*
+ * plx_fwd_train -- plx_fwd for training: the same o and lse (bit for bit), and
+ * also vbar_i = sum_j w_ij v_j (the softmax-attention output o_i^SA of the
+ * same weights) and c_i = sum_j w_ij (rho_i.k_j), the two per-row values the
+ * gradients' row statistics are formed from (plx_bwd_saved).  The pages give
+ * no backward pass; the split follows the streaming identity of
+ * zhichai.net section 1.3 (o = (1 + c) vbar - u).
+ *
+ *   q, k, v, rho : bf16 [B][H][N][d], 16-byte aligned; rho is required.
+ *   out, lse     : as plx_fwd (lse is required here).
+ *   vbar         : fp32 [B][H][N][d] output, 16-byte aligned.
+ *   c            : fp32 [B][H][N] output, 4-byte aligned.
+ *   B, H, N >= 1; d in {64, 128}; scale finite and >= 0.
+ * One launch on `stream`; vbar leaves through the same shared-memory staging
+ * and TMA store as o, so the epilogue of every 128-row tile stores twice.
+ * Errors: PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_MISALIGNED,
+ * PLX_ERR_CUDA; device-side conditions as plx_fwd.
+ */
+plx_status plx_fwd_train(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
+                         float* vbar, float* c, int B, int H, int N, int d, float scale, plx_dtype out_dtype,
+                         void* stream);
+
+/*
+ * plx_bwd_saved -- plx_bwd's gradients from the training forward's saved
+ * values instead of a statistics pass: a bandwidth-bound kernel forms each
+ * row's (log2e lse_i, c_i, a_i = dO_i.vbar_i, D_i = dO_i.o_i + c_i a_i), then
+ * the same dq/drho and dk/dv passes as plx_bwd run.  Inputs as plx_bwd, plus:
+ *
+ *   out, out_dtype : the forward's o (PLX_F32 or PLX_BF16), 16-byte aligned.
+ *   lse            : the forward's lse, fp32 [B][H][N] (natural log).
+ *   vbar, c        : plx_fwd_train's outputs; required with rho, ignored (may
+ *                    be NULL) for softmax attention (rho = NULL), where
+ *                    vbar = o and c = 0.
+ *   workspace      : plx_bwd_bf16_workspace_size(B, H, N, d) bytes.
+ * Three launches on `stream` (the row statistics, the query-tile pass, the
+ * key-tile pass); deterministic.  The gradient passes take the weights from
+ * the forward's lse, whose sum l was formed from the fp16-rounded P, so the
+ * gradients differ from plx_bwd's in the last bits of that rounding.
+ * Errors: PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_MISALIGNED,
+ * PLX_ERR_WORKSPACE, PLX_ERR_CUDA; device-side wait timeouts are reported by
+ * plx_last_device_error.
+ */
+plx_status plx_bwd_saved(const void* q, const void* k, const void* v, const void* rho, const void* dout,
+                         const void* out, plx_dtype out_dtype, const float* lse, const float* vbar, const float* c,
+                         float* dq, float* dk, float* dv, float* drho, void* workspace, size_t workspace_bytes, int B,
+                         int H, int N, int d, float scale, void* stream);
+
+/*
  * plx_decode -- one query token per sequence against a bf16 KV cache
  * (the streaming decode of gist.science "Algoritmo Consapevole
  * dell'Hardware").  The cache already holds the current token at position

@@ -85,6 +85,10 @@ def load(path: str) -> ctypes.CDLL:
     lib.plx_bwd.argtypes = [vp] * 10 + [sz, i, i, i, i, f, vp]
     lib.plx_bwd_bf16_workspace_size.restype = sz
     lib.plx_bwd_bf16_workspace_size.argtypes = [i, i, i, i]
+    lib.plx_fwd_train.restype = i
+    lib.plx_fwd_train.argtypes = [vp] * 8 + [i, i, i, i, f, i, vp]
+    lib.plx_bwd_saved.restype = i
+    lib.plx_bwd_saved.argtypes = [vp] * 6 + [i] + [vp] * 8 + [sz, i, i, i, i, f, vp]
     lib.plx_decode_noalloc.restype = i
     lib.plx_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.plx_probe_proj.restype = i
@@ -305,6 +309,72 @@ def plx_bwd(q, k, v, rho, dout, *, scale=None, workspace=None, grads=None):
     st = library().plx_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                            _ptr(drho), _ptr(workspace), ws_bytes, B, H, N, d, scale, _stream(dev))
     _check(st, "plx_bwd")
+    return dq, dk, dv, drho
+
+
+def plx_fwd_train(q, k, v, rho, *, scale=None, out=None, lse=None, vbar=None, c=None, out_dtype=torch.float32):
+    """plx_fwd for training: returns ``(out, lse, vbar, c)``, where vbar (fp32
+    [B, H, N, d]) and c (fp32 [B, H, N]) are the per-row values plx_bwd_saved
+    forms the gradients' row statistics from.  rho is required."""
+    B, H, N, d = q.shape
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("rho", rho)):
+        _need(t, name, torch.bfloat16, (B, H, N, d), dev)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=out_dtype, device=dev)
+    else:
+        _need(out, "out", out.dtype, (B, H, N, d), dev)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    _need(lse, "lse", torch.float32, (B, H, N), dev)
+    if vbar is None:
+        vbar = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    _need(vbar, "vbar", torch.float32, (B, H, N, d), dev)
+    if c is None:
+        c = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    _need(c, "c", torch.float32, (B, H, N), dev)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().plx_fwd_train(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(out), _ptr(lse), _ptr(vbar), _ptr(c),
+                                 B, H, N, d, scale, _out_code(out.dtype), _stream(dev))
+    _check(st, "plx_fwd_train")
+    return out, lse, vbar, c
+
+
+def plx_bwd_saved(q, k, v, rho, dout, out, lse, vbar=None, c=None, *, scale=None, workspace=None, grads=None):
+    """plx_bwd from the training forward's saved values (plx_fwd_train's out,
+    lse, vbar, c; for ``rho=None`` plx_fwd's out and lse, vbar and c unused):
+    the row statistics come from a bandwidth-bound kernel instead of an
+    attention pass.  Returns (dq, dk, dv, drho), fp32."""
+    B, H, N, d = q.shape
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)) + ((("rho", rho),) if rho is not None else ()):
+        _need(t, name, torch.bfloat16, (B, H, N, d), dev)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be float32 or bfloat16")
+    _need(out, "out", out.dtype, (B, H, N, d), dev)
+    _need(lse, "lse", torch.float32, (B, H, N), dev)
+    if rho is not None:
+        if vbar is None or c is None:
+            raise ValueError("vbar and c are required with rho")
+        _need(vbar, "vbar", torch.float32, (B, H, N, d), dev)
+        _need(c, "c", torch.float32, (B, H, N), dev)
+    else:
+        vbar = c = None
+    if grads is None:
+        grads = tuple(torch.empty((B, H, N, d), dtype=torch.float32, device=dev) for _ in range(3)) + (
+            torch.empty((B, H, N, d), dtype=torch.float32, device=dev) if rho is not None else None,)
+    dq, dk, dv, drho = grads
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)) + ((("drho", drho),) if rho is not None else ()):
+        _need(t, name, torch.float32, (B, H, N, d), dev)
+    need = plx_bwd_bf16_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().plx_bwd_saved(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(dout), _ptr(out), _out_code(out.dtype),
+                                 _ptr(lse), _ptr(vbar), _ptr(c), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(drho),
+                                 _ptr(workspace), ws_bytes, B, H, N, d, scale, _stream(dev))
+    _check(st, "plx_bwd_saved")
     return dq, dk, dv, drho
 
 

@@ -648,4 +648,81 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
     }
 }
 
+// ---------------------------------------------------------------------------
+// The row statistics from the training forward's saved values (plx_bwd_saved),
+// instead of the statistics pass: with vbar_i = O_i / l_i and c_i from the
+// forward, a_i = dO_i.vbar_i and D_i = dO_i.o_i + c_i a_i (the same identities
+// as the header above: e_i = dO_i.u_i with u_i = (1 + c_i) vbar_i - o_i).  For
+// softmax attention (no rho) vbar_i = o_i and c_i = 0.  One warp per row, each
+// lane D/32 consecutive elements (coalesced 16- and 8-byte loads).
+struct BwdPrepParams {
+    const float* lse;      // natural-log lse per row, [rows]
+    const float* c;        // c_i per row, or nullptr (softmax attention)
+    const float* vbar;     // fp32 [rows][D], or nullptr (softmax attention: vbar = o)
+    const void* out;       // the forward's o, fp32 or bf16 [rows][D]
+    const uint16_t* dout;  // bf16 [rows][D]
+    float4* stats;         // (log2e lse, c, a, D) per row
+    long long rows;
+    int out_f32;
+};
+constexpr int BWD_PREP_ROWS_PER_BLOCK = 8;
+
+template <int D>
+__device__ __forceinline__ void load_bf16_vec(const uint16_t* src, float (&x)[D / 32]) {
+    if constexpr (D == 128) {
+        const uint2 w = *reinterpret_cast<const uint2*>(src);
+        x[0] = bf16x2_lo(w.x); x[1] = bf16x2_hi(w.x); x[2] = bf16x2_lo(w.y); x[3] = bf16x2_hi(w.y);
+    } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+        x[0] = bf16x2_lo(w); x[1] = bf16x2_hi(w);
+    }
+}
+template <int D>
+__device__ __forceinline__ void load_f32_vec(const float* src, float (&x)[D / 32]) {
+    if constexpr (D == 128) {
+        const float4 w = *reinterpret_cast<const float4*>(src);
+        x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+    } else {
+        const float2 w = *reinterpret_cast<const float2*>(src);
+        x[0] = w.x; x[1] = w.y;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(BWD_PREP_ROWS_PER_BLOCK * 32)
+plx_bwd_prep_kernel(const BwdPrepParams p) {
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long long row = static_cast<long long>(blockIdx.x) * BWD_PREP_ROWS_PER_BLOCK + (threadIdx.x >> 5);
+    if (row >= p.rows) return;
+    const size_t base = static_cast<size_t>(row) * D + lane * E;
+    float g[E], o[E], vb[E];
+    load_bf16_vec<D>(p.dout + base, g);
+    if (p.out_f32)
+        load_f32_vec<D>(static_cast<const float*>(p.out) + base, o);
+    else
+        load_bf16_vec<D>(static_cast<const uint16_t*>(p.out) + base, o);
+    if (p.vbar) {
+        load_f32_vec<D>(p.vbar + base, vb);
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) vb[e] = o[e];
+    }
+    float a = 0.f, od = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        a = fmaf(g[e], vb[e], a);
+        od = fmaf(g[e], o[e], od);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, off);
+        od += __shfl_xor_sync(0xffffffffu, od, off);
+    }
+    if (lane == 0) {
+        const float ci = p.c ? p.c[row] : 0.f;
+        p.stats[row] = make_float4(p.lse[row] * 1.4426950408889634f, ci, a, fmaf(ci, a, od));
+    }
+}
+
 }  // namespace plx

@@ -89,7 +89,9 @@ struct FwdTcCfg {
     // (l, C) per item [2 item parities][2 halves][BM] float2
     static constexpr int OFF_XMAX = OFF_STG + SM_WARPS * STG_SLOT_BYTES;
     static constexpr int OFF_XLC = OFF_XMAX + 2 * 2 * BM * 4;
-    static constexpr int OFF_BAR = OFF_XLC + 2 * 2 * BM * 8;
+    // the training forward's fp32 (l, C) of the unrounded terms, the same shape
+    static constexpr int OFF_XLC32 = OFF_XLC + 2 * 2 * BM * 8;
+    static constexpr int OFF_BAR = OFF_XLC32 + 2 * 2 * BM * 8;
     // barriers: q_full, q_empty, k_full[KSTAGE], k_empty[KSTAGE], v_full[NSTAGE], v_empty[NSTAGE],
     // v_ready[NSTAGE], s_full[2], p_full[2], pv_done[2], drain, pair[4]
     static constexpr int NBARS = 2 + 2 * KSTAGE + 3 * NSTAGE + 2 + 2 + 2 + 1 + 4;
@@ -120,6 +122,7 @@ struct FwdTcParams {
     float scale_log2;
     int out_f32;
     int no_intercept;      // the family's no-intercept member: o = -u
+    float* c_out;          // the training forward: c_i per row, [BH][Tq] (else unused)
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -170,12 +173,17 @@ __device__ __forceinline__ int snake_item(int r, int c, int G) {
     return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
-template <int D, bool PLX, bool CACHED = false>
+// TRAIN: the training forward, which also writes vbar_i = O_i / l_i (fp32,
+// through mapVb, the same layout as an fp32 o) and c_i (p.c_out), the values
+// the backward's row statistics are formed from.
+template <int D, bool PLX, bool CACHED = false, bool TRAIN = false>
 __global__ void __launch_bounds__(FwdTcCfg<D, PLX>::THREADS, 1)
 plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapR,
                   const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
-                  const __grid_constant__ CUtensorMap mapO, const FwdTcParams p) {
+                  const __grid_constant__ CUtensorMap mapO, const __grid_constant__ CUtensorMap mapVb,
+                  const FwdTcParams p) {
     using Cfg = FwdTcCfg<D, PLX>;
+    static_assert(!TRAIN || (PLX && !CACHED), "the training forward is the PLX prefill");
     constexpr int BM = Cfg::BM, BN = Cfg::BN, NP = Cfg::NP, NSTAGE = Cfg::NSTAGE, KSTAGE = Cfg::KSTAGE,
                   HALF = Cfg::HALF;
     extern __shared__ uint8_t smem_raw[];
@@ -186,6 +194,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
     uint8_t* sV = smem + Cfg::OFF_V;
     float* xmax = reinterpret_cast<float*>(smem + Cfg::OFF_XMAX);
     float2* xlc = reinterpret_cast<float2*>(smem + Cfg::OFF_XLC);
+    float2* xlc32 = reinterpret_cast<float2*>(smem + Cfg::OFF_XLC32);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     uint64_t* q_full = bars;
     uint64_t* q_empty = bars + 1;
@@ -235,6 +244,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         tma_prefetch_desc(&mapV);
         tma_prefetch_desc(&mapO);
         if (PLX) tma_prefetch_desc(&mapR);
+        if (TRAIN) tma_prefetch_desc(&mapVb);
     }
     tc_fence_before();
     __syncthreads();
@@ -402,7 +412,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
         // r in the tensor map's swizzle (16-byte unit u of row r at u ^ (r & 7)
         // for 128-byte fp32 rows, u ^ ((r >> 1) & 3) for 64-byte bf16 rows), so
         // the eight rows of a quarter-warp hit eight different bank groups.
-        auto epilogue = [&](int eu, int eg, float em, const float2* xe) -> bool {
+        auto epilogue = [&](int eu, int eg, float em, const float2* xe, const float2* xe32) -> bool {
             if (!wait_warp(&pv_done[eg & 1], (eg >> 1) & 1)) return false;
             tc_fence_after();
             int ebh, eqt;
@@ -415,6 +425,15 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             const float l_all = e0.x + e1.x, C_all = e0.y + e1.y;
             const float inv_l = 1.f / l_all;
             const float cc_ = C_all * inv_l;
+            // the training forward's c_i: the same weights summed in fp32 before
+            // the fp16 rounding of P and P o R.  (o uses the rounded sums, whose
+            // rounding cancels against U's; c on its own feeds the backward's
+            // 1 + c_i - r_ij, where it would not.)
+            float c32 = 0.f;
+            if constexpr (TRAIN) {
+                const float2 f0 = xe32[row], f1 = xe32[BM + row];
+                c32 = (f0.y + f1.y) / (f0.x + f1.x);
+            }
             // 0 * o is NaN exactly when o is not finite: one running sum flags them all
             float bad = 0.f;
 #pragma unroll 1
@@ -471,11 +490,31 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                     tma_store_3d(&mapO, stg, col, eq0 + quad * 32, ebh);
                     bulk_commit_group();
                 }
+                if constexpr (TRAIN) {
+                    // vbar of the same block, fp32, through the same slot once o's
+                    // store has read it
+                    if (lane == 0) bulk_wait_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int u4 = 0; u4 < 8; ++u4)
+                        *reinterpret_cast<uint4*>(stg + lane * 128 + ((u4 ^ (lane & 7)) << 4)) =
+                            make_uint4(__float_as_uint(__uint_as_float(ov[4 * u4]) * inv_l),
+                                       __float_as_uint(__uint_as_float(ov[4 * u4 + 1]) * inv_l),
+                                       __float_as_uint(__uint_as_float(ov[4 * u4 + 2]) * inv_l),
+                                       __float_as_uint(__uint_as_float(ov[4 * u4 + 3]) * inv_l));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&mapVb, stg, col, eq0 + quad * 32, ebh);
+                        bulk_commit_group();
+                    }
+                }
             }
             const int ei = eq0 + row;
             const bool store = ei < p.Tq;
             if (store && half == 0 && p.lse && in_bounds(ebh < p.BH))
                 p.lse[static_cast<size_t>(ebh) * p.Tq + ei] = (em + __log2f(l_all)) * 0.69314718055994531f;
+            if (TRAIN && store && half == 0 && in_bounds(ebh < p.BH)) p.c_out[static_cast<size_t>(ebh) * p.Tq + ei] = c32;
             if (__any_sync(0xffffffffu, store && !(bad == 0.f)) && lane == 0)
                 atomicOr(&g_plx_status, PLX_DEV_ERR_NONFINITE);
             return true;
@@ -489,6 +528,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             const int i = q0 + row;                 // this thread's query row
             const int pos = it.off + i;             // its position: keys 0 .. pos
             float m = -INFINITY, l = 0.f, C = 0.f;
+            float2 l32 = make_float2(0.f, 0.f), C32 = make_float2(0.f, 0.f);   // training forward only
             // cached mode: a quadrant none of whose 32 rows is a query row (T < 128)
             // stores nothing; its two warps only keep the barrier phases in step,
             // and the garbage left in its lanes stays in its own rows
@@ -568,6 +608,10 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                         m = m_new;
                         l *= alpha;
                         C *= alpha;
+                        if constexpr (TRAIN) {
+                            l32 = fmul2(l32, make_float2(alpha, alpha));
+                            C32 = fmul2(C32, make_float2(alpha, alpha));
+                        }
                     }
                 }
                 // P = 2^(scale S - m) <= 2^4: every score of the tile is within 2^4 of m
@@ -589,6 +633,10 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                     ls[cc & 3] = add_f16x2(ls[cc & 3], pk[cc]);
                 }
                 l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                if constexpr (TRAIN) {
+#pragma unroll
+                    for (int cc = 0; cc < HALF; cc += 2) l32 = fadd2(l32, make_float2(pe[cc], pe[cc + 1]));
+                }
                 tmem_st32x32b_x16(tS + half * HALF, pk);
                 if constexpr (PLX) {
                     tmem_ld_wait(rraw);
@@ -607,6 +655,7 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
                                                            __uint_as_float(rraw[2 * cc + 1])));
                         pk[cc] = pack_f16x2(a.x, a.y);
                         cs[cc & 3] = add_f16x2(cs[cc & 3], pk[cc]);
+                        if constexpr (TRAIN) C32 = fadd2(C32, a);
                     }
                     C += (cs[0] + cs[1]) + (cs[2] + cs[3]);
                     tmem_st32x32b_x16(tR + half * HALF, pk);
@@ -646,9 +695,11 @@ plx_fwd_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constan
             // of that item and so comes after the epilogue.
             if (!idle) {
                 float2* xe = xlc + ((items & 1) * 2) * BM;
+                float2* xe32 = xlc32 + ((items & 1) * 2) * BM;
                 xe[half * BM + row] = make_float2(l, C);
+                if constexpr (TRAIN) xe32[half * BM + row] = make_float2(l32.x + l32.y, C32.x + C32.y);
                 pair_arrive();
-                if (!pair_wait() || !epilogue(u, g - 1, m, xe)) { ok = false; break; }
+                if (!pair_wait() || !epilogue(u, g - 1, m, xe, xe32)) { ok = false; break; }
             }
             ++items;
         }

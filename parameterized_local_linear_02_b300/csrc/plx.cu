@@ -75,6 +75,8 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, false, true>, FwdTcCfg<128, false>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, true, true>, FwdTcCfg<64, true>::SMEM);
     e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, false, true>, FwdTcCfg<64, false>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<128, true, false, true>, FwdTcCfg<128, true>::SMEM);
+    e = e ? e : set_smem(plx::plx_fwd_tc_kernel<64, true, false, true>, FwdTcCfg<64, true>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, true, plx::BWD_STATS>, BwdTcCfg<128, true, plx::BWD_STATS>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<128, false, plx::BWD_STATS>, BwdTcCfg<128, false, plx::BWD_STATS>::SMEM);
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, true, plx::BWD_STATS>, BwdTcCfg<64, true, plx::BWD_STATS>::SMEM);
@@ -206,20 +208,29 @@ struct CachedQueries {
 };
 
 // The tcgen05 forward: the self-attention prefill, or the cached mode.
+// vbar != nullptr: the training forward, which also writes vbar (fp32, the layout of an fp32 o) and
+// c (fp32 per row); PLX self-attention prefill only.
 template <int D, bool PLX>
 plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
                          int N, long long BH, float scale, plx_dtype out_dtype, cudaStream_t stream,
-                         int sm_count, bool no_intercept = false, const CachedQueries& cq = CachedQueries()) {
+                         int sm_count, bool no_intercept = false, const CachedQueries& cq = CachedQueries(),
+                         float* vbar = nullptr, float* c_out = nullptr) {
     using Cfg = FwdTcCfg<D, PLX>;
     const int Tq = cq.Tq > 0 ? cq.Tq : N;
     const long long n_qt = (Tq + Cfg::BM - 1) / Cfg::BM;
     const long long n_items = BH * n_qt;
     if (n_items > INT_MAX || BH > INT_MAX) return PLX_ERR_UNSUPPORTED;
-    CUtensorMap mq, mr, mk, mv, mo;
+    CUtensorMap mq, mr, mk, mv, mo, mvb;
     if (!make_map(&mq, q, D, Tq, BH, Cfg::BM) || !make_map(&mk, k, D, N, BH, Cfg::BN) ||
         !make_map(&mv, v, D, N, BH, Cfg::BN))
         return PLX_ERR_CUDA;
     if (!make_out_map(&mo, out, D, Tq, BH, out_dtype == PLX_F32)) return PLX_ERR_CUDA;
+    const bool train = PLX && vbar != nullptr && !cq.seqlens;
+    if (train) {
+        if (!make_out_map(&mvb, vbar, D, Tq, BH, true)) return PLX_ERR_CUDA;
+    } else {
+        mvb = mo;
+    }
     if (PLX) {
         if (!make_map(&mr, rho, D, Tq, BH, Cfg::BM)) return PLX_ERR_CUDA;
     } else {
@@ -237,11 +248,17 @@ plx_status launch_fwd_tc(const void* q, const void* k, const void* v, const void
     p.scale_log2 = scale * kLog2e;
     p.out_f32 = out_dtype == PLX_F32;
     p.no_intercept = no_intercept ? 1 : 0;
+    p.c_out = train ? c_out : nullptr;
     const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
-    if (cq.seqlens)
-        plx::plx_fwd_tc_kernel<D, PLX, true><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
-    else
-        plx::plx_fwd_tc_kernel<D, PLX, false><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, p);
+    if (cq.seqlens) {
+        plx::plx_fwd_tc_kernel<D, PLX, true><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, mvb, p);
+    } else if (train) {
+        if constexpr (PLX)
+            plx::plx_fwd_tc_kernel<D, PLX, false, true><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv,
+                                                                                                    mo, mvb, p);
+    } else {
+        plx::plx_fwd_tc_kernel<D, PLX, false><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mr, mk, mv, mo, mvb, p);
+    }
     return launch_status();
 }
 
@@ -298,10 +315,12 @@ size_t bwd_bf16_ws_bytes(long long BH, int N) { return align256(static_cast<size
 
 // plx_bwd on the tensor cores: the pre-pass (the forward in statistics mode),
 // the dq pass and the dkv pass.
+// prep == nullptr: the statistics pass computes the row statistics; otherwise
+// plx_bwd_prep_kernel forms them from the training forward's saved values.
 template <int D, bool PLX>
 plx_status launch_bwd_tc(const void* q, const void* k, const void* v, const void* rho, const void* dout, float* dq,
                          float* dk, float* dv, float* drho, void* workspace, int N, long long BH, float scale,
-                         cudaStream_t s, int sm_count) {
+                         cudaStream_t s, int sm_count, const plx::BwdPrepParams* prep = nullptr) {
     using CfgS = BwdTcCfg<D, PLX, plx::BWD_STATS>;
     using CfgQ = BwdTcCfg<D, PLX, plx::BWD_DQ>;
     using CfgK = BwdTcCfg<D, PLX, plx::BWD_DKV>;
@@ -337,9 +356,19 @@ plx_status launch_bwd_tc(const void* q, const void* k, const void* v, const void
         m_dr = m_dq;
     }
     // unused slots get a valid map of the right kind
-    // the row statistics (lse, c, a, D) with the weights the two gradient passes use
-    plx::plx_bwd_tc_kernel<D, PLX, plx::BWD_STATS><<<grid, CfgS::THREADS, CfgS::SMEM, s>>>(
-        mq_r, PLX ? mr_r : mo_r, mo_r, mk_s, mv_s, mv_s, mstat, m_dq, m_dr, p);
+    if (prep) {
+        // the row statistics from the forward's lse, c, vbar and o
+        plx::BwdPrepParams pp = *prep;
+        pp.stats = stats;
+        pp.rows = BH * N;
+        const long long blocks = (pp.rows + plx::BWD_PREP_ROWS_PER_BLOCK - 1) / plx::BWD_PREP_ROWS_PER_BLOCK;
+        if (blocks > INT_MAX) return PLX_ERR_UNSUPPORTED;
+        plx::plx_bwd_prep_kernel<D><<<static_cast<unsigned>(blocks), plx::BWD_PREP_ROWS_PER_BLOCK * 32, 0, s>>>(pp);
+    } else {
+        // the row statistics (lse, c, a, D) with the weights the two gradient passes use
+        plx::plx_bwd_tc_kernel<D, PLX, plx::BWD_STATS><<<grid, CfgS::THREADS, CfgS::SMEM, s>>>(
+            mq_r, PLX ? mr_r : mo_r, mo_r, mk_s, mv_s, mv_s, mstat, m_dq, m_dr, p);
+    }
     if (cudaGetLastError() != cudaSuccess) return PLX_ERR_CUDA;
     plx::plx_bwd_tc_kernel<D, PLX, plx::BWD_DQ><<<grid, CfgQ::THREADS, CfgQ::SMEM, s>>>(
         mq_r, PLX ? mr_r : mo_r, mo_r, mk_s, mv_s, mv_s, mstat, m_dq, m_dr, p);
@@ -810,6 +839,74 @@ plx_status plx_bwd(const void* q, const void* k, const void* v, const void* rho,
                                              info->sm_count)
                    : launch_bwd_tc<64, false>(q, k, v, rho, dout, dq, dk, dv, drho, workspace, N, BH, scale, s,
                                               info->sm_count);
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+plx_status plx_fwd_train(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
+                         float* vbar, float* c, int B, int H, int N, int d, float scale, plx_dtype out_dtype,
+                         void* stream) {
+    try {
+        if (!q || !k || !v || !rho || !out || !lse || !vbar || !c) return PLX_ERR_INVALID_ARG;
+        if (B < 1 || H < 1 || N < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
+        if (out_dtype != PLX_BF16 && out_dtype != PLX_F32) return PLX_ERR_INVALID_ARG;
+        if (d != 128 && d != 64) return PLX_ERR_UNSUPPORTED;
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(rho, 16) || !aligned(out, 16) ||
+            !aligned(vbar, 16) || !aligned(lse, 4) || !aligned(c, 4))
+            return PLX_ERR_MISALIGNED;
+        const DeviceInfo* info = device_info();
+        if (!info) return PLX_ERR_CUDA;
+        const long long BH = static_cast<long long>(B) * H;
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        if (d == 128)
+            return launch_fwd_tc<128, true>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count,
+                                            false, CachedQueries(), vbar, c);
+        return launch_fwd_tc<64, true>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count, false,
+                                       CachedQueries(), vbar, c);
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+plx_status plx_bwd_saved(const void* q, const void* k, const void* v, const void* rho, const void* dout,
+                         const void* out, plx_dtype out_dtype, const float* lse, const float* vbar, const float* c,
+                         float* dq, float* dk, float* dv, float* drho, void* workspace, size_t workspace_bytes, int B,
+                         int H, int N, int d, float scale, void* stream) {
+    try {
+        if (!q || !k || !v || !dout || !out || !lse || !dq || !dk || !dv) return PLX_ERR_INVALID_ARG;
+        if (rho && (!drho || !vbar || !c)) return PLX_ERR_INVALID_ARG;
+        if (B < 1 || H < 1 || N < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
+        if (out_dtype != PLX_BF16 && out_dtype != PLX_F32) return PLX_ERR_INVALID_ARG;
+        if (d != 128 && d != 64) return PLX_ERR_UNSUPPORTED;
+        const void* ptrs16[] = {q, k, v, dout, out, dq, dk, dv, workspace};
+        for (const void* ptr : ptrs16)
+            if (ptr && !aligned(ptr, 16)) return PLX_ERR_MISALIGNED;
+        if (rho && (!aligned(rho, 16) || !aligned(drho, 16) || !aligned(vbar, 16) || !aligned(c, 4)))
+            return PLX_ERR_MISALIGNED;
+        if (!aligned(lse, 4)) return PLX_ERR_MISALIGNED;
+        const size_t need = plx_bwd_bf16_workspace_size(B, H, N, d);
+        if (!workspace || workspace_bytes < need) return PLX_ERR_WORKSPACE;
+        const DeviceInfo* info = device_info();
+        if (!info) return PLX_ERR_CUDA;
+        const long long BH = static_cast<long long>(B) * H;
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        plx::BwdPrepParams pp{};
+        pp.lse = lse;
+        pp.c = rho ? c : nullptr;
+        pp.vbar = rho ? vbar : nullptr;
+        pp.out = out;
+        pp.dout = static_cast<const uint16_t*>(dout);
+        pp.out_f32 = out_dtype == PLX_F32;
+        if (d == 128)
+            return rho ? launch_bwd_tc<128, true>(q, k, v, rho, dout, dq, dk, dv, drho, workspace, N, BH, scale, s,
+                                                  info->sm_count, &pp)
+                       : launch_bwd_tc<128, false>(q, k, v, rho, dout, dq, dk, dv, drho, workspace, N, BH, scale, s,
+                                                   info->sm_count, &pp);
+        return rho ? launch_bwd_tc<64, true>(q, k, v, rho, dout, dq, dk, dv, drho, workspace, N, BH, scale, s,
+                                             info->sm_count, &pp)
+                   : launch_bwd_tc<64, false>(q, k, v, rho, dout, dq, dk, dv, drho, workspace, N, BH, scale, s,
+                                              info->sm_count, &pp);
     } catch (...) {
         return PLX_ERR_CUDA;
     }

@@ -282,3 +282,31 @@ def test_no_cpu_fallback_without_a_device():
     for call in calls:
         with pytest.raises((RuntimeError, plx.PlxError)):
             call()
+
+
+def test_fwd_train_and_bwd_saved_reject_bad_arguments_before_launch():
+    lib = plx.library()
+    f = lib.plx_fwd_train
+    # q, k, v, rho, out, lse, vbar, c, B, H, N, d, scale, out_dtype, stream
+    assert f(P16, P16, P16, None, P16, P16, P16, P16, 1, 1, 8, 128, 0.1, 1, None) == 1   # rho required
+    assert f(P16, P16, P16, P16, P16, None, P16, P16, 1, 1, 8, 128, 0.1, 1, None) == 1   # lse required
+    assert f(P16, P16, P16, P16, P16, P16, None, P16, 1, 1, 8, 128, 0.1, 1, None) == 1   # vbar required
+    assert f(P16, P16, P16, P16, P16, P16, P16, None, 1, 1, 8, 128, 0.1, 1, None) == 1   # c required
+    assert f(P16, P16, P16, P16, P16, P16, P16, P16, 1, 1, 0, 128, 0.1, 1, None) == 1
+    assert f(P16, P16, P16, P16, P16, P16, P16, P16, 1, 1, 8, 128, 0.1, 9, None) == 1
+    assert f(P16, P16, P16, P16, P16, P16, P16, P16, 1, 1, 8, 96, 0.1, 1, None) == 2
+    assert f(P16, P16, P16, P16, P16, P16, P_ODD, P16, 1, 1, 8, 128, 0.1, 1, None) == 3
+    g = lib.plx_bwd_saved
+    ws = plx.plx_bwd_bf16_workspace_size(1, 1, 8, 128)
+    # q, k, v, rho, dout, out, out_dtype, lse, vbar, c, dq, dk, dv, drho, ws, ws_bytes, B, H, N, d, scale, stream
+    ok = [P16] * 6 + [1] + [P16] * 8 + [ws, 1, 1, 8, 128, 0.1, None]
+    bad = list(ok); bad[8] = None                           # vbar missing while rho is given
+    assert g(*bad) == 1
+    bad = list(ok); bad[6] = 5                              # unknown out dtype
+    assert g(*bad) == 1
+    bad = list(ok); bad[19] = 96                            # head dim without a kernel
+    assert g(*bad) == 2
+    bad = list(ok); bad[5] = P_ODD                          # misaligned out
+    assert g(*bad) == 3
+    bad = list(ok); bad[15] = ws - 1                        # workspace too small
+    assert g(*bad) == 6
