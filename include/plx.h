@@ -222,6 +222,39 @@ plx_status plx_bwd(const void* q, const void* k, const void* v, const void* rho,
 size_t plx_bwd_bf16_workspace_size(int B, int H, int N, int d);
 
 /*
+ * plx_fwd_host -- plx_fwd on HOST buffers (the paper has no counterpart: this
+ * is the transfer path around the forward of "Parallax: Parameterized Local
+ * Linear Attention for Language Modeling", gist.science, "Algoritmo
+ * Consapevole dell'Hardware").  q, k, v, rho, out and lse live in host memory
+ * (page-locked, for the copies to run asynchronously and to overlap; pageable
+ * memory works, with the copies staged by the driver).  The heads go through
+ * the device workspace in up to 16 chunks: while chunk c is computed, chunk
+ * c + 1 is copied in and chunk c - 1 copied out, on the GPU's copy engines
+ * (two streams of the library, one cudaMemcpyAsync per array and chunk).  The
+ * results are those of plx_fwd on the same values, bit for bit.
+ *
+ *   q, k, v, rho : host bf16 [B][H][N][d]; rho may be NULL (softmax attention).
+ *   out          : host [B][H][N][d], fp32 or bf16 as out_dtype.
+ *   lse          : host fp32 [B][H][N], or NULL.
+ *   workspace    : device scratch of plx_fwd_host_workspace_size(B, H, N, d,
+ *                  out_dtype) bytes, 256-byte aligned, no initialisation.
+ *   B, H, N >= 1; d in {64, 128}; scale finite and >= 0.
+ * Asynchronous: the copies start after the work already on `stream`, the
+ * kernels run on `stream`, and `stream` waits for the last copy back, so a
+ * synchronisation of `stream` returns with out and lse in host memory.  Calls
+ * that share a workspace must be ordered (the same stream orders them).  The
+ * host buffers must stay valid, and out/lse unread, until then.
+ * Errors: PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_MISALIGNED (the
+ * workspace), PLX_ERR_WORKSPACE, PLX_ERR_CUDA.
+ */
+plx_status plx_fwd_host(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale,
+                        plx_dtype out_dtype, void* stream);
+
+/* Workspace bytes plx_fwd_host needs (0 for invalid sizes). */
+size_t plx_fwd_host_workspace_size(int B, int H, int N, int d, plx_dtype out_dtype);
+
+/*
  * plx_fwd_train -- plx_fwd for training: the same o and lse (bit for bit), and
  * also vbar_i = sum_j w_ij v_j (the softmax-attention output o_i^SA of the
  * same weights) and c_i = sum_j w_ij (rho_i.k_j), the two per-row values the

@@ -85,6 +85,10 @@ def load(path: str) -> ctypes.CDLL:
     lib.plx_bwd.argtypes = [vp] * 10 + [sz, i, i, i, i, f, vp]
     lib.plx_bwd_bf16_workspace_size.restype = sz
     lib.plx_bwd_bf16_workspace_size.argtypes = [i, i, i, i]
+    lib.plx_fwd_host.restype = i
+    lib.plx_fwd_host.argtypes = [vp] * 7 + [sz, i, i, i, i, f, i, vp]
+    lib.plx_fwd_host_workspace_size.restype = sz
+    lib.plx_fwd_host_workspace_size.argtypes = [i, i, i, i, i]
     lib.plx_fwd_train.restype = i
     lib.plx_fwd_train.argtypes = [vp] * 8 + [i, i, i, i, f, i, vp]
     lib.plx_bwd_saved.restype = i
@@ -310,6 +314,39 @@ def plx_bwd(q, k, v, rho, dout, *, scale=None, workspace=None, grads=None):
                            _ptr(drho), _ptr(workspace), ws_bytes, B, H, N, d, scale, _stream(dev))
     _check(st, "plx_bwd")
     return dq, dk, dv, drho
+
+
+def plx_fwd_host_workspace_size(B: int, H: int, N: int, d: int, out_dtype=torch.float32) -> int:
+    return library().plx_fwd_host_workspace_size(B, H, N, d, _out_code(out_dtype))
+
+
+def plx_fwd_host(q, k, v, rho, out, lse=None, *, workspace, scale=None, stream=None):
+    """plx_fwd on host tensors (page-locked for overlap): ``q``, ``k``, ``v``,
+    ``rho`` bf16 [B, H, N, d] and ``out`` (fp32 or bf16) / ``lse`` (fp32
+    [B, H, N] or None) on the CPU; ``workspace`` a CUDA uint8 tensor of
+    plx_fwd_host_workspace_size bytes.  Asynchronous on ``stream`` (default:
+    the current stream of the workspace's device): synchronize it before
+    reading out and lse."""
+    B, H, N, d = q.shape
+    cpu = torch.device("cpu")
+    for name, t in (("q", q), ("k", k), ("v", v)) + ((("rho", rho),) if rho is not None else ()):
+        _need(t, name, torch.bfloat16, (B, H, N, d), cpu)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be float32 or bfloat16")
+    _need(out, "out", out.dtype, (B, H, N, d), cpu)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, N), cpu)
+    if not isinstance(workspace, torch.Tensor) or workspace.device.type != "cuda":
+        raise ValueError("workspace must be a CUDA tensor")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st_ = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(workspace.device):
+        st = library().plx_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(out), _ptr(lse), _ptr(workspace),
+                                    ws_bytes, B, H, N, d, scale, _out_code(out.dtype),
+                                    ctypes.c_void_p(st_.cuda_stream))
+    _check(st, "plx_fwd_host")
+    return out, lse
 
 
 def plx_fwd_train(q, k, v, rho, *, scale=None, out=None, lse=None, vbar=None, c=None, out_dtype=torch.float32):

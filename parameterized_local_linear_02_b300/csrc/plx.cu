@@ -639,6 +639,66 @@ float* noalloc_scratch() {
     return g_noalloc_scratch[dev];
 }
 
+// plx_fwd_host: host buffers streamed through a device workspace in chunks of
+// heads.  kHostBuffers chunks are in flight at once (one being copied in, one
+// computed, one copied out), each in its own slice of the workspace.
+constexpr int kHostBuffers = 3;
+constexpr int kHostChunks = 16;          // chunks per call (fewer when B H is smaller)
+
+// The copy streams and the events of the pipeline, one set per device and
+// CUDA context (cudaDeviceReset gives the device a new context, in which the
+// old handles are gone; they are created again, not destroyed).
+struct HostPipe {
+    unsigned long long ctx = 0;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t loaded[kHostBuffers] = {}, computed[kHostBuffers] = {}, stored[kHostBuffers] = {};
+    std::mutex m;                         // one call's enqueue sequence at a time
+};
+HostPipe g_pipe[kMaxDevices];
+
+// The pipeline of the current device with its lock held, or nullptr on a CUDA error.
+HostPipe* host_pipe(std::unique_lock<std::mutex>& lock) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    HostPipe& hp = g_pipe[dev];
+    lock = std::unique_lock<std::mutex>(hp.m);
+    const unsigned long long ctx = current_context_id();
+    if (hp.h2d && ctx != 0 && ctx == hp.ctx) return &hp;
+    bool ok = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming) == cudaSuccess;
+    for (int b = 0; ok && b < kHostBuffers; ++b)
+        ok = cudaEventCreateWithFlags(&hp.loaded[b], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&hp.computed[b], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&hp.stored[b], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        hp.h2d = nullptr;
+        return nullptr;
+    }
+    hp.ctx = current_context_id();
+    return &hp;
+}
+
+// Heads per chunk and the bytes of one chunk's slice of the workspace.
+struct HostChunking {
+    long long heads_per_chunk = 0, chunks = 0;
+    size_t in_bytes = 0, out_bytes = 0, lse_bytes = 0, slice_bytes = 0;
+};
+HostChunking host_chunking(long long BH, int N, int d, bool out_f32) {
+    HostChunking hc;
+    const long long want = BH < kHostChunks ? BH : kHostChunks;
+    hc.heads_per_chunk = (BH + want - 1) / want;
+    hc.chunks = (BH + hc.heads_per_chunk - 1) / hc.heads_per_chunk;
+    const size_t rows = static_cast<size_t>(hc.heads_per_chunk) * N;
+    hc.in_bytes = align256(rows * d * 2);
+    hc.out_bytes = align256(rows * d * (out_f32 ? 4 : 2));
+    hc.lse_bytes = align256(rows * 4);
+    hc.slice_bytes = 4 * hc.in_bytes + hc.out_bytes + hc.lse_bytes;
+    return hc;
+}
+
 // One bounded wait on a fresh barrier (the diagnostic behind
 // plx_selftest_wait): a wait that gives up records PLX_DEV_ERR_TIMEOUT.
 __global__ void plx_wait_selftest_kernel(unsigned long long limit_ns, int arrive) {
@@ -864,6 +924,91 @@ plx_status plx_fwd_train(const void* q, const void* k, const void* v, const void
                                             false, CachedQueries(), vbar, c);
         return launch_fwd_tc<64, true>(q, k, v, rho, out, lse, N, BH, scale, out_dtype, s, info->sm_count, false,
                                        CachedQueries(), vbar, c);
+    } catch (...) {
+        return PLX_ERR_CUDA;
+    }
+}
+
+size_t plx_fwd_host_workspace_size(int B, int H, int N, int d, plx_dtype out_dtype) {
+    if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || (out_dtype != PLX_BF16 && out_dtype != PLX_F32)) return 0;
+    const HostChunking hc = host_chunking(static_cast<long long>(B) * H, N, d, out_dtype == PLX_F32);
+    return kHostBuffers * hc.slice_bytes;
+}
+
+plx_status plx_fwd_host(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale,
+                        plx_dtype out_dtype, void* stream) {
+    try {
+        if (!q || !k || !v || !out) return PLX_ERR_INVALID_ARG;
+        if (B < 1 || H < 1 || N < 1 || !valid_scale(scale)) return PLX_ERR_INVALID_ARG;
+        if (out_dtype != PLX_BF16 && out_dtype != PLX_F32) return PLX_ERR_INVALID_ARG;
+        if (d != 128 && d != 64) return PLX_ERR_UNSUPPORTED;
+        if (!workspace || !aligned(workspace, 256)) return workspace ? PLX_ERR_MISALIGNED : PLX_ERR_WORKSPACE;
+        const size_t need = plx_fwd_host_workspace_size(B, H, N, d, out_dtype);
+        if (need == 0 || workspace_bytes < need) return PLX_ERR_WORKSPACE;
+        const DeviceInfo* info = device_info();
+        if (!info) return PLX_ERR_CUDA;
+        const long long BH = static_cast<long long>(B) * H;
+        const bool f32 = out_dtype == PLX_F32;
+        const HostChunking hc = host_chunking(BH, N, d, f32);
+        const size_t head_in = static_cast<size_t>(N) * d * 2, head_out = static_cast<size_t>(N) * d * (f32 ? 4 : 2);
+        const size_t head_lse = static_cast<size_t>(N) * 4;
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        std::unique_lock<std::mutex> lock;
+        HostPipe* hp = host_pipe(lock);
+        if (!hp) return PLX_ERR_CUDA;
+        auto ck = [](cudaError_t e) { return e == cudaSuccess; };
+        // the copies start after the caller's earlier work on `stream`
+        if (!ck(cudaEventRecord(hp->start, s)) || !ck(cudaStreamWaitEvent(hp->h2d, hp->start, 0)) ||
+            !ck(cudaStreamWaitEvent(hp->d2h, hp->start, 0)))
+            return PLX_ERR_CUDA;
+        const char* in_h[4] = {static_cast<const char*>(q), static_cast<const char*>(k), static_cast<const char*>(v),
+                               static_cast<const char*>(rho)};
+        for (long long c = 0; c < hc.chunks; ++c) {
+            const int b = static_cast<int>(c % kHostBuffers);
+            const long long h0 = c * hc.heads_per_chunk;
+            const long long g = (BH - h0) < hc.heads_per_chunk ? (BH - h0) : hc.heads_per_chunk;
+            char* slice = static_cast<char*>(workspace) + b * hc.slice_bytes;
+            char* in_d[4] = {slice, slice + hc.in_bytes, slice + 2 * hc.in_bytes, slice + 3 * hc.in_bytes};
+            char* out_d = slice + 4 * hc.in_bytes;
+            float* lse_d = reinterpret_cast<float*>(out_d + hc.out_bytes);
+            // a slice is reused once its previous chunk has been copied out
+            if (c >= kHostBuffers && !ck(cudaStreamWaitEvent(hp->h2d, hp->stored[b], 0))) return PLX_ERR_CUDA;
+            for (int a = 0; a < 4; ++a) {
+                if (!in_h[a]) continue;
+                if (!ck(cudaMemcpyAsync(in_d[a], in_h[a] + h0 * head_in, g * head_in, cudaMemcpyHostToDevice,
+                                        hp->h2d)))
+                    return PLX_ERR_CUDA;
+            }
+            if (!ck(cudaEventRecord(hp->loaded[b], hp->h2d)) || !ck(cudaStreamWaitEvent(s, hp->loaded[b], 0)))
+                return PLX_ERR_CUDA;
+            const void* r_d = rho ? in_d[3] : nullptr;
+            float* l_d = lse ? lse_d : nullptr;
+            plx_status st;
+            if (d == 128)
+                st = rho ? launch_fwd_tc<128, true>(in_d[0], in_d[1], in_d[2], r_d, out_d, l_d, N, g, scale, out_dtype,
+                                                    s, info->sm_count)
+                         : launch_fwd_tc<128, false>(in_d[0], in_d[1], in_d[2], r_d, out_d, l_d, N, g, scale,
+                                                     out_dtype, s, info->sm_count);
+            else
+                st = rho ? launch_fwd_tc<64, true>(in_d[0], in_d[1], in_d[2], r_d, out_d, l_d, N, g, scale, out_dtype,
+                                                   s, info->sm_count)
+                         : launch_fwd_tc<64, false>(in_d[0], in_d[1], in_d[2], r_d, out_d, l_d, N, g, scale, out_dtype,
+                                                    s, info->sm_count);
+            if (st != PLX_OK) return st;
+            if (!ck(cudaEventRecord(hp->computed[b], s)) || !ck(cudaStreamWaitEvent(hp->d2h, hp->computed[b], 0)))
+                return PLX_ERR_CUDA;
+            if (!ck(cudaMemcpyAsync(static_cast<char*>(out) + h0 * head_out, out_d, g * head_out,
+                                    cudaMemcpyDeviceToHost, hp->d2h)))
+                return PLX_ERR_CUDA;
+            if (lse && !ck(cudaMemcpyAsync(reinterpret_cast<char*>(lse) + h0 * head_lse, lse_d, g * head_lse,
+                                           cudaMemcpyDeviceToHost, hp->d2h)))
+                return PLX_ERR_CUDA;
+            if (!ck(cudaEventRecord(hp->stored[b], hp->d2h))) return PLX_ERR_CUDA;
+        }
+        // the caller's stream resumes once the last chunk is back in host memory
+        if (!ck(cudaEventRecord(hp->done, hp->d2h)) || !ck(cudaStreamWaitEvent(s, hp->done, 0))) return PLX_ERR_CUDA;
+        return PLX_OK;
     } catch (...) {
         return PLX_ERR_CUDA;
     }

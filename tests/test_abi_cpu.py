@@ -310,3 +310,31 @@ def test_fwd_train_and_bwd_saved_reject_bad_arguments_before_launch():
     assert g(*bad) == 3
     bad = list(ok); bad[15] = ws - 1                        # workspace too small
     assert g(*bad) == 6
+
+
+def test_fwd_host_rejects_bad_arguments_before_launch():
+    lib = plx.library()
+    f = lib.plx_fwd_host
+    ws = plx.plx_fwd_host_workspace_size(1, 2, 64, 128)
+    assert ws > 0
+    assert plx.plx_fwd_host_workspace_size(1, 2, 64, 96) == 0
+    assert plx.plx_fwd_host_workspace_size(0, 2, 64, 128) == 0
+    # more heads than chunks: the workspace holds three chunks of ceil(B H / 16) heads
+    assert plx.plx_fwd_host_workspace_size(4, 16, 2048, 128) < 64 * 2048 * 128 * 12
+    W = ctypes.c_void_p(0x100000)                    # 256-byte aligned fake device address
+    # q, k, v, rho, out, lse, workspace, ws_bytes, B, H, N, d, scale, out_dtype, stream
+    ok = [P16, P16, P16, None, P16, None, W, ws, 1, 2, 64, 128, 0.1, 1, None]
+    bad = list(ok); bad[0] = None
+    assert f(*bad) == 1
+    bad = list(ok); bad[10] = 0
+    assert f(*bad) == 1
+    bad = list(ok); bad[13] = 4
+    assert f(*bad) == 1
+    bad = list(ok); bad[11] = 96
+    assert f(*bad) == 2
+    bad = list(ok); bad[6] = ctypes.c_void_p(0x100010)  # workspace 16- but not 256-byte aligned
+    assert f(*bad) == 3
+    bad = list(ok); bad[6] = None
+    assert f(*bad) == 6
+    bad = list(ok); bad[7] = ws - 1
+    assert f(*bad) == 6
