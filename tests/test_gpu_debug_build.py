@@ -114,3 +114,41 @@ def test_debug_build_lla():
     ref, got = both(lambda: plx.plx_lla_f32(tl["q"], tl["k"], tl["v"], lam=0.1, max_iters=8, tol=1e-6,
                                            scale=x.scale))
     same(ref[:1], got[:1])
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 300, 128), (2, 1, 130, 64)])
+def test_debug_build_training_pair(shape):
+    """plx_fwd_train and plx_bwd_saved under the bounds checks."""
+    import torch
+    import parameterized_local_linear_02_b300 as plx
+    B, H, N, d = shape
+    x = plx_inputs.prefill(B, H, N, d, seed=N + d + 1, dtype="bf16", rho="normal", rho_std=0.3)
+    t = x.device_tensors()
+    dout = torch.randn((B, H, N, d), device="cuda").to(torch.bfloat16)
+
+    def run():
+        o, lse, vbar, c = plx.plx_fwd_train(t["q"], t["k"], t["v"], t["rho"])
+        g = plx.plx_bwd_saved(t["q"], t["k"], t["v"], t["rho"], dout, o, lse, vbar, c)
+        return (o, lse, vbar, c) + tuple(g)
+    ref, got = both(run)
+    same(ref, got)
+
+
+def test_debug_build_host_forward():
+    """plx_fwd_host (chunked copies around the forward) under the bounds checks."""
+    import torch
+    import parameterized_local_linear_02_b300 as plx
+    B, H, N, d = 2, 5, 200, 128
+    x = plx_inputs.prefill(B, H, N, d, seed=97, dtype="bf16", rho="normal", rho_std=0.3)
+    t = x.device_tensors()
+    host = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v", "rho")}
+    ws = torch.empty(plx.plx_fwd_host_workspace_size(B, H, N, d, torch.float32), dtype=torch.uint8, device="cuda")
+
+    def run():
+        out = torch.empty((B, H, N, d)).pin_memory()
+        lse = torch.empty((B, H, N)).pin_memory()
+        plx.plx_fwd_host(host["q"], host["k"], host["v"], host["rho"], out, lse, workspace=ws)
+        torch.cuda.synchronize()
+        return out, lse
+    ref, got = both(run)
+    same(ref, got)
