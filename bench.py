@@ -188,10 +188,11 @@ def rank_seed(seed, rank):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_prefill_sample(cfg, budget_s=12.0, x=None):
+def oracle_prefill_sample(cfg, budget_s=12.0, x=None, per_batch=4):
     """Time the fp64 oracle (streaming form, all host threads) on whole heads
-    of the prefill workload until ``budget_s`` has elapsed or every head is
-    done.  Returns (TFLOP/s, seconds, description, threads)."""
+    of the prefill workload, ``per_batch`` heads at a time, until ``budget_s``
+    has elapsed or every head is done.  Returns (TFLOP/s, seconds,
+    description, threads)."""
     import oracle
     import plx_inputs
     if x is None:
@@ -201,7 +202,7 @@ def oracle_prefill_sample(cfg, budget_s=12.0, x=None):
     done, flops, t0 = 0, 0.0, time.perf_counter()
     threads = oracle.n_threads()
     while done < len(heads) and time.perf_counter() - t0 < budget_s:
-        batch = heads[done:done + 4]
+        batch = heads[done:done + per_batch]
         oracle.prefill("stream", x.q, x.k, x.v, x.rho, x.scale, heads=batch, threads=threads)
         done += len(batch)
         flops += len(batch) * prefill_flops(1, 1, cfg["N"], cfg["d"])
@@ -297,7 +298,9 @@ def run_ours(args, world, rank, local):
         xl = plx_inputs.prefill(Bl, Hl, Nl, dl, seed=rank_seed(lc["seed"], rank), dtype="bf16", rho=lc["rho"],
                                 rho_std=lc["rho_std"], keys=lc["keys"])
         tl = xl.device_tensors(dev)
-        del xl
+        if world > 1 or args.no_cpu_baseline:
+            del xl
+            xl = None
         out_l = torch.empty((Bl, Hl, Nl, dl), dtype=torch.float32, device=dev)
         lse_l = torch.empty((Bl, Hl, Nl), dtype=torch.float32, device=dev)
     if do_dec:
@@ -525,6 +528,11 @@ def run_ours(args, world, rank, local):
         v, dt, desc, threads = oracle_prefill_sample(pc, budget_s=args.cpu_budget, x=x)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                 "sample": desc, "seconds": dt}
+        if do_long and xl is not None:
+            lv, ldt, ldesc, lthreads = oracle_prefill_sample(lc, budget_s=min(6.0, args.cpu_budget), x=xl,
+                                                             per_batch=1)
+            line["cpu_baseline"]["prefill_long"] = {"value": lv, "unit": "TFLOP/s", "cores": lthreads,
+                                                    "kind": "oracle", "sample": ldesc, "seconds": ldt}
         if do_dec:
             gbs, ddt, ddesc, dthreads = oracle_decode_sample(min(5.0, args.cpu_budget))
             line["cpu_baseline"]["decode"] = {"value": gbs, "unit": "GB/s", "cores": dthreads, "kind": "oracle",
