@@ -232,6 +232,21 @@ def oracle_decode_sample(budget_s=5.0):
     return gbs, dt, desc, threads
 
 
+def step_config(do_pf=True, do_long=True, do_dec=True, decode_batch=None):
+    """The workload a bench step times (the same dict on both arms)."""
+    import plx_inputs
+    pc = plx_inputs.CONFIGS[PREFILL]
+    cfg = {"workload": PREFILL if do_pf else (PREFILL_LONG if do_long else DECODE), "B": pc["B"], "H": pc["H"],
+           "N": pc["N"], "d": pc["d"], "causal": True, "rho": "W_R x", "out": "fp32 o + fp32 lse",
+           "l2": "flushed (256 MiB write) before every launch"}
+    if do_long:
+        cfg["long_prefill_workload"] = PREFILL_LONG
+    if do_dec:
+        cfg.update({"decode_workload": DECODE,
+                    "decode_batch": decode_batch or plx_inputs.CONFIGS[DECODE]["B"]})
+    return cfg
+
+
 def run_reference(args, world, rank):
     import plx_inputs
     if rank != 0:
@@ -253,8 +268,8 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * float(np.median(times)), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": PREFILL, "B": cfg["B"], "H": cfg["H"], "N": cfg["N"], "d": cfg["d"],
-                   "causal": True, "rho": "W_R x"},
+        "config": step_config(args.only in ("both", "prefill"), args.only in ("both", "long") and not args.no_long,
+                              args.only in ("both", "decode"), args.decode_batch),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -422,13 +437,7 @@ def run_ours(args, world, rank, local):
             line.update({"value": d_gbs, "unit": "GB/s", "roofline": droof})
     line["ms_per_step"] = ((f_avg if do_pf else 0.0) + (l_avg if do_long else 0.0)
                            + (d_avg if do_dec else 0.0))
-    line["config"] = {"workload": PREFILL if do_pf else (PREFILL_LONG if do_long else DECODE), "B": B, "H": H, "N": N, "d": d, "causal": True,
-                      "rho": "W_R x", "out": "fp32 o + fp32 lse",
-                      "l2": "flushed (256 MiB write) before every launch"}
-    if do_long:
-        line["config"].update({"long_prefill_workload": PREFILL_LONG})
-    if do_dec:
-        line["config"].update({"decode_workload": DECODE, "decode_batch": Bd, "decode_splits": splits})
+    line["config"] = step_config(do_pf, do_long, do_dec, Bd)
 
     if extras and do_pf:
         # the same launches back to back, no L2 flush between them (sustained clocks)
