@@ -721,4 +721,247 @@ __global__ void __launch_bounds__(LLA_WARPS * 32) plx_lla_out_kernel(const LlaPa
     }
 }
 
+// The output pass in the block-GEMM form of the CG step (d = 64, 128): a
+// block owns BM = 64 rows and streams the K and V rows of keys 0 .. i_b + 63
+// in tiles of BK = 32, both through one bulk copy per row into two buffers.
+//   phase 1   [S; R] = [scale q; rho] K^T    (128 stacked rows x 32 keys)
+//             w = exp(s - lse), r' = (rho.k) - (kbar.rho); thread (rg, kg)
+//             writes G1 = w (1 - r') and G2 = w for rows {rg, rg + 32} and
+//             keys {kg + 8 jj} to shared memory and keeps its part of the row
+//             sums L = sum w and C = sum w r';
+//   phase 2   O += G1 V, A += G2 V           (64 rows x d, K = 32 keys)
+// then o = (C/L) A/L + O/L, the centred form of plx_lla_out_kernel above.
+template <int D>
+struct LlaOutCfg {
+    static constexpr int BM = 64, BK = 32, THREADS = 256;
+    static constexpr int LD = D + 4;
+    static constexpr int DG = D / 16;
+    static constexpr int OFF_K = 0;                          // 2 x [BK][LD]
+    static constexpr int OFF_V = OFF_K + 2 * BK * LD;        // 2 x [BK][LD]
+    static constexpr int OFF_QP = OFF_V + 2 * BK * LD;       // [2 BM][LD]: scale q rows, then rho rows
+    static constexpr int GLD = BM + 4;
+    static constexpr int OFF_G = OFF_QP + 2 * BM * LD;       // 2 x [BK][GLD]: w (1 - r'), w
+    static constexpr int OFF_ROW = OFF_G + 2 * BK * GLD;     // lse, kbar.rho, L, C [BM] each
+    static constexpr int OFF_BAR = OFF_ROW + 4 * BM;         // 2 mbarriers + abort flag
+    static constexpr int SMEM = OFF_BAR * 4 + 32;
+    static_assert(D == 64 || D == 128, "the block output pass is built for d in {64, 128}");
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) plx_lla_out_gemm_kernel(const LlaParams p, const float* v, float* out,
+                                                               float* lse_out) {
+    using Cfg = LlaOutCfg<D>;
+    constexpr int BM = Cfg::BM, BK = Cfg::BK, LD = Cfg::LD, DG = Cfg::DG, GLD = Cfg::GLD;
+    extern __shared__ __align__(128) float lla_osmem[];
+    float* kstage = lla_osmem + Cfg::OFF_K;
+    float* vstage = lla_osmem + Cfg::OFF_V;
+    float* QP = lla_osmem + Cfg::OFF_QP;
+    float* G1s = lla_osmem + Cfg::OFF_G;
+    float* G2s = G1s + BK * GLD;
+    float* s_lse = lla_osmem + Cfg::OFF_ROW;
+    float* s_kx = s_lse + BM;
+    float* s_L = s_kx + BM;
+    float* s_C = s_L + BM;
+    uint64_t* full = reinterpret_cast<uint64_t*>(lla_osmem + Cfg::OFF_BAR);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const size_t bh = blockIdx.y;
+    const int ib = blockIdx.x * BM;
+    if (ib >= p.N) return;
+    const float* K = p.k + bh * p.N * D;
+    const float* V = v + bh * p.N * D;
+
+    if (tid < BM) s_lse[tid] = ib + tid < p.N ? p.lse[bh * p.N + ib + tid] : 0.f;
+    for (int idx = tid; idx < 2 * BM * (D / 4); idx += Cfg::THREADS) {
+        const int r = idx / (D / 4), c = idx % (D / 4);
+        const int i = ib + (r & (BM - 1));
+        float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < p.N) {
+            const size_t off = (bh * p.N + i) * D + c * 4;
+            x4 = *reinterpret_cast<const float4*>((r < BM ? p.q : p.x) + off);
+            if (r < BM) {
+                x4.x *= p.scale;
+                x4.y *= p.scale;
+                x4.z *= p.scale;
+                x4.w *= p.scale;
+            }
+        }
+        *reinterpret_cast<float4*>(QP + r * LD + c * 4) = x4;
+    }
+    // kbar . rho per row: warp w takes rows w, w + 8, ...
+    for (int r = warp; r < BM; r += Cfg::THREADS / 32) {
+        const int i = ib + r;
+        float part = 0.f;
+        if (i < p.N) {
+            const size_t off = (bh * p.N + i) * D;
+            for (int x = lane; x < D; x += 32) part = fmaf(p.kbar[off + x], p.x[off + x], part);
+        }
+        part = warp_sum(part);
+        if (lane == 0) s_kx[r] = part;
+    }
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int kmax = min(ib + BM, p.N) - 1;
+    const int n_tiles = kmax / BK + 1;
+    auto issue = [&](int t) {                             // warp 0, all lanes
+        const int j0 = t * BK;
+        const int nk = min(BK, kmax + 1 - j0);
+        if (!in_bounds(nk > 0 && j0 + nk <= p.N)) {
+            if (lane == 0) mbar_arrive(&full[t & 1]);
+            return;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full[t & 1], static_cast<uint32_t>(2 * nk) * D * 4);
+        __syncwarp();
+        if (lane < nk) {
+            bulk_g2s(kstage + (t & 1) * BK * LD + lane * LD, K + static_cast<size_t>(j0 + lane) * D, D * 4,
+                     &full[t & 1]);
+            bulk_g2s(vstage + (t & 1) * BK * LD + lane * LD, V + static_cast<size_t>(j0 + lane) * D, D * 4,
+                     &full[t & 1]);
+        }
+    };
+    if (warp == 0) issue(0);
+
+    const int rg = tid >> 3, kg = tid & 7;
+    const int rgrp = tid >> 4, dgrp = tid & 15;
+    float O[4][DG], A[4][DG];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int x = 0; x < DG; ++x) {
+            O[i][x] = 0.f;
+            A[i][x] = 0.f;
+        }
+    const float lse0 = s_lse[rg], lse1 = s_lse[rg + 32];
+    const float kx0 = s_kx[rg], kx1 = s_kx[rg + 32];
+    const bool in0 = ib + rg < p.N, in1 = ib + rg + 32 < p.N;
+    float L0 = 0.f, L1 = 0.f, C0 = 0.f, C1 = 0.f;
+    int last_issued = 0;
+
+    for (int t = 0; t < n_tiles; ++t) {
+        if (warp == 0 && t + 1 < n_tiles) {
+            issue(t + 1);
+            last_issued = t + 1;
+        }
+        if (!mbar_wait(&full[t & 1], (t >> 1) & 1)) {
+            atomicOr(&g_plx_status, PLX_DEV_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        const float* kt = kstage + (t & 1) * BK * LD;
+        const float* vt = vstage + (t & 1) * BK * LD;
+        const int j0 = t * BK;
+        const int nk = min(BK, kmax + 1 - j0);
+        float acc[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) acc[m][jj] = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < D; c += 4) {
+            float4 a[4], b[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) a[m] = *reinterpret_cast<const float4*>(QP + (rg + 32 * m) * LD + c);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) b[jj] = *reinterpret_cast<const float4*>(kt + (kg + 8 * jj) * LD + c);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    acc[m][jj] = fmaf(a[m].x, b[jj].x, acc[m][jj]);
+                    acc[m][jj] = fmaf(a[m].y, b[jj].y, acc[m][jj]);
+                    acc[m][jj] = fmaf(a[m].z, b[jj].z, acc[m][jj]);
+                    acc[m][jj] = fmaf(a[m].w, b[jj].w, acc[m][jj]);
+                }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int kk = kg + 8 * jj, j = j0 + kk;
+            // keys past the tile's rows read unfilled shared memory: their r' is not
+            // formed at all (0 x NaN would still be NaN)
+            const bool v0 = kk < nk && in0 && j <= ib + rg, v1 = kk < nk && in1 && j <= ib + rg + 32;
+            const float w0 = v0 ? expf(acc[0][jj] - lse0) : 0.f;
+            const float w1 = v1 ? expf(acc[1][jj] - lse1) : 0.f;
+            const float rc0 = v0 ? acc[2][jj] - kx0 : 0.f, rc1 = v1 ? acc[3][jj] - kx1 : 0.f;
+            L0 += w0;
+            L1 += w1;
+            C0 = fmaf(w0, rc0, C0);
+            C1 = fmaf(w1, rc1, C1);
+            const int a0 = kk * GLD + (rg & 15) * 4 + (rg >> 4), a1 = kk * GLD + (rg & 15) * 4 + ((rg + 32) >> 4);
+            G1s[a0] = w0 - w0 * rc0;
+            G1s[a1] = w1 - w1 * rc1;
+            G2s[a0] = w0;
+            G2s[a1] = w1;
+        }
+        __syncthreads();
+        if (!*abort_flag) {
+#pragma unroll 2
+            for (int kk = 0; kk < nk; ++kk) {
+                const float4 g1 = *reinterpret_cast<const float4*>(G1s + kk * GLD + rgrp * 4);
+                const float4 g2 = *reinterpret_cast<const float4*>(G2s + kk * GLD + rgrp * 4);
+                float vv[DG];
+#pragma unroll
+                for (int x = 0; x < DG; x += 4) {
+                    const float4 v4 = *reinterpret_cast<const float4*>(vt + kk * LD + dgrp * 4 + 16 * x);
+                    vv[x] = v4.x;
+                    vv[x + 1] = v4.y;
+                    vv[x + 2] = v4.z;
+                    vv[x + 3] = v4.w;
+                }
+#pragma unroll
+                for (int x = 0; x < DG; ++x) {
+                    O[0][x] = fmaf(g1.x, vv[x], O[0][x]);
+                    O[1][x] = fmaf(g1.y, vv[x], O[1][x]);
+                    O[2][x] = fmaf(g1.z, vv[x], O[2][x]);
+                    O[3][x] = fmaf(g1.w, vv[x], O[3][x]);
+                    A[0][x] = fmaf(g2.x, vv[x], A[0][x]);
+                    A[1][x] = fmaf(g2.y, vv[x], A[1][x]);
+                    A[2][x] = fmaf(g2.z, vv[x], A[2][x]);
+                    A[3][x] = fmaf(g2.w, vv[x], A[3][x]);
+                }
+            }
+        }
+        __syncthreads();
+        if (*abort_flag) break;
+    }
+    if (warp == 0 && lane == 0 && *abort_flag) mbar_wait(&full[last_issued & 1], (last_issued >> 1) & 1);
+    if (*abort_flag) return;
+    // row sums over the 8 threads of a row (consecutive lanes)
+#pragma unroll
+    for (int m = 4; m >= 1; m >>= 1) {
+        L0 += __shfl_xor_sync(0xffffffffu, L0, m);
+        L1 += __shfl_xor_sync(0xffffffffu, L1, m);
+        C0 += __shfl_xor_sync(0xffffffffu, C0, m);
+        C1 += __shfl_xor_sync(0xffffffffu, C1, m);
+    }
+    if (kg == 0) {
+        s_L[rg] = L0;
+        s_L[rg + 32] = L1;
+        s_C[rg] = C0;
+        s_C[rg + 32] = C1;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int a = rgrp + 16 * i;
+        if (ib + a >= p.N) continue;
+        const size_t row = bh * p.N + ib + a;
+        const float inv = 1.f / s_L[a];
+        const float cn = s_C[a] * inv;
+        float* dst = out + row * D + dgrp * 4;
+#pragma unroll
+        for (int x = 0; x < DG; x += 4)
+            *reinterpret_cast<float4*>(dst + 16 * x) =
+                make_float4(fmaf(cn, A[i][x] * inv, O[i][x] * inv), fmaf(cn, A[i][x + 1] * inv, O[i][x + 1] * inv),
+                            fmaf(cn, A[i][x + 2] * inv, O[i][x + 2] * inv),
+                            fmaf(cn, A[i][x + 3] * inv, O[i][x + 3] * inv));
+        if (dgrp == 0 && lse_out) lse_out[row] = s_lse[a];
+    }
+}
+
 }  // namespace plx

@@ -91,6 +91,8 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, false, plx::BWD_DKV>, BwdTcCfg<64, false, plx::BWD_DKV>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<128>, plx::LlaGemmCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<64>, plx::LlaGemmCfg<64>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<128>, plx::LlaOutCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<64>, plx::LlaOutCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_proj_tc_kernel<128>, ProjCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_proj_tc_kernel<64>, ProjCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_decode_split_kernel<128, true>, DecodeCfg<128>::SMEM);
@@ -444,7 +446,13 @@ void launch_lla(const float* q, const float* k, const float* v, float* out, floa
         for (int it = 0; it < max_iters; ++it)
             plx::plx_lla_cg_step_kernel<DPL><<<grid, plx::LLA_WARPS * 32, plx::LlaTile<DPL>::SMEM, s>>>(lp);
     }
-    plx::plx_lla_out_kernel<DPL><<<grid, plx::LLA_WARPS * 32, 0, s>>>(lp, v, out, lse);
+    if constexpr (DPL == 2 || DPL == 4) {
+        using O = plx::LlaOutCfg<DPL * 32>;
+        dim3 ogrid((N + O::BM - 1) / O::BM, static_cast<unsigned>(BH));
+        plx::plx_lla_out_gemm_kernel<DPL * 32><<<ogrid, O::THREADS, O::SMEM, s>>>(lp, v, out, lse);
+    } else {
+        plx::plx_lla_out_kernel<DPL><<<grid, plx::LLA_WARPS * 32, 0, s>>>(lp, v, out, lse);
+    }
 }
 
 template <int DPL, bool PLX>
