@@ -964,4 +964,227 @@ __global__ void __launch_bounds__(256) plx_lla_out_gemm_kernel(const LlaParams p
     }
 }
 
+// kbar and lse (the softmax attention of the keys themselves) in the same
+// block form (d = 64, 128): a block owns BM = 64 rows and streams key tiles
+// of BK = 32 through two buffers, with an online softmax over the tiles.
+//   phase 1   S = scale q K^T (64 rows x 32 keys); per row the tile max over
+//             its 8 threads, m' = max(m, tile max), alpha = e^(m - m'),
+//             P = e^(s - m') to shared memory, l = alpha l + sum P;
+//   phase 2   U = alpha U + P K                 (64 rows x d, K = 32 keys)
+// then kbar = U / l, lse = m + ln l.
+template <int D>
+struct LlaKbarCfg {
+    static constexpr int BM = 64, BK = 32, THREADS = 256;
+    static constexpr int LD = D + 4;
+    static constexpr int DG = D / 16;
+    static constexpr int OFF_K = 0;                          // 2 x [BK][LD]
+    static constexpr int OFF_Q = OFF_K + 2 * BK * LD;        // [BM][LD]: scale q rows
+    static constexpr int GLD = BM + 4;
+    static constexpr int OFF_P = OFF_Q + BM * LD;            // [BK][GLD]
+    static constexpr int OFF_ROW = OFF_P + BK * GLD;         // alpha, l, m [BM] each
+    static constexpr int OFF_BAR = OFF_ROW + 3 * BM;         // 2 mbarriers + abort flag
+    static constexpr int SMEM = OFF_BAR * 4 + 32;
+    static_assert(D == 64 || D == 128, "the block kbar pass is built for d in {64, 128}");
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) plx_lla_kbar_gemm_kernel(const LlaParams p, float* kbar, float* lse) {
+    using Cfg = LlaKbarCfg<D>;
+    constexpr int BM = Cfg::BM, BK = Cfg::BK, LD = Cfg::LD, DG = Cfg::DG, GLD = Cfg::GLD;
+    extern __shared__ __align__(128) float lla_ksmem[];
+    float* kstage = lla_ksmem + Cfg::OFF_K;
+    float* Qs = lla_ksmem + Cfg::OFF_Q;
+    float* Ps = lla_ksmem + Cfg::OFF_P;
+    float* s_alpha = lla_ksmem + Cfg::OFF_ROW;
+    float* s_l = s_alpha + BM;
+    float* s_m = s_l + BM;
+    uint64_t* full = reinterpret_cast<uint64_t*>(lla_ksmem + Cfg::OFF_BAR);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const size_t bh = blockIdx.y;
+    const int ib = blockIdx.x * BM;
+    if (ib >= p.N) return;
+    const float* K = p.k + bh * p.N * D;
+
+    for (int idx = tid; idx < BM * (D / 4); idx += Cfg::THREADS) {
+        const int r = idx / (D / 4), c = idx % (D / 4);
+        const int i = ib + r;
+        float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < p.N) {
+            x4 = *reinterpret_cast<const float4*>(p.q + (bh * p.N + i) * D + c * 4);
+            x4.x *= p.scale;
+            x4.y *= p.scale;
+            x4.z *= p.scale;
+            x4.w *= p.scale;
+        }
+        *reinterpret_cast<float4*>(Qs + r * LD + c * 4) = x4;
+    }
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int kmax = min(ib + BM, p.N) - 1;
+    const int n_tiles = kmax / BK + 1;
+    auto issue = [&](int t) {                             // warp 0, all lanes
+        const int j0 = t * BK;
+        const int nk = min(BK, kmax + 1 - j0);
+        if (!in_bounds(nk > 0 && j0 + nk <= p.N)) {
+            if (lane == 0) mbar_arrive(&full[t & 1]);
+            return;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full[t & 1], static_cast<uint32_t>(nk) * D * 4);
+        __syncwarp();
+        if (lane < nk)
+            bulk_g2s(kstage + (t & 1) * BK * LD + lane * LD, K + static_cast<size_t>(j0 + lane) * D, D * 4,
+                     &full[t & 1]);
+    };
+    if (warp == 0) issue(0);
+
+    const int rg = tid >> 3, kg = tid & 7;               // phase 1: rows {rg, rg + 32}, keys kg + 8 jj
+    const int rgrp = tid >> 4, dgrp = tid & 15;          // phase 2: rows rgrp + 16 i, dims dgrp * 4 + 64 h + e
+    float U[4][DG];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int x = 0; x < DG; ++x) U[i][x] = 0.f;
+    const bool in0 = ib + rg < p.N, in1 = ib + rg + 32 < p.N;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // per thread: its keys' part of l
+    int last_issued = 0;
+
+    for (int t = 0; t < n_tiles; ++t) {
+        if (warp == 0 && t + 1 < n_tiles) {
+            issue(t + 1);
+            last_issued = t + 1;
+        }
+        if (!mbar_wait(&full[t & 1], (t >> 1) & 1)) {
+            atomicOr(&g_plx_status, PLX_DEV_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        const float* kt = kstage + (t & 1) * BK * LD;
+        const int j0 = t * BK;
+        const int nk = min(BK, kmax + 1 - j0);
+        float acc[2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) acc[m][jj] = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < D; c += 4) {
+            float4 a[2], b[4];
+#pragma unroll
+            for (int m = 0; m < 2; ++m) a[m] = *reinterpret_cast<const float4*>(Qs + (rg + 32 * m) * LD + c);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) b[jj] = *reinterpret_cast<const float4*>(kt + (kg + 8 * jj) * LD + c);
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    acc[m][jj] = fmaf(a[m].x, b[jj].x, acc[m][jj]);
+                    acc[m][jj] = fmaf(a[m].y, b[jj].y, acc[m][jj]);
+                    acc[m][jj] = fmaf(a[m].z, b[jj].z, acc[m][jj]);
+                    acc[m][jj] = fmaf(a[m].w, b[jj].w, acc[m][jj]);
+                }
+        }
+        // masked scores (keys past the row, past the tile's rows, rows past N) are -inf
+        float t0 = -INFINITY, t1 = -INFINITY;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int kk = kg + 8 * jj, j = j0 + kk;
+            if (!(kk < nk && in0 && j <= ib + rg)) acc[0][jj] = -INFINITY;
+            if (!(kk < nk && in1 && j <= ib + rg + 32)) acc[1][jj] = -INFINITY;
+            t0 = fmaxf(t0, acc[0][jj]);
+            t1 = fmaxf(t1, acc[1][jj]);
+        }
+#pragma unroll
+        for (int off = 4; off >= 1; off >>= 1) {
+            t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
+            t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
+        }
+        const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
+        // a row with no valid key so far keeps alpha = 1 and P = 0
+        const float a0 = n0 == -INFINITY ? 1.f : expf(m0 - n0), a1 = n1 == -INFINITY ? 1.f : expf(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+        l0 *= a0;
+        l1 *= a1;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int kk = kg + 8 * jj;
+            const float p0 = acc[0][jj] == -INFINITY ? 0.f : expf(acc[0][jj] - n0);
+            const float p1 = acc[1][jj] == -INFINITY ? 0.f : expf(acc[1][jj] - n1);
+            l0 += p0;
+            l1 += p1;
+            Ps[kk * GLD + (rg & 15) * 4 + (rg >> 4)] = p0;
+            Ps[kk * GLD + (rg & 15) * 4 + ((rg + 32) >> 4)] = p1;
+        }
+        if (kg == 0) {
+            s_alpha[rg] = a0;
+            s_alpha[rg + 32] = a1;
+        }
+        __syncthreads();
+        if (!*abort_flag) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float al = s_alpha[rgrp + 16 * i];
+#pragma unroll
+                for (int x = 0; x < DG; ++x) U[i][x] *= al;
+            }
+#pragma unroll 2
+            for (int kk = 0; kk < nk; ++kk) {
+                const float4 g = *reinterpret_cast<const float4*>(Ps + kk * GLD + rgrp * 4);
+                float kv[DG];
+#pragma unroll
+                for (int x = 0; x < DG; x += 4) {
+                    const float4 k4 = *reinterpret_cast<const float4*>(kt + kk * LD + dgrp * 4 + 16 * x);
+                    kv[x] = k4.x;
+                    kv[x + 1] = k4.y;
+                    kv[x + 2] = k4.z;
+                    kv[x + 3] = k4.w;
+                }
+#pragma unroll
+                for (int x = 0; x < DG; ++x) {
+                    U[0][x] = fmaf(g.x, kv[x], U[0][x]);
+                    U[1][x] = fmaf(g.y, kv[x], U[1][x]);
+                    U[2][x] = fmaf(g.z, kv[x], U[2][x]);
+                    U[3][x] = fmaf(g.w, kv[x], U[3][x]);
+                }
+            }
+        }
+        __syncthreads();
+        if (*abort_flag) break;
+    }
+    if (warp == 0 && lane == 0 && *abort_flag) mbar_wait(&full[last_issued & 1], (last_issued >> 1) & 1);
+    if (*abort_flag) return;
+#pragma unroll
+    for (int off = 4; off >= 1; off >>= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    if (kg == 0) {
+        s_l[rg] = l0;
+        s_l[rg + 32] = l1;
+        s_m[rg] = m0;
+        s_m[rg + 32] = m1;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int a = rgrp + 16 * i;
+        if (ib + a >= p.N) continue;
+        const size_t row = bh * p.N + ib + a;
+        const float inv = 1.f / s_l[a];
+        float* dst = kbar + row * D + dgrp * 4;
+#pragma unroll
+        for (int x = 0; x < DG; x += 4)
+            *reinterpret_cast<float4*>(dst + 16 * x) =
+                make_float4(U[i][x] * inv, U[i][x + 1] * inv, U[i][x + 2] * inv, U[i][x + 3] * inv);
+        if (dgrp == 0) lse[row] = s_m[a] + logf(s_l[a]);
+    }
+}
+
 }  // namespace plx

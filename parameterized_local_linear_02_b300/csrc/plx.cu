@@ -93,6 +93,8 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<64>, plx::LlaGemmCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<128>, plx::LlaOutCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<64>, plx::LlaOutCfg<64>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_kbar_gemm_kernel<128>, plx::LlaKbarCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_kbar_gemm_kernel<64>, plx::LlaKbarCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_proj_tc_kernel<128>, ProjCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_proj_tc_kernel<64>, ProjCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_decode_split_kernel<128, true>, DecodeCfg<128>::SMEM);
@@ -431,9 +433,16 @@ LlaWorkspace lla_ws_carve(void* base, long long R, int d) {
 template <int DPL>
 void launch_lla(const float* q, const float* k, const float* v, float* out, float* lse, const LlaWorkspace& w,
                 int N, long long BH, float scale, float lambda, int max_iters, float tol, cudaStream_t s) {
-    plx::FwdF32Params f{q, k, k, nullptr, w.kbar, w.lse, N, scale};
-    launch_f32<DPL, false>(f, BH, s);
     plx::LlaParams lp{q, k, w.kbar, w.lse, w.x, w.r, w.p, w.rs, w.rs0, w.steps, N, scale, lambda, tol * tol};
+    if constexpr (DPL == 2 || DPL == 4) {
+        // d = 64, 128: kbar and lse in the block form of the CG step
+        using Kc = plx::LlaKbarCfg<DPL * 32>;
+        dim3 kgrid((N + Kc::BM - 1) / Kc::BM, static_cast<unsigned>(BH));
+        plx::plx_lla_kbar_gemm_kernel<DPL * 32><<<kgrid, Kc::THREADS, Kc::SMEM, s>>>(lp, w.kbar, w.lse);
+    } else {
+        plx::FwdF32Params f{q, k, k, nullptr, w.kbar, w.lse, N, scale};
+        launch_f32<DPL, false>(f, BH, s);
+    }
     dim3 grid((N + plx::LLA_ROWS_PER_BLOCK - 1) / plx::LLA_ROWS_PER_BLOCK, static_cast<unsigned>(BH));
     plx::plx_lla_init_kernel<DPL><<<grid, plx::LLA_WARPS * 32, 0, s>>>(lp);
     if constexpr (DPL == 2 || DPL == 4) {
