@@ -149,6 +149,19 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def hold_device(us=100.0):
+    """Queue a spin kernel of about `us` microseconds on the current stream.
+    A CUDA-event pair recorded on an idle device also times the host's work
+    to issue the launch between them (argument checks, tensor-map encoding,
+    the launch call): the start event fires at once and the device then
+    waits for the kernel.  With the device busy for longer than that, the
+    launch is queued before the start event fires, and the pair times the
+    kernel alone.  It is queued before the L2 flush, outside every timed
+    pair."""
+    import torch
+    torch.cuda._sleep(int(us * 2000))    # clock64 cycles, about 2 GHz
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -374,6 +387,10 @@ def run_ours(args, world, rank, local):
     ev_f, ev_l, ev_d = [], [], []
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    # the device works through this while the host queues the first steps; a
+    # step's launches then run well behind the host, so no timed pair
+    # contains the time to issue a launch
+    hold_device(1000.0)
     t_start.record(stream)
     for _ in range(args.steps):
         if do_pf:
@@ -455,6 +472,7 @@ def run_ours(args, world, rank, local):
                                             / peaks["bf16_tflops_sustained"]}
     if extras:
         sa = {}
+        hold_device(1000.0)
         if do_pf:
             sa_f = timed(lambda: fwd(False), max(5, args.steps // 2))
         if do_long:
@@ -603,6 +621,7 @@ def run_decode_sweep(args, world, rank, local):
                     call()
                 ms = []
                 for _ in range(args.sweep_iters):
+                    hold_device()
                     flush.zero_()
                     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a.record(stream)
@@ -670,6 +689,7 @@ def run_backward_bench(args, world, rank, local):
         torch.cuda.synchronize()
         ms = []
         for _ in range(steps):
+            hold_device()
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -682,11 +702,13 @@ def run_backward_bench(args, world, rank, local):
     def call():
         plx.plx_bwd(tb["q"], tb["k"], tb["v"], tb["rho"], dout, scale=x.scale, workspace=ws, grads=grads)
 
+    # the sampler's first readings come in before the warm-up (as in the main step)
     sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
     for _ in range(max(3, args.warmup)):
         call()
     torch.cuda.synchronize()
-    sampler.start()
     med, nsteps = timed(call, max(3, args.steps), 0)
     clocks = sampler.stop()
     # the fp32 path on the same values
@@ -783,6 +805,7 @@ def run_cached_bench(args, world, rank, local):
         torch.cuda.synchronize()
         ms = []
         for _ in range(steps):
+            hold_device()
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -795,6 +818,9 @@ def run_cached_bench(args, world, rank, local):
     kv_bytes = B * H * S * d * 2 * 2
     q1 = torch.randn((B, H, d), generator=g, device=dev).to(torch.bfloat16)
     r1 = (0.1 * torch.randn((B, H, d), generator=g, device=dev)).to(torch.bfloat16)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
     dec_ms = timed(lambda: plx.plx_decode(q1, r1, kc, vc, seqlens), max(3, args.steps))
     rows = []
     for T in (1, 16, 64, 128):
@@ -805,6 +831,7 @@ def run_cached_bench(args, world, rank, local):
         gbs = kv_bytes / (ms * 1e-3) / 1e9
         rows.append({"T": T, "ms": ms, "kv_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
                      "tokens_per_s": B * T / (ms * 1e-3), "vs_T_decode_calls": T * dec_ms / ms})
+    clocks = sampler.stop()
     line = {"metric": "PLX multi-token decode against a KV cache (plx_fwd_cached), K/V GB/s and tokens/s, 1 GPU",
             "unit": "GB/s", "value": rows[1]["kv_gbs"], "n_gpus": 1, "steps": max(3, args.steps),
             "warmup": max(3, args.warmup), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
@@ -813,6 +840,7 @@ def run_cached_bench(args, world, rank, local):
             "roofline": {"bound": "hbm", "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "peak_source": f"{peaks['source']} HBM copy"},
             "plx_decode_ms": dec_ms, "plx_decode_kv_gbs": kv_bytes / (dec_ms * 1e-3) / 1e9, "by_T": rows,
+            "clocks": clocks,
             "gpu_launches": (4 + 1) * max(3, args.steps), "device_status": plx.plx_last_device_error()}
     print(json.dumps(line), flush=True)
     return 0
@@ -848,6 +876,7 @@ def run_proj_bench(args, world, rank, local):
         torch.cuda.synchronize()
         ms = []
         for _ in range(steps):
+            hold_device()
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -858,10 +887,11 @@ def run_proj_bench(args, world, rank, local):
         return float(np.median(ms)), len(ms)
 
     sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
     for _ in range(max(3, args.warmup)):
         plx.plx_probe_proj(x, w, heads=H, out=rho)
     torch.cuda.synchronize()
-    sampler.start()
     med, nsteps = timed(lambda: plx.plx_probe_proj(x, w, heads=H, out=rho), max(3, args.steps))
     clocks = sampler.stop()
     y = torch.empty((B * N, H * d), dtype=torch.bfloat16, device=dev)
@@ -930,6 +960,7 @@ def run_lla_bench(args, world, rank, local):
     sampler.start()
     ms = []
     for _ in range(max(3, args.steps)):
+        hold_device()
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
