@@ -228,7 +228,7 @@ size_t plx_bwd_bf16_workspace_size(int B, int H, int N, int d);
  * Consapevole dell'Hardware").  q, k, v, rho, out and lse live in host memory
  * (page-locked, for the copies to run asynchronously and to overlap; pageable
  * memory works, with the copies staged by the driver).  The heads go through
- * the device workspace in up to 16 chunks: while chunk c is computed, chunk
+ * the device workspace in up to 8 chunks: while chunk c is computed, chunk
  * c + 1 is copied in and chunk c - 1 copied out, on the GPU's copy engines
  * (two streams of the library, one cudaMemcpyAsync per array and chunk).  The
  * results are those of plx_fwd on the same values, bit for bit.

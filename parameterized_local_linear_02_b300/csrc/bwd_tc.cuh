@@ -653,8 +653,9 @@ plx_bwd_tc_kernel(const __grid_constant__ CUtensorMap mapRes0, const __grid_cons
 // instead of the statistics pass: with vbar_i = O_i / l_i and c_i from the
 // forward, a_i = dO_i.vbar_i and D_i = dO_i.o_i + c_i a_i (the same identities
 // as the header above: e_i = dO_i.u_i with u_i = (1 + c_i) vbar_i - o_i).  For
-// softmax attention (no rho) vbar_i = o_i and c_i = 0.  One warp per row, each
-// lane D/32 consecutive elements (coalesced 16- and 8-byte loads).
+// softmax attention (no rho) vbar_i = o_i and c_i = 0.  Each warp takes two
+// rows and issues both rows' loads before either reduction; each lane holds D/32
+// consecutive elements of a row (coalesced 16- and 8-byte loads).
 struct BwdPrepParams {
     const float* lse;      // natural-log lse per row, [rows]
     const float* c;        // c_i per row, or nullptr (softmax attention)
@@ -665,7 +666,9 @@ struct BwdPrepParams {
     long long rows;
     int out_f32;
 };
-constexpr int BWD_PREP_ROWS_PER_BLOCK = 8;
+constexpr int BWD_PREP_WARPS = 8;
+constexpr int BWD_PREP_ROWS_PER_WARP = 2;   // both rows' loads in flight before either reduction
+constexpr int BWD_PREP_ROWS_PER_BLOCK = BWD_PREP_WARPS * BWD_PREP_ROWS_PER_WARP;
 
 template <int D>
 __device__ __forceinline__ void load_bf16_vec(const uint16_t* src, float (&x)[D / 32]) {
@@ -689,39 +692,47 @@ __device__ __forceinline__ void load_f32_vec(const float* src, float (&x)[D / 32
 }
 
 template <int D>
-__global__ void __launch_bounds__(BWD_PREP_ROWS_PER_BLOCK * 32)
+__global__ void __launch_bounds__(BWD_PREP_WARPS * 32)
 plx_bwd_prep_kernel(const BwdPrepParams p) {
-    constexpr int E = D / 32;
+    constexpr int E = D / 32, R = BWD_PREP_ROWS_PER_WARP;
     const int lane = threadIdx.x & 31;
-    const long long row = static_cast<long long>(blockIdx.x) * BWD_PREP_ROWS_PER_BLOCK + (threadIdx.x >> 5);
-    if (row >= p.rows) return;
-    const size_t base = static_cast<size_t>(row) * D + lane * E;
-    float g[E], o[E], vb[E];
-    load_bf16_vec<D>(p.dout + base, g);
-    if (p.out_f32)
-        load_f32_vec<D>(static_cast<const float*>(p.out) + base, o);
-    else
-        load_bf16_vec<D>(static_cast<const uint16_t*>(p.out) + base, o);
-    if (p.vbar) {
-        load_f32_vec<D>(p.vbar + base, vb);
-    } else {
+    const long long row0 = (static_cast<long long>(blockIdx.x) * BWD_PREP_WARPS + (threadIdx.x >> 5)) * R;
+    float g[R][E], o[R][E], vb[R][E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) vb[e] = o[e];
-    }
-    float a = 0.f, od = 0.f;
+    for (int i = 0; i < R; ++i) {
+        if (row0 + i >= p.rows) continue;
+        const size_t base = static_cast<size_t>(row0 + i) * D + lane * E;
+        load_bf16_vec<D>(p.dout + base, g[i]);
+        if (p.out_f32)
+            load_f32_vec<D>(static_cast<const float*>(p.out) + base, o[i]);
+        else
+            load_bf16_vec<D>(static_cast<const uint16_t*>(p.out) + base, o[i]);
+        if (p.vbar) {
+            load_f32_vec<D>(p.vbar + base, vb[i]);
+        } else {
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-        a = fmaf(g[e], vb[e], a);
-        od = fmaf(g[e], o[e], od);
+            for (int e = 0; e < E; ++e) vb[i][e] = o[i][e];
+        }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        a += __shfl_xor_sync(0xffffffffu, a, off);
-        od += __shfl_xor_sync(0xffffffffu, od, off);
-    }
-    if (lane == 0) {
-        const float ci = p.c ? p.c[row] : 0.f;
-        p.stats[row] = make_float4(p.lse[row] * 1.4426950408889634f, ci, a, fmaf(ci, a, od));
+    for (int i = 0; i < R; ++i) {
+        const long long row = row0 + i;
+        if (row >= p.rows) break;
+        float a = 0.f, od = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            a = fmaf(g[i][e], vb[i][e], a);
+            od = fmaf(g[i][e], o[i][e], od);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, off);
+            od += __shfl_xor_sync(0xffffffffu, od, off);
+        }
+        if (lane == 0) {
+            const float ci = p.c ? p.c[row] : 0.f;
+            p.stats[row] = make_float4(p.lse[row] * 1.4426950408889634f, ci, a, fmaf(ci, a, od));
+        }
     }
 }
 

@@ -367,7 +367,7 @@ plx_status launch_bwd_tc(const void* q, const void* k, const void* v, const void
         pp.rows = BH * N;
         const long long blocks = (pp.rows + plx::BWD_PREP_ROWS_PER_BLOCK - 1) / plx::BWD_PREP_ROWS_PER_BLOCK;
         if (blocks > INT_MAX) return PLX_ERR_UNSUPPORTED;
-        plx::plx_bwd_prep_kernel<D><<<static_cast<unsigned>(blocks), plx::BWD_PREP_ROWS_PER_BLOCK * 32, 0, s>>>(pp);
+        plx::plx_bwd_prep_kernel<D><<<static_cast<unsigned>(blocks), plx::BWD_PREP_WARPS * 32, 0, s>>>(pp);
     } else {
         // the row statistics (lse, c, a, D) with the weights the two gradient passes use
         plx::plx_bwd_tc_kernel<D, PLX, plx::BWD_STATS><<<grid, CfgS::THREADS, CfgS::SMEM, s>>>(
@@ -660,7 +660,11 @@ float* noalloc_scratch() {
 // heads.  kHostBuffers chunks are in flight at once (one being copied in, one
 // computed, one copied out), each in its own slice of the workspace.
 constexpr int kHostBuffers = 3;
-constexpr int kHostChunks = 16;          // chunks per call (fewer when B H is smaller)
+// Chunks per call (fewer when B H is smaller).  The copies set the time: every
+// cudaMemcpyAsync costs about 2 us beyond its bytes, and the last chunk's
+// kernel and copy-out run alone after the last copy-in.  On the bench prefill
+// shape 8 chunks took 3.38 ms per call, 16 took 3.48 and 32 took 3.74.
+constexpr int kHostChunks = 8;
 
 // The copy streams and the events of the pipeline, one set per device and
 // CUDA context (cudaDeviceReset gives the device a new context, in which the
