@@ -24,6 +24,10 @@
 
 namespace plx {
 
+// the largest split count whose combine runs inside one thread-block cluster
+// (clusters of more than 8 CTAs are the non-portable, opt-in sizes)
+constexpr int DECODE_MAX_CLUSTER_SPLITS = 16;
+
 template <int D>
 struct DecodeCfg {
     static constexpr int T = 32;                    // cache rows per stage
@@ -372,19 +376,51 @@ plx_decode_split_kernel(const DecodeParams p) {
         // rank 0 has read them.  The merge is the combine kernel's, in rank order.
         cluster_sync_all();
         if (cluster_rank() == 0 && threadIdx.x < D) {
+            // The remote reads go four ranks at a time, all of a group's loads in
+            // flight before any is used: a loop that used each value before the
+            // next load waited out the distributed-shared-memory latency once per
+            // load (three or four times per rank).  Same operations, same order.
+            constexpr int G4 = 4;
+            static_assert(DECODE_MAX_CLUSTER_SPLITS % G4 == 0, "groups of four ranks");
             const int t = threadIdx.x;
             float M = -INFINITY;
-            for (int r = 0; r < p.splits; ++r) M = fmaxf(M, ld_cluster_f32(cpart, r));
+#pragma unroll
+            for (int r0 = 0; r0 < DECODE_MAX_CLUSTER_SPLITS; r0 += G4) {
+                if (r0 >= p.splits) break;
+                float mv[G4];
+#pragma unroll
+                for (int k = 0; k < G4; ++k) mv[k] = r0 + k < p.splits ? ld_cluster_f32(cpart, r0 + k) : -INFINITY;
+#pragma unroll
+                for (int k = 0; k < G4; ++k) M = fmaxf(M, mv[k]);
+            }
             float Lsum = 0.f, Cs = 0.f, As = 0.f, Us = 0.f;
             if (M != -INFINITY) {
-                for (int r = 0; r < p.splits; ++r) {
-                    const float mr = ld_cluster_f32(cpart, r);
-                    if (mr == -INFINITY) continue;
-                    const float sc = exp2f(mr - M);
-                    Lsum = fmaf(sc, ld_cluster_f32(cpart + 1, r), Lsum);
-                    Cs = fmaf(sc, ld_cluster_f32(cpart + 2, r), Cs);
-                    As = fmaf(sc, ld_cluster_f32(cpart + 4 + t, r), As);
-                    if constexpr (PLX) Us = fmaf(sc, ld_cluster_f32(cpart + 4 + D + t, r), Us);
+#pragma unroll
+                for (int r0 = 0; r0 < DECODE_MAX_CLUSTER_SPLITS; r0 += G4) {
+                    if (r0 >= p.splits) break;
+                    float mv[G4], lv[G4], cv[G4], av[G4], uv[G4];
+#pragma unroll
+                    for (int k = 0; k < G4; ++k) {
+                        const int r = r0 + k;
+                        mv[k] = -INFINITY;
+                        lv[k] = cv[k] = av[k] = uv[k] = 0.f;
+                        if (r < p.splits) {
+                            mv[k] = ld_cluster_f32(cpart, r);
+                            lv[k] = ld_cluster_f32(cpart + 1, r);
+                            cv[k] = ld_cluster_f32(cpart + 2, r);
+                            av[k] = ld_cluster_f32(cpart + 4 + t, r);
+                            if constexpr (PLX) uv[k] = ld_cluster_f32(cpart + 4 + D + t, r);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < G4; ++k) {
+                        if (mv[k] == -INFINITY) continue;
+                        const float sc = exp2f(mv[k] - M);
+                        Lsum = fmaf(sc, lv[k], Lsum);
+                        Cs = fmaf(sc, cv[k], Cs);
+                        As = fmaf(sc, av[k], As);
+                        if constexpr (PLX) Us = fmaf(sc, uv[k], Us);
+                    }
                 }
             }
             float o = 0.f;
@@ -415,16 +451,32 @@ __global__ void __launch_bounds__(D) plx_decode_combine_kernel(const DecodeParam
     }
     float Lsum = 0.f, Cs = 0.f, As = 0.f, Us = 0.f;
     if (M != -INFINITY) {
+        // four splits' values loaded before any is used (one memory latency per
+        // four splits rather than two per split); same operations, same order
+        constexpr int G4 = 4;
         for (int g = 0; g < p.groups; ++g) {
             const float* base = p.ws + g * group_stride + static_cast<size_t>(bh) * p.splits * PART;
-            for (int s = 0; s < p.splits; ++s) {
-                const float* ps = base + s * PART;
-                if (ps[0] == -INFINITY) continue;
-                const float sc = exp2f(ps[0] - M);
-                Lsum = fmaf(sc, ps[1], Lsum);
-                Cs = fmaf(sc, ps[2], Cs);
-                As = fmaf(sc, ps[4 + t], As);
-                if constexpr (PLX) Us = fmaf(sc, ps[4 + D + t], Us);
+            for (int s0 = 0; s0 < p.splits; s0 += G4) {
+                float mv[G4], lv[G4], cv[G4], av[G4], uv[G4];
+#pragma unroll
+                for (int k = 0; k < G4; ++k) {
+                    const float* ps = base + (s0 + k) * PART;
+                    const bool in = s0 + k < p.splits;
+                    mv[k] = in ? ps[0] : -INFINITY;
+                    lv[k] = in ? ps[1] : 0.f;
+                    cv[k] = in ? ps[2] : 0.f;
+                    av[k] = in ? ps[4 + t] : 0.f;
+                    uv[k] = (PLX && in) ? ps[4 + D + t] : 0.f;
+                }
+#pragma unroll
+                for (int k = 0; k < G4; ++k) {
+                    if (mv[k] == -INFINITY) continue;
+                    const float sc = exp2f(mv[k] - M);
+                    Lsum = fmaf(sc, lv[k], Lsum);
+                    Cs = fmaf(sc, cv[k], Cs);
+                    As = fmaf(sc, av[k], As);
+                    if constexpr (PLX) Us = fmaf(sc, uv[k], Us);
+                }
             }
         }
     }

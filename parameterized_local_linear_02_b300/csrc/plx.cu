@@ -45,7 +45,7 @@ struct DeviceInfo {
     bool decode_cluster_ok = false;
 };
 
-constexpr int kMaxFusedSplits = 16;
+constexpr int kMaxFusedSplits = plx::DECODE_MAX_CLUSTER_SPLITS;
 
 std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
