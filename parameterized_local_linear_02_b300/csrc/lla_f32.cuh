@@ -178,6 +178,13 @@ __global__ void __launch_bounds__(LLA_WARPS * 32) plx_lla_cg_step_kernel(const L
         rs[r] = p.rs[row];
         act[r] = i < p.N && rs[r] > p.tol2 * p.rs0[row];
         any |= act[r];
+    }
+    // a block whose rows have all stopped returns before it reads anything else
+    if (!__syncthreads_or(any)) return;
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+        const int i = i0 + r;
+        const size_t row = bh * p.N + (i < p.N ? i : ib);
         lse[r] = p.lse[row];
         float kb[DPL];
         load_own<DPL>(p.q + row * D, lane, qv[r]);
@@ -198,7 +205,7 @@ __global__ void __launch_bounds__(LLA_WARPS * 32) plx_lla_cg_step_kernel(const L
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (!__syncthreads_or(any)) return;                   // every row of the block has stopped
+    __syncthreads();
 
     const int kmax = min(ib + LLA_ROWS_PER_BLOCK, p.N) - 1;   // last key the block needs
     const int n_tiles = kmax / TK + 1;
@@ -378,7 +385,10 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
     const int ib = blockIdx.x * BM;
     const float* K = p.k + bh * p.N * D;
 
-    // ---- prologue: row scalars, q (scaled) and p rows into shared memory
+    // ---- prologue: row scalars first; a block whose rows have all stopped
+    // returns before it reads anything else (late steps launch every block, and
+    // most of them have nothing left to do)
+    int any_local = 0;
     if (tid < BM) {
         const int i = ib + tid;
         int a = 0;
@@ -392,7 +402,10 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
         s_act[tid] = a;
         s_lse[tid] = lse;
         s_rs[tid] = rs;
+        any_local = a;
     }
+    if (!__syncthreads_or(any_local)) return;             // every row of the block has stopped
+    // q (scaled) and p rows into shared memory
     for (int idx = tid; idx < 2 * BM * (D / 4); idx += Cfg::THREADS) {
         const int r = idx / (D / 4), c = idx % (D / 4);
         const int i = ib + (r & (BM - 1));
@@ -427,8 +440,6 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
         fence_mbar_init();
     }
     __syncthreads();
-    int any_local = tid < BM ? s_act[tid] : 0;
-    if (!__syncthreads_or(any_local)) return;             // every row of the block has stopped
 
     const int kmax = min(ib + BM, p.N) - 1;
     const int n_tiles = kmax / BK + 1;
