@@ -475,7 +475,9 @@ plx_status plx_decode_combine(const void* partials, int groups, int num_splits, 
  *   lse      : fp32 [B][H][N] natural-log softmax normaliser, or NULL.
  *   steps_out: int32 [B][H][N] conjugate-gradient steps taken per row, or NULL.
  *   workspace: device scratch of plx_lla_workspace_size(B, H, N, d) bytes,
- *              256-byte aligned, no initialisation.
+ *              256-byte aligned, no initialisation; with at least
+ *              plx_lla_kept_weights_workspace_size(B, H, N, d) bytes the
+ *              softmax weights are kept across the CG steps (same results).
  *   B, H, N >= 1, B * H <= 65535; d a multiple of 32 in [32, 256];
  *   lambda >= 0 (finite); max_iters >= 0; tol >= 0 (finite).
  *   lambda = 0 needs every row's Sigma_KK to be non-singular (a prefix of at
@@ -491,6 +493,18 @@ plx_status plx_lla_f32(const float* q, const float* k, const float* v, float* ou
 
 /* Workspace bytes plx_lla_f32 needs: about B*H*N*(4d + 4)*4 (0 for invalid sizes). */
 size_t plx_lla_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Workspace bytes with which plx_lla_f32 keeps the CG steps' softmax weights
+ * w_ij = exp(s_ij - lse_i) from the first step instead of recomputing them in
+ * every step (they do not depend on the iterate): plx_lla_workspace_size plus
+ * B*H*N*N*4 bytes, for d in {64, 128} (for other d the same as
+ * plx_lla_workspace_size).  A call given at least this many bytes takes that
+ * path; its results are those of the recomputing path, bit for bit.  The
+ * extra space grows as N^2 (1.07 GB at B = 4, H = 16, N = 2048; 275 GB at
+ * N = 32768), so it is for short contexts.
+ */
+size_t plx_lla_kept_weights_workspace_size(int B, int H, int N, int d);
 
 /*
  * plx_probe_proj -- the probe projection rho_i = W_R x_i that feeds every

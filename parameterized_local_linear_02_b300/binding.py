@@ -100,6 +100,8 @@ def load(path: str) -> ctypes.CDLL:
     lib.plx_lla_f32.argtypes = [vp] * 8 + [sz, i, i, i, i, f, f, i, f, vp]
     lib.plx_lla_workspace_size.restype = sz
     lib.plx_lla_workspace_size.argtypes = [i, i, i, i]
+    lib.plx_lla_kept_weights_workspace_size.restype = sz
+    lib.plx_lla_kept_weights_workspace_size.argtypes = [i, i, i, i]
     lib.plx_probe_proj.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
     lib.plx_last_device_error.restype = i
     lib.plx_last_device_error.argtypes = [vp]
@@ -419,13 +421,19 @@ def plx_lla_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return library().plx_lla_workspace_size(B, H, N, d)
 
 
+def plx_lla_kept_weights_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return library().plx_lla_kept_weights_workspace_size(B, H, N, d)
+
+
 def plx_lla_f32(q, k, v, *, lam, max_iters, tol=0.0, scale=None, workspace=None, out=None, rho_out=None,
-                lse=None, steps=None, with_rho=True, with_steps=True):
+                lse=None, steps=None, with_rho=True, with_steps=True, keep_weights=False):
     """Local linear attention with the probe solved by conjugate gradients
     (fp32 [B, H, N, d] q, k, v; ridge ``lam``; at most ``max_iters`` steps per
     row, a row stopping once |r| <= tol |mu|).  Returns ``(out, rho, lse,
     steps)``; rho (the solved probe) and steps (int32 per row) are None when
-    not requested."""
+    not requested.  ``keep_weights`` allocates the larger workspace with which
+    the CG steps keep their softmax weights (same results; B H N^2 fp32 more);
+    a caller-given ``workspace`` of that size has the same effect."""
     B, H, N, d = q.shape
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -444,7 +452,7 @@ def plx_lla_f32(q, k, v, *, lam, max_iters, tol=0.0, scale=None, workspace=None,
         steps = torch.empty((B, H, N), dtype=torch.int32, device=dev)
     if steps is not None:
         _need(steps, "steps", torch.int32, (B, H, N), dev)
-    need = plx_lla_workspace_size(B, H, N, d)
+    need = plx_lla_kept_weights_workspace_size(B, H, N, d) if keep_weights else plx_lla_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()

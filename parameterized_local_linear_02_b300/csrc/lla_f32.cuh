@@ -47,6 +47,9 @@ struct LlaParams {
     float scale;
     float lambda;
     float tol2;          // tol^2
+    // [BH][N][N] fp32: the CG steps' softmax weights w_ij = exp(s_ij - lse_i),
+    // j <= i, kept from the first step (nullptr: every step recomputes them)
+    float* wts;
 };
 
 constexpr int LLA_WARPS = 4;
@@ -365,7 +368,12 @@ struct LlaGemmCfg {
     static_assert(D == 64 || D == 128, "the block GEMM step is built for d in {64, 128}");
 };
 
-template <int D>
+// WMODE 0: the step computes the weights w_ij from s_ij = scale q_i.k_j and
+// lse_i; 1: it also stores them (those of active rows) in p.wts; 2: it reads
+// them from p.wts and computes only p.k_j, half of phase 1.  The weights do
+// not depend on the iterate, and the stored values are the computed ones, so
+// the three modes give the same bits.
+template <int D, int WMODE = 0>
 __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p) {
     using Cfg = LlaGemmCfg<D>;
     constexpr int BM = Cfg::BM, BK = Cfg::BK, LD = Cfg::LD, DG = Cfg::DG, GLD = Cfg::GLD;
@@ -409,6 +417,7 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
     for (int idx = tid; idx < 2 * BM * (D / 4); idx += Cfg::THREADS) {
         const int r = idx / (D / 4), c = idx % (D / 4);
         const int i = ib + (r & (BM - 1));
+        if (WMODE == 2 && r < BM) continue;              // q rows: the weights are stored
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < p.N) {
             const size_t off = (bh * p.N + i) * D + c * 4;
@@ -485,7 +494,22 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
         const float* kt = stage + (t & 1) * BK * LD;
         const int j0 = t * BK;
         const int nk = min(BK, kmax + 1 - j0);
+        // rows rg, rg + 32 of the block and their weight rows (WMODE 1, 2)
+        const size_t wrow0 = (bh * p.N + ib + rg) * static_cast<size_t>(p.N);
+        const size_t wrow1 = wrow0 + 32 * static_cast<size_t>(p.N);
+        float wv[2][4];
+        if constexpr (WMODE == 2) {
+            // the stored weights of this tile, loaded ahead of phase 1's FMAs
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int kk = kg + 8 * jj, j = j0 + kk;
+                wv[0][jj] = (kk < nk && act0 && j <= ib + rg) ? p.wts[wrow0 + j] : 0.f;
+                wv[1][jj] = (kk < nk && act1 && j <= ib + rg + 32) ? p.wts[wrow1 + j] : 0.f;
+            }
+        }
         // phase 1: acc[m][jj], m = 0, 1: s of rows rg, rg+32; m = 2, 3: p.k of the same rows
+        // (WMODE 2: only m = 2, 3)
+        constexpr int M0 = WMODE == 2 ? 2 : 0;
         float acc[4][4];
 #pragma unroll
         for (int m = 0; m < 4; ++m)
@@ -495,11 +519,11 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
         for (int c = 0; c < D; c += 4) {
             float4 a[4], b[4];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) a[m] = *reinterpret_cast<const float4*>(QP + (rg + 32 * m) * LD + c);
+            for (int m = M0; m < 4; ++m) a[m] = *reinterpret_cast<const float4*>(QP + (rg + 32 * m) * LD + c);
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) b[jj] = *reinterpret_cast<const float4*>(kt + (kg + 8 * jj) * LD + c);
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int m = M0; m < 4; ++m)
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     acc[m][jj] = fmaf(a[m].x, b[jj].x, acc[m][jj]);
@@ -513,8 +537,21 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
         for (int jj = 0; jj < 4; ++jj) {
             const int kk = kg + 8 * jj, j = j0 + kk;
             const bool in = kk < nk;
-            const float g0 = (in && act0 && j <= ib + rg) ? expf(acc[0][jj] - lse0) * (acc[2][jj] - kp0) : 0.f;
-            const float g1 = (in && act1 && j <= ib + rg + 32) ? expf(acc[1][jj] - lse1) * (acc[3][jj] - kp1) : 0.f;
+            const bool live0 = in && act0 && j <= ib + rg, live1 = in && act1 && j <= ib + rg + 32;
+            float w0, w1;
+            if constexpr (WMODE == 2) {
+                w0 = wv[0][jj];
+                w1 = wv[1][jj];
+            } else {
+                w0 = live0 ? expf(acc[0][jj] - lse0) : 0.f;
+                w1 = live1 ? expf(acc[1][jj] - lse1) : 0.f;
+                if constexpr (WMODE == 1) {
+                    if (live0) p.wts[wrow0 + j] = w0;
+                    if (live1) p.wts[wrow1 + j] = w1;
+                }
+            }
+            const float g0 = live0 ? w0 * (acc[2][jj] - kp0) : 0.f;
+            const float g1 = live1 ? w1 * (acc[3][jj] - kp1) : 0.f;
             Gs[kk * GLD + (rg & 15) * 4 + (rg >> 4)] = g0;
             Gs[kk * GLD + (rg & 15) * 4 + ((rg + 32) >> 4)] = g1;
         }

@@ -91,6 +91,10 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, false, plx::BWD_DKV>, BwdTcCfg<64, false, plx::BWD_DKV>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<128>, plx::LlaGemmCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<64>, plx::LlaGemmCfg<64>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<128, 1>, plx::LlaGemmCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<64, 1>, plx::LlaGemmCfg<64>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<128, 2>, plx::LlaGemmCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<64, 2>, plx::LlaGemmCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<128>, plx::LlaOutCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<64>, plx::LlaOutCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_kbar_gemm_kernel<128>, plx::LlaKbarCfg<128>::SMEM);
@@ -408,6 +412,7 @@ bool dispatch_f32(const plx::FwdF32Params& p, int d, long long BH, cudaStream_t 
 struct LlaWorkspace {
     float *kbar, *x, *r, *p, *lse, *rs, *rs0;
     int* steps;
+    float* wts;      // the kept softmax weights [B H][N][N], or nullptr
 };
 size_t lla_ws_bytes(long long R, int d) {
     return 4 * align256(static_cast<size_t>(R) * d * sizeof(float)) + 4 * align256(static_cast<size_t>(R) * 4);
@@ -424,7 +429,13 @@ LlaWorkspace lla_ws_carve(void* base, long long R, int d) {
     w.rs = reinterpret_cast<float*>(c + 4 * vec + sc);
     w.rs0 = reinterpret_cast<float*>(c + 4 * vec + 2 * sc);
     w.steps = reinterpret_cast<int*>(c + 4 * vec + 3 * sc);
+    w.wts = nullptr;
     return w;
+}
+// The kept weights of every (b, h, i, j), j <= i, dense [B H][N][N] fp32 after
+// the rest of the workspace (d = 64, 128: the block form of the CG step).
+size_t lla_wts_bytes(long long BH, int N) {
+    return align256(static_cast<size_t>(BH) * N * static_cast<size_t>(N) * sizeof(float));
 }
 
 // plx_lla_f32's launches: kbar and lse (softmax attention of the keys
@@ -433,7 +444,7 @@ LlaWorkspace lla_ws_carve(void* base, long long R, int d) {
 template <int DPL>
 void launch_lla(const float* q, const float* k, const float* v, float* out, float* lse, const LlaWorkspace& w,
                 int N, long long BH, float scale, float lambda, int max_iters, float tol, cudaStream_t s) {
-    plx::LlaParams lp{q, k, w.kbar, w.lse, w.x, w.r, w.p, w.rs, w.rs0, w.steps, N, scale, lambda, tol * tol};
+    plx::LlaParams lp{q, k, w.kbar, w.lse, w.x, w.r, w.p, w.rs, w.rs0, w.steps, N, scale, lambda, tol * tol, w.wts};
     if constexpr (DPL == 2 || DPL == 4) {
         // d = 64, 128: kbar and lse in the block form of the CG step
         using Kc = plx::LlaKbarCfg<DPL * 32>;
@@ -449,8 +460,14 @@ void launch_lla(const float* q, const float* k, const float* v, float* out, floa
         // d = 64, 128: the step as two block GEMMs per key tile
         using G = plx::LlaGemmCfg<DPL * 32>;
         dim3 ggrid((N + G::BM - 1) / G::BM, static_cast<unsigned>(BH));
-        for (int it = 0; it < max_iters; ++it)
-            plx::plx_lla_cg_gemm_kernel<DPL * 32><<<ggrid, G::THREADS, G::SMEM, s>>>(lp);
+        for (int it = 0; it < max_iters; ++it) {
+            if (!w.wts)
+                plx::plx_lla_cg_gemm_kernel<DPL * 32, 0><<<ggrid, G::THREADS, G::SMEM, s>>>(lp);
+            else if (it == 0)      // the first step keeps the weights it computes
+                plx::plx_lla_cg_gemm_kernel<DPL * 32, 1><<<ggrid, G::THREADS, G::SMEM, s>>>(lp);
+            else
+                plx::plx_lla_cg_gemm_kernel<DPL * 32, 2><<<ggrid, G::THREADS, G::SMEM, s>>>(lp);
+        }
     } else {
         for (int it = 0; it < max_iters; ++it)
             plx::plx_lla_cg_step_kernel<DPL><<<grid, plx::LLA_WARPS * 32, plx::LlaTile<DPL>::SMEM, s>>>(lp);
@@ -1354,6 +1371,12 @@ size_t plx_lla_workspace_size(int B, int H, int N, int d) {
     return lla_ws_bytes(static_cast<long long>(B) * H * N, d);
 }
 
+size_t plx_lla_kept_weights_workspace_size(int B, int H, int N, int d) {
+    const size_t base = plx_lla_workspace_size(B, H, N, d);
+    if (base == 0 || (d != 64 && d != 128)) return base;
+    return base + lla_wts_bytes(static_cast<long long>(B) * H, N);
+}
+
 plx_status plx_lla_f32(const float* q, const float* k, const float* v, float* out, float* rho_out, float* lse,
                        int32_t* steps_out, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                        float scale, float lambda, int max_iters, float tol, void* stream) {
@@ -1374,7 +1397,10 @@ plx_status plx_lla_f32(const float* q, const float* k, const float* v, float* ou
         const long long R = BH * N;
         if (!workspace || workspace_bytes < lla_ws_bytes(R, d)) return PLX_ERR_WORKSPACE;
         if (!device_info()) return PLX_ERR_CUDA;          // kernel attributes (shared-memory sizes)
-        const LlaWorkspace w = lla_ws_carve(workspace, R, d);
+        LlaWorkspace w = lla_ws_carve(workspace, R, d);
+        // a workspace with room for the weights keeps them across the CG steps
+        if ((d == 64 || d == 128) && workspace_bytes >= lla_ws_bytes(R, d) + lla_wts_bytes(BH, N))
+            w.wts = reinterpret_cast<float*>(static_cast<char*>(workspace) + lla_ws_bytes(R, d));
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         switch (d / 32) {
             case 1: launch_lla<1>(q, k, v, out, lse, w, N, BH, scale, lambda, max_iters, tol, s); break;

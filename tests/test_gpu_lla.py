@@ -19,12 +19,12 @@ from parity import assert_f32
 pytestmark = pytest.mark.gpu
 
 
-def run_lla(x, lam, max_iters, tol):
+def run_lla(x, lam, max_iters, tol, keep_weights=False):
     import torch
     import parameterized_local_linear_02_b300 as plx
     t = {n: torch.from_numpy(getattr(x, n)).to("cuda") for n in ("q", "k", "v")}
     out, rho, lse, steps = plx.plx_lla_f32(t["q"], t["k"], t["v"], lam=lam, max_iters=max_iters, tol=tol,
-                                           scale=x.scale)
+                                           scale=x.scale, keep_weights=keep_weights)
     torch.cuda.synchronize()
     assert plx.plx_last_device_error() == 0
     return out.cpu().numpy(), rho.cpu().numpy(), lse.cpu().numpy(), steps.cpu().numpy()
@@ -136,13 +136,17 @@ def test_lla_well_conditioned_matches_direct_solve_at_fp32_tolerance(shape, lam)
 def test_lla_full_size_sampled_rows():
     """The bench's LLA workload in the launch configuration the bench times:
     B=4, H=16, N=2048, d=128 fp32, lambda = 0.1, at most 48 steps, tol 1e-4
-    (rows near prefix length d need the most, about 36 in fp64).
-    Sampled rows of three heads checked by their fp64 residuals and against
-    the direct solve."""
+    (rows near prefix length d need the most, about 36 in fp64), the softmax
+    weights kept across the steps.  Sampled rows of three heads checked by
+    their fp64 residuals and against the direct solve; the whole result equal,
+    bit for bit, to the path that recomputes the weights in every step."""
     B, H, N, d = 4, 16, 2048, 128
     x = inputs(B, H, N, d, seed=41)
     lam, tol, iters = 0.1, 1e-4, 48
-    out, rho, _, steps = run_lla(x, lam, iters, tol)
+    out, rho, lse, steps = run_lla(x, lam, iters, tol, keep_weights=True)
+    out0, rho0, lse0, steps0 = run_lla(x, lam, iters, tol)
+    assert np.array_equal(out, out0) and np.array_equal(rho, rho0)
+    assert np.array_equal(lse, lse0) and np.array_equal(steps, steps0)
     rows = [0, 1, 2, 63, 127, 128, 129, 500, 1023, 2047]
     heads = [(0, 0), (1, 9), (3, 15)]
     n_conv = _residual_checks(x, out, rho, steps, lam, tol, iters, heads, rows)
@@ -159,3 +163,21 @@ def test_lla_large_lambda_is_softmax_attention():
     for (b, h), (o_ref, lse_ref, rows) in oracle.prefill("sa", x.q, x.k, x.v, np.zeros_like(x.q), x.scale).items():
         assert_f32(out[b, h][rows], o_ref, f"LLA at lambda 1e6 vs softmax attention ({b}, {h})", tol=1e-4)
         assert float(np.max(np.abs(lse[b, h][rows] - lse_ref))) <= 1e-5
+
+
+@pytest.mark.parametrize("shape,tol", [((2, 3, 200, 64), 1e-4), ((1, 2, 130, 128), 0.0), ((3, 1, 70, 128), 1e-3)])
+def test_lla_kept_weights_bitwise_equal(shape, tol):
+    """With a workspace of plx_lla_kept_weights_workspace_size the CG steps
+    read the softmax weights the first step stored instead of recomputing them:
+    the same values in the same operations, so out, rho, lse and the step
+    counts are the recomputing path's, bit for bit (rows that stop early
+    included: tol > 0)."""
+    import parameterized_local_linear_02_b300 as plx
+    B, H, N, d = shape
+    assert plx.plx_lla_kept_weights_workspace_size(B, H, N, d) == (
+        plx.plx_lla_workspace_size(B, H, N, d) + ((B * H * N * N * 4 + 255) // 256) * 256)
+    x = inputs(B, H, N, d, seed=50 + N)
+    a = run_lla(x, 0.1, 12, tol, keep_weights=True)
+    b = run_lla(x, 0.1, 12, tol)
+    for got, ref, name in zip(a, b, ("out", "rho", "lse", "steps")):
+        assert np.array_equal(got, ref), name
