@@ -165,7 +165,10 @@ def test_lla_large_lambda_is_softmax_attention():
         assert float(np.max(np.abs(lse[b, h][rows] - lse_ref))) <= 1e-5
 
 
-@pytest.mark.parametrize("shape,tol", [((2, 3, 200, 64), 1e-4), ((1, 2, 130, 128), 0.0), ((3, 1, 70, 128), 1e-3)])
+@pytest.mark.parametrize("shape,tol", [((2, 3, 200, 64), 1e-4), ((1, 2, 130, 128), 0.0), ((3, 1, 70, 128), 1e-3),
+                                       ((1, 1, 1, 64), 0.0),
+                                       # every row stops before its first step: no weights are stored
+                                       ((1, 2, 90, 128), 2.0)])
 def test_lla_kept_weights_bitwise_equal(shape, tol):
     """With a workspace of plx_lla_kept_weights_workspace_size the CG steps
     read the softmax weights the first step stored instead of recomputing them:
