@@ -21,6 +21,7 @@
 #include "decode.cuh"
 #include "fwd_f32.cuh"
 #include "lla_f32.cuh"
+#include "lla_tc.cuh"
 #include "fwd_tc.cuh"
 #include "bwd_tc.cuh"
 #include "proj_tc.cuh"
@@ -95,6 +96,8 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<64, 1>, plx::LlaGemmCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<128, 2>, plx::LlaGemmCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<64, 2>, plx::LlaGemmCfg<64>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_cg_tc_kernel<128>, plx::LlaTcCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_cg_tc_kernel<64>, plx::LlaTcCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<128>, plx::LlaOutCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<64>, plx::LlaOutCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_kbar_gemm_kernel<128>, plx::LlaKbarCfg<128>::SMEM);
@@ -438,6 +441,21 @@ size_t lla_wts_bytes(long long BH, int N) {
     return align256(static_cast<size_t>(BH) * N * static_cast<size_t>(N) * sizeof(float));
 }
 
+// 3-D fp32 tensor map over the kept weights [BH][N][N] for the tensor-core CG
+// step: a {32 keys, 128 rows, 1} box, 128B swizzle (rows past N read as 0).
+// The row stride N * 4 bytes must be a multiple of 16: N % 4 == 0.
+bool make_wts_map(CUtensorMap* map, const float* wts, int N, long long BH) {
+    auto enc = encoder();
+    if (!enc || N % 4 != 0) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 4, static_cast<cuuint64_t>(N) * N * 4};
+    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(wts), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // plx_lla_f32's launches: kbar and lse (softmax attention of the keys
 // themselves), the CG set-up, max_iters CG steps, and Parallax's output with
 // the solved probe (centred).
@@ -459,12 +477,20 @@ void launch_lla(const float* q, const float* k, const float* v, float* out, floa
     if constexpr (DPL == 2 || DPL == 4) {
         // d = 64, 128: the step as two block GEMMs per key tile
         using G = plx::LlaGemmCfg<DPL * 32>;
+        using T = plx::LlaTcCfg<DPL * 32>;
         dim3 ggrid((N + G::BM - 1) / G::BM, static_cast<unsigned>(BH));
+        // with the weights kept, the later steps run on the tensor cores (split tf32)
+        CUtensorMap mw;
+        const bool tc = w.wts && make_wts_map(&mw, w.wts, N, BH);
+        const int n_blk = (N + T::BM - 1) / T::BM;
         for (int it = 0; it < max_iters; ++it) {
             if (!w.wts)
                 plx::plx_lla_cg_gemm_kernel<DPL * 32, 0><<<ggrid, G::THREADS, G::SMEM, s>>>(lp);
             else if (it == 0)      // the first step keeps the weights it computes
                 plx::plx_lla_cg_gemm_kernel<DPL * 32, 1><<<ggrid, G::THREADS, G::SMEM, s>>>(lp);
+            else if (tc)
+                plx::plx_lla_cg_tc_kernel<DPL * 32>
+                    <<<static_cast<unsigned>(n_blk * BH), T::THREADS, T::SMEM, s>>>(mw, lp, n_blk);
             else
                 plx::plx_lla_cg_gemm_kernel<DPL * 32, 2><<<ggrid, G::THREADS, G::SMEM, s>>>(lp);
         }
