@@ -928,11 +928,17 @@ def run_lla_bench(args, world, rank, local):
     (q.k, 2 d flop per causal pair), then each CG step of row i streams its
     i + 1 keys at 4 d flop per key (p.k and the update of Sigma p); the softmax
     pass for kbar costs 4 d and the output pass 8 d per causal pair.  The timed
-    call keeps the weights across the steps (the kept-weights workspace); the
-    path that recomputes them in every step (the minimal workspace, 2 d more
-    per key and step) is timed beside it.  The roofline is the fp32 FMA rate
-    of the CUDA cores (SMs x 128 lanes x 2 flop x the max SM clock).  L2 is
-    flushed before every launch sequence.  Prints one JSON line."""
+    call keeps the weights across the steps (the kept-weights workspace), and
+    its steps after the first run on the tensor cores in split tf32; the path
+    that recomputes the weights in every step on the CUDA cores (the minimal
+    workspace, 2 d more per key and step) is timed beside it.  The roofline is
+    that of the dominant kernel, the tensor-core CG step: its time is the
+    solve's minus that of the same call with one CG step (the k-bar pass, the
+    first step and the output pass), its work 4 d per key of the steps after
+    the first, its peak the dense tf32 rate (the measured bf16 burst rate x
+    the nominal tf32 / bf16 ratio 1.1 / 2.25); each product costs 3 tf32 MMA
+    products.  L2 is flushed before every launch sequence.  Prints one JSON
+    line."""
     import torch
     import parameterized_local_linear_02_b300 as plx
 
@@ -953,13 +959,13 @@ def run_lla_bench(args, world, rank, local):
     steps = torch.empty((B, H, N), dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    def call(workspace=ws):
-        plx.plx_lla_f32(q, k, v, lam=lam, max_iters=iters, tol=tol, workspace=workspace, out=out, lse=lse,
+    def call(workspace=ws, n_iters=iters):
+        plx.plx_lla_f32(q, k, v, lam=lam, max_iters=n_iters, tol=tol, workspace=workspace, out=out, lse=lse,
                         steps=steps, with_rho=False)
 
-    def timed(workspace):
+    def timed(workspace, n_iters=iters):
         for _ in range(max(3, args.warmup)):
-            call(workspace)
+            call(workspace, n_iters)
         torch.cuda.synchronize()
         ms = []
         for _ in range(max(3, args.steps)):
@@ -967,7 +973,7 @@ def run_lla_bench(args, world, rank, local):
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            call(workspace)
+            call(workspace, n_iters)
             b.record(stream)
             torch.cuda.synchronize()
             ms.append(a.elapsed_time(b))
@@ -979,27 +985,39 @@ def run_lla_bench(args, world, rank, local):
     ms = timed(ws)
     clocks = sampler.stop()
     med = float(np.median(ms))
-    med_min = float(np.median(timed(ws_min)))
     st = steps.double()
+    n_max, n_at_max = int(steps.max()), int((steps == iters).sum())
     keys = torch.arange(1, N + 1, device=dev, dtype=torch.float64)
     cg_flops = float((st * keys).sum()) * 4 * d
+    tc_flops = float((torch.clamp(st - 1, min=0) * keys).sum()) * 4 * d     # the steps after the first
     pairs = B * H * N * (N + 1) / 2
     flops = cg_flops + pairs * (2 + 12) * d
     value = flops / (med * 1e-3) / 1e12
+    med_min = float(np.median(timed(ws_min)))
+    med_one = float(np.median(timed(ws, 1)))       # k-bar, init, the first step (CUDA cores), output
+    tc_ms = med - med_one
+    tc_value = tc_flops / (tc_ms * 1e-3) / 1e12
+    peaks = read_peaks()
+    tf32_peak = peaks["bf16_tflops"] * 1.1 / 2.25
     props = torch.cuda.get_device_properties(dev)
     sm_max = clocks.get("sm_max_mhz") or 2032.0
     alu_peak = props.multi_processor_count * 128 * 2 * sm_max * 1e6 / 1e12
-    line = {"metric": "LLA (probe solved by fp32 CG) TFLOP/s on the CUDA cores, 1 GPU",
+    line = {"metric": "LLA (probe solved by conjugate gradients) TFLOP/s, 1 GPU",
             "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": len(ms), "warmup": max(3, args.warmup),
-            "ms_per_step": med, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+            "ms_per_step": med, "higher_is_better": True, "dtype": "f32, tf32x3", "data": "synthetic",
             "config": {"workload": "lla_b4_h16_n2048_d128", "B": B, "H": H, "N": N, "d": d, "lambda": lam,
                        "max_iters": iters, "tol": tol, "l2": "flushed (256 MiB write) before every launch sequence"},
-            "cg_steps": {"max": int(steps.max()), "mean": float(st.mean()),
-                         "rows_at_max": int((steps == iters).sum()), "rows": B * H * N},
-            "roofline": {"bound": "alu", "achieved": value, "peak": alu_peak, "unit": "TFLOP/s",
-                         "frac": value / alu_peak,
-                         "peak_source": f"{props.multi_processor_count} SMs x 128 fp32 lanes x 2 flop x {sm_max:.0f} MHz",
-                         "flop_per_launch_sequence": flops, "cg_flop": cg_flops},
+            "cg_steps": {"max": n_max, "mean": float(st.mean()), "rows_at_max": n_at_max, "rows": B * H * N},
+            "roofline": {"bound": "tensor", "kernel": "plx_lla_cg_tc_kernel<128> (CG steps 2 ..)",
+                         "achieved": tc_value, "peak": tf32_peak, "unit": "TFLOP/s", "frac": tc_value / tf32_peak,
+                         "peak_source": f"dense tf32: measured bf16 burst {peaks['bf16_tflops']} x 1.1 / 2.25 "
+                                        f"({peaks['source']})",
+                         "mma_products_per_product": 3, "ms_per_solve": tc_ms, "flop_per_solve": tc_flops,
+                         "ms_rest_of_solve": med_one},
+            "solve_vs_fp32_fma_peak": {"frac": value / alu_peak, "peak": alu_peak,
+                                       "peak_source": f"{props.multi_processor_count} SMs x 128 fp32 lanes x 2 flop x "
+                                                      f"{sm_max:.0f} MHz"},
+            "flop_per_launch_sequence": flops, "cg_flop": cg_flops,
             "weights": {"kept": "softmax weights of the CG steps stored by the first step (B H N^2 fp32 of workspace)",
                         "recomputed_ms_per_step": med_min,
                         "recomputed_value": flops / (med_min * 1e-3) / 1e12},

@@ -72,8 +72,49 @@ struct LlaTcCfg {
     static constexpr uint32_t TM_PHI = 0, TM_PLO = D, TM_U = 2 * D, TM_R = 3 * D, TM_GHI = 3 * D + 2 * BK,
                               TM_GLO = TM_GHI + BK, TM_COLS = 512;
     static_assert(TM_GLO + BK <= TM_COLS, "TMEM columns");
+    // the column and byte offsets lla_mma_r and lla_mma_u are written for
+    static_assert(BK == 32 && TM_PLO == TM_PHI + D && TM_GLO == TM_GHI + 32 && PANEL == 4096, "MMA batch layout");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
+
+// ------------------------------------------------- batched tf32 MMA issue
+// One warp-wide asm block per GEMM of a key tile, one elected lane issuing;
+// the descriptors are the stage's base descriptors plus a compile-time offset
+// in their low word (start address in 16-byte units; the offsets keep the
+// address below 256 KB, so no carry into the next field).
+//
+// lla_mma_r<D>: R = P K^T of a 32-key tile as two partial sums, over dims
+// [0, d/2) into t_d and [d/2, d) into t_d + 32; k-step s (8 dims) reads
+// P_hi / P_lo at TMEM columns t_a + 8 s / t_a + d + 8 s and the K tile's
+// panel s / 4 (32 rows x 128 B, 256 x 16 bytes apart) at (s % 4) x 32 bytes.
+// In each partial the hi.lo and lo.hi products come first, the hi.hi ones
+// last; the first MMA of a partial overwrites it.
+template <int D>
+__device__ __forceinline__ void lla_mma_r(uint32_t t_d, uint32_t t_a, uint64_t b_hi, uint64_t b_lo, uint32_t idesc);
+
+template <>
+__device__ __forceinline__ void lla_mma_r<64>(uint32_t t_d, uint32_t t_a, uint64_t b_hi, uint64_t b_lo, uint32_t idesc) {
+    asm volatile("{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 lo, ta, td;\n\t.reg .b64 db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\tadd.u32 td, %0, 0;\n\tadd.u32 ta, %1, 0; add.u32 lo, %4, 0; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pf;\n\tadd.u32 ta, %1, 64; add.u32 lo, %2, 0; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 8; add.u32 lo, %4, 2; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 72; add.u32 lo, %2, 2; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 16; add.u32 lo, %4, 4; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 80; add.u32 lo, %2, 4; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 24; add.u32 lo, %4, 6; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 88; add.u32 lo, %2, 6; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 0; add.u32 lo, %2, 0; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 8; add.u32 lo, %2, 2; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 16; add.u32 lo, %2, 4; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 24; add.u32 lo, %2, 6; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 td, %0, 32;\n\tadd.u32 ta, %1, 32; add.u32 lo, %4, 256; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pf;\n\tadd.u32 ta, %1, 96; add.u32 lo, %2, 256; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 40; add.u32 lo, %4, 258; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 104; add.u32 lo, %2, 258; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 48; add.u32 lo, %4, 260; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 112; add.u32 lo, %2, 260; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 56; add.u32 lo, %4, 262; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 120; add.u32 lo, %2, 262; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 32; add.u32 lo, %2, 256; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 40; add.u32 lo, %2, 258; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 48; add.u32 lo, %2, 260; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 56; add.u32 lo, %2, 262; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\t}"
+                 ::"r"(t_d), "r"(t_a), "r"(static_cast<uint32_t>(b_hi)), "r"(static_cast<uint32_t>(b_hi >> 32)),
+                   "r"(static_cast<uint32_t>(b_lo)), "r"(static_cast<uint32_t>(b_lo >> 32)), "r"(idesc)
+                 : "memory");
+}
+
+template <>
+__device__ __forceinline__ void lla_mma_r<128>(uint32_t t_d, uint32_t t_a, uint64_t b_hi, uint64_t b_lo, uint32_t idesc) {
+    asm volatile("{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 lo, ta, td;\n\t.reg .b64 db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\tadd.u32 td, %0, 0;\n\tadd.u32 ta, %1, 0; add.u32 lo, %4, 0; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pf;\n\tadd.u32 ta, %1, 128; add.u32 lo, %2, 0; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 8; add.u32 lo, %4, 2; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 136; add.u32 lo, %2, 2; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 16; add.u32 lo, %4, 4; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 144; add.u32 lo, %2, 4; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 24; add.u32 lo, %4, 6; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 152; add.u32 lo, %2, 6; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 32; add.u32 lo, %4, 256; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 160; add.u32 lo, %2, 256; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 40; add.u32 lo, %4, 258; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 168; add.u32 lo, %2, 258; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 48; add.u32 lo, %4, 260; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 176; add.u32 lo, %2, 260; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 56; add.u32 lo, %4, 262; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 184; add.u32 lo, %2, 262; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 0; add.u32 lo, %2, 0; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 8; add.u32 lo, %2, 2; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 16; add.u32 lo, %2, 4; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 24; add.u32 lo, %2, 6; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 32; add.u32 lo, %2, 256; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 40; add.u32 lo, %2, 258; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 48; add.u32 lo, %2, 260; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 56; add.u32 lo, %2, 262; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 td, %0, 32;\n\tadd.u32 ta, %1, 64; add.u32 lo, %4, 512; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pf;\n\tadd.u32 ta, %1, 192; add.u32 lo, %2, 512; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 72; add.u32 lo, %4, 514; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 200; add.u32 lo, %2, 514; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 80; add.u32 lo, %4, 516; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 208; add.u32 lo, %2, 516; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 88; add.u32 lo, %4, 518; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 216; add.u32 lo, %2, 518; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 96; add.u32 lo, %4, 768; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 224; add.u32 lo, %2, 768; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 104; add.u32 lo, %4, 770; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 232; add.u32 lo, %2, 770; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 112; add.u32 lo, %4, 772; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 240; add.u32 lo, %2, 772; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 120; add.u32 lo, %4, 774; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 248; add.u32 lo, %2, 774; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 64; add.u32 lo, %2, 512; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 72; add.u32 lo, %2, 514; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 80; add.u32 lo, %2, 516; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 88; add.u32 lo, %2, 518; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 96; add.u32 lo, %2, 768; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 104; add.u32 lo, %2, 770; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 112; add.u32 lo, %2, 772; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 120; add.u32 lo, %2, 774; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\t}"
+                 ::"r"(t_d), "r"(t_a), "r"(static_cast<uint32_t>(b_hi)), "r"(static_cast<uint32_t>(b_hi >> 32)),
+                   "r"(static_cast<uint32_t>(b_lo)), "r"(static_cast<uint32_t>(b_lo >> 32)), "r"(idesc)
+                 : "memory");
+}
+// lla_mma_u: U_tile = G K of a 32-key tile (fresh): G_hi / G_lo at TMEM
+// columns t_a + 8 s / t_a + 32 + 8 s, K^T [d][32 keys] at s x 32 bytes.
+__device__ __forceinline__ void lla_mma_u(uint32_t t_d, uint32_t t_a, uint64_t b_hi, uint64_t b_lo, uint32_t idesc) {
+    asm volatile("{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 lo, ta, td;\n\t.reg .b64 db;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\tmov.b32 td, %0;\n\tadd.u32 ta, %1, 0; add.u32 lo, %4, 0; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pf;\n\tadd.u32 ta, %1, 32; add.u32 lo, %2, 0; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 8; add.u32 lo, %4, 2; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 40; add.u32 lo, %2, 2; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 16; add.u32 lo, %4, 4; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 48; add.u32 lo, %2, 4; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 24; add.u32 lo, %4, 6; mov.b64 db, {lo, %5};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 56; add.u32 lo, %2, 6; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 0; add.u32 lo, %2, 0; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 8; add.u32 lo, %2, 2; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 16; add.u32 lo, %2, 4; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\tadd.u32 ta, %1, 24; add.u32 lo, %2, 6; mov.b64 db, {lo, %3};\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [td], [ta], db, %6, pt;\n\t}"
+                 ::"r"(t_d), "r"(t_a), "r"(static_cast<uint32_t>(b_hi)), "r"(static_cast<uint32_t>(b_hi >> 32)),
+                   "r"(static_cast<uint32_t>(b_lo)), "r"(static_cast<uint32_t>(b_lo >> 32)), "r"(idesc)
+                 : "memory");
+}
 
 // One CG step over every row that is still active, reading the weights kept
 // by the first step (p.wts, through mapW: dims {N, N, BH}, box {32, 128, 1}).
@@ -361,24 +402,11 @@ __global__ void __launch_bounds__(LlaTcCfg<D>::THREADS, 1)
         auto gemm_u = [&](int tp) -> bool {
             if (!wait_warp(g_full, tp & 1)) return false;
             tc_fence_after();
-            if (lane == 0) {
-                const uint32_t kb_hi = cv0 + (tp % NCV) * Cfg::CV_STAGE + 2 * Cfg::KA_BYTES;
-                const uint32_t kb_lo = kb_hi + Cfg::KB_BYTES;
-#pragma unroll
-                for (int s = 0; s < BK / 8; ++s) {
-                    const uint64_t bh_d = sdesc_sw128(kb_hi + 32 * s, 16, 1024);
-                    const uint64_t bl_d = sdesc_sw128(kb_lo + 32 * s, 16, 1024);
-                    mma_ts_tf32(tmem + Cfg::TM_U, tmem + Cfg::TM_GHI + 8 * s, bl_d, ID_U, s > 0 ? 1u : 0u);
-                    mma_ts_tf32(tmem + Cfg::TM_U, tmem + Cfg::TM_GLO + 8 * s, bh_d, ID_U, 1u);
-                }
-#pragma unroll
-                for (int s = 0; s < BK / 8; ++s)
-                    mma_ts_tf32(tmem + Cfg::TM_U, tmem + Cfg::TM_GHI + 8 * s, sdesc_sw128(kb_hi + 32 * s, 16, 1024),
-                                ID_U, 1u);
-                mma_commit(g_free);                      // U_tile complete, G free
-                mma_commit(&cv_empty[tp % NCV]);
-            }
-            __syncwarp();
+            const uint32_t kb_hi = cv0 + (tp % NCV) * Cfg::CV_STAGE + 2 * Cfg::KA_BYTES;
+            lla_mma_u(tmem + Cfg::TM_U, tmem + Cfg::TM_GHI, sdesc_sw128(kb_hi, 16, 1024),
+                      sdesc_sw128(kb_hi + Cfg::KB_BYTES, 16, 1024), ID_U);
+            mma_commit_warp(g_free);                     // U_tile complete, G free
+            mma_commit_warp(&cv_empty[tp % NCV]);
             return true;
         };
         for (int t = 0; ok && t < n_tiles; ++t) {
@@ -388,29 +416,13 @@ __global__ void __launch_bounds__(LlaTcCfg<D>::THREADS, 1)
             // R of the previous tile has been read by the row warps
             if (t >= 1 && !wait_warp(r_free, (t - 1) & 1)) { ok = false; break; }
             tc_fence_after();
-            if (lane == 0) {
-                const uint32_t ka_hi = cv0 + cs * Cfg::CV_STAGE, ka_lo = ka_hi + Cfg::KA_BYTES;
-                // two partial sums over halves of the dims; in each, the small
-                // products first, then the hi.hi ones
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const uint32_t dR = tmem + Cfg::TM_R + hf * BK;
-#pragma unroll
-                    for (int s = hf * D / 16; s < (hf + 1) * D / 16; ++s) {
-                        const uint32_t off = (s / 4) * Cfg::PANEL + (s % 4) * 32;
-                        mma_ts_tf32(dR, tmem + Cfg::TM_PHI + 8 * s, sdesc_sw128(ka_lo + off, 16, 1024), ID_R,
-                                    s > hf * D / 16 ? 1u : 0u);
-                        mma_ts_tf32(dR, tmem + Cfg::TM_PLO + 8 * s, sdesc_sw128(ka_hi + off, 16, 1024), ID_R, 1u);
-                    }
-#pragma unroll
-                    for (int s = hf * D / 16; s < (hf + 1) * D / 16; ++s) {
-                        const uint32_t off = (s / 4) * Cfg::PANEL + (s % 4) * 32;
-                        mma_ts_tf32(dR, tmem + Cfg::TM_PHI + 8 * s, sdesc_sw128(ka_hi + off, 16, 1024), ID_R, 1u);
-                    }
-                }
-                mma_commit(r_full);
+            {
+                // two partial sums over halves of the dims (the small products first)
+                const uint32_t ka_hi = cv0 + cs * Cfg::CV_STAGE;
+                lla_mma_r<D>(tmem + Cfg::TM_R, tmem + Cfg::TM_PHI, sdesc_sw128(ka_hi, 16, 1024),
+                             sdesc_sw128(ka_hi + Cfg::KA_BYTES, 16, 1024), ID_R);
+                mma_commit_warp(r_full);
             }
-            __syncwarp();
             issued_any = 1;
             // the previous tile's U GEMM after this tile's R GEMM, so the row warps
             // form G of tile t - 1 while R of tile t runs
@@ -420,8 +432,7 @@ __global__ void __launch_bounds__(LlaTcCfg<D>::THREADS, 1)
         if (!ok) fail();
         // drain: every MMA issued by this warp has finished before TMEM is freed
         if (issued_any) {
-            if (lane == 0) mma_commit(drain);
-            __syncwarp();
+            mma_commit_warp(drain);
             if (!wait_warp(drain, 0)) fail();
         }
     } else {

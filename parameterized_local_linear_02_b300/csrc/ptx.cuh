@@ -263,17 +263,6 @@ __host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
     return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
 }
-// D[tmem] (+)= A[tmem] * B[smem]^T with kind::tf32 (one fp32 element of A per
-// TMEM column, 8 columns per MMA); issued by the calling thread alone
-__device__ __forceinline__ void mma_ts_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 // x rounded to the nearest tf32 value (ties away from zero), as fp32: the
 // high part of the split x = hi + lo, with lo = x - hi exact in fp32
 __device__ __forceinline__ float tf32_hi(float x) {
