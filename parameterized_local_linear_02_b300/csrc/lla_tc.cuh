@@ -63,9 +63,13 @@ struct LlaTcCfg {
     static constexpr int W_STAGE = BM * BK * 4;            // [128 rows][128 B], swizzled by the TMA
     static constexpr int OFF_CV = 0;
     static constexpr int OFF_W = OFF_CV + NCV * CV_STAGE;
-    static constexpr int OFF_BAR = OFF_W + NW * W_STAGE;
-    // cv_full, cv_empty [NCV]; w_full, w_empty [NW]; r_full, r_free, g_full, g_free, p_ready, drain
-    static constexpr int N_BARS = 2 * NCV + 2 * NW + 6;
+    // the epilogue: p, x, r rows of each row warp, rows padded to D + 4 floats,
+    // over the converter and weight buffers (free by then)
+    static constexpr int LDE = D + 4;
+    static constexpr int EPI_BYTES = ROW_WARPS * 3 * 32 * LDE * 4;
+    static constexpr int OFF_BAR = (OFF_W + NW * W_STAGE) > EPI_BYTES ? (OFF_W + NW * W_STAGE) : EPI_BYTES;
+    // cv_full, cv_empty [NCV]; w_full, w_empty [NW]; r_full, r_free, g_full, g_free, p_ready, drain; epi [ROW_WARPS]
+    static constexpr int N_BARS = 2 * NCV + 2 * NW + 6 + ROW_WARPS;
     static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + TMEM slot and abort flag, + alignment
     // TMEM columns
     // R: two partial sums (dims 0 .. d/2 - 1 and d/2 .. d - 1), 32 columns each
@@ -139,7 +143,8 @@ __global__ void __launch_bounds__(LlaTcCfg<D>::THREADS, 1)
     uint64_t* g_free = g_full + 1;
     uint64_t* p_ready = g_free + 1;
     uint64_t* drain = p_ready + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* epi = drain + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi + Cfg::ROW_WARPS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -181,6 +186,7 @@ __global__ void __launch_bounds__(LlaTcCfg<D>::THREADS, 1)
         mbar_init(g_free, 1);
         mbar_init(p_ready, Cfg::ROW_WARPS);
         mbar_init(drain, 1);
+        for (int w = 0; w < Cfg::ROW_WARPS; ++w) mbar_init(&epi[w], 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&mapW);
@@ -310,10 +316,28 @@ __global__ void __launch_bounds__(LlaTcCfg<D>::THREADS, 1)
                 mbar_arrive(g_full);
             }
         }
+        // the epilogue's rows (below) in shared memory: p, x, r of each row warp,
+        // padded to D + 4 floats, over the converter and weight buffers
+        constexpr int LDE = Cfg::LDE;
+        float* pr = reinterpret_cast<float*>(smem) + (warp * 3 * 32 + lane) * LDE;
+        float* xr = pr + 32 * LDE;
+        float* rr = xr + 32 * LDE;
         if (ok) {
             if (wait_warp(g_free, (n_tiles - 1) & 1)) {
+                // every MMA has finished and every tile has been consumed, so those
+                // buffers are free: each lane fetches its row of p, x and r by 1-D bulk
+                // copies (all in flight at once) while the last tile is added
+                const int nrow = max(0, min(32, N - (ib + warp * 32)));   // the warp's rows inside the head
+                if (lane == 0) mbar_arrive_expect_tx(&epi[warp], static_cast<uint32_t>(nrow) * 3 * D * 4);
+                __syncwarp();
+                if (i < N) {
+                    bulk_g2s(pr, p.p + grow * D, D * 4, &epi[warp]);
+                    bulk_g2s(xr, p.x + grow * D, D * 4, &epi[warp]);
+                    bulk_g2s(rr, p.r + grow * D, D * 4, &epi[warp]);
+                }
                 tc_fence_after();
                 add_tile();
+                if (!wait_warp(&epi[warp], 0)) ok = false;   // (the copies complete on their own)
             } else {
                 ok = false;
             }
@@ -321,55 +345,64 @@ __global__ void __launch_bounds__(LlaTcCfg<D>::THREADS, 1)
         if (!ok) {
             fail();
         } else {
-            // ---- Ap = U + lambda p and one conjugate-gradient step per active row
-            float* xo = p.x + grow * D;
-            float* ro = p.r + grow * D;
-            float* po = p.p + grow * D;
-            float pap = 0.f;
-            if (act) {
+            // ---- Ap = U + lambda p and one conjugate-gradient step per active row,
+            // on the row in shared memory (the lanes' padded rows fall on different
+            // banks); the updated rows go back by 1-D bulk copies
+            {
+                float pap = 0.f;
+                if (act) {
 #pragma unroll
-                for (int o = 0; o < D; o += 4) {
-                    const float4 pv = *reinterpret_cast<const float4*>(prow + o);
-                    const float v4[4] = {pv.x, pv.y, pv.z, pv.w};
+                    for (int o = 0; o < D; o += 4) {
+                        const float4 pv = *reinterpret_cast<const float4*>(pr + o);
+                        const float v4[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        acc[o + m] = fmaf(p.lambda, v4[m], acc[o + m]);   // acc := Ap
-                        pap = fmaf(v4[m], acc[o + m], pap);
+                        for (int m = 0; m < 4; ++m) {
+                            acc[o + m] = fmaf(p.lambda, v4[m], acc[o + m]);   // acc := Ap
+                            pap = fmaf(v4[m], acc[o + m], pap);
+                        }
+                        asm volatile("" ::: "memory");
                     }
                 }
-            }
-            const bool okr = act && pap > 0.f;
-            if (act && !okr) p.rs[grow] = 0.f;             // breakdown: stop the row
-            if (okr) {
-                const float alpha = rs / pap;
-                float rn = 0.f;
+                const bool okr = act && pap > 0.f;
+                if (act && !okr) p.rs[grow] = 0.f;         // breakdown: stop the row
+                if (okr) {
+                    const float alpha = rs / pap;
+                    float rn = 0.f;
 #pragma unroll
-                for (int o = 0; o < D; o += 4) {
-                    const float4 pv = *reinterpret_cast<const float4*>(prow + o);
-                    const float4 xv = *reinterpret_cast<const float4*>(xo + o);
-                    const float4 rv = *reinterpret_cast<const float4*>(ro + o);
-                    const float v4[4] = {pv.x, pv.y, pv.z, pv.w};
-                    float x4[4] = {xv.x, xv.y, xv.z, xv.w}, r4[4] = {rv.x, rv.y, rv.z, rv.w};
+                    for (int o = 0; o < D; o += 4) {
+                        const float4 pv = *reinterpret_cast<const float4*>(pr + o);
+                        const float4 xv = *reinterpret_cast<const float4*>(xr + o);
+                        const float4 rv = *reinterpret_cast<const float4*>(rr + o);
+                        const float v4[4] = {pv.x, pv.y, pv.z, pv.w};
+                        float x4[4] = {xv.x, xv.y, xv.z, xv.w}, r4[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        x4[m] = fmaf(alpha, v4[m], x4[m]);
-                        r4[m] = fmaf(-alpha, acc[o + m], r4[m]);
-                        rn = fmaf(r4[m], r4[m], rn);
-                        acc[o + m] = r4[m];                  // acc := the new residual
+                        for (int m = 0; m < 4; ++m) {
+                            x4[m] = fmaf(alpha, v4[m], x4[m]);
+                            r4[m] = fmaf(-alpha, acc[o + m], r4[m]);
+                            rn = fmaf(r4[m], r4[m], rn);
+                        }
+                        *reinterpret_cast<float4*>(xr + o) = make_float4(x4[0], x4[1], x4[2], x4[3]);
+                        *reinterpret_cast<float4*>(rr + o) = make_float4(r4[0], r4[1], r4[2], r4[3]);
+                        asm volatile("" ::: "memory");     // keep the loads of later dims from being hoisted
                     }
-                    *reinterpret_cast<float4*>(xo + o) = make_float4(x4[0], x4[1], x4[2], x4[3]);
-                    *reinterpret_cast<float4*>(ro + o) = make_float4(r4[0], r4[1], r4[2], r4[3]);
-                }
-                const float beta = rn / rs;
+                    const float beta = rn / rs;
 #pragma unroll
-                for (int o = 0; o < D; o += 4) {
-                    const float4 pv = *reinterpret_cast<const float4*>(prow + o);
-                    *reinterpret_cast<float4*>(po + o) =
-                        make_float4(fmaf(beta, pv.x, acc[o]), fmaf(beta, pv.y, acc[o + 1]),
-                                    fmaf(beta, pv.z, acc[o + 2]), fmaf(beta, pv.w, acc[o + 3]));
+                    for (int o = 0; o < D; o += 4) {
+                        const float4 pv = *reinterpret_cast<const float4*>(pr + o);
+                        const float4 rv = *reinterpret_cast<const float4*>(rr + o);
+                        *reinterpret_cast<float4*>(pr + o) = make_float4(fmaf(beta, pv.x, rv.x), fmaf(beta, pv.y, rv.y),
+                                                                         fmaf(beta, pv.z, rv.z), fmaf(beta, pv.w, rv.w));
+                    }
+                    p.rs[grow] = rn;
+                    p.steps[grow] += 1;
+                    // the rows back to global memory; the CTA leaves only once they are written
+                    fence_proxy_async_smem();
+                    bulk_s2g(p.x + grow * D, xr, D * 4);
+                    bulk_s2g(p.r + grow * D, rr, D * 4);
+                    bulk_s2g(p.p + grow * D, pr, D * 4);
+                    bulk_commit_group();
+                    bulk_wait_all();
                 }
-                p.rs[grow] = rn;
-                p.steps[grow] += 1;
             }
         }
     } else if (warp == Cfg::W_PROD) {
@@ -463,11 +496,11 @@ __global__ void __launch_bounds__(LlaTcCfg<D>::THREADS, 1)
             }
         };
         bool ok = true;
-        if (n_tiles > 0) load_tile(0, cur);
         for (int t = 0; t < n_tiles; ++t) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) { ok = false; break; }   // one read for the warp
-            float4 nxt[NB][4];
-            if (t + 1 < n_tiles) load_tile(t + 1, nxt);
+            // the tile's loads go out before the wait for a free stage (the ring of
+            // NCV converted stages keeps the converters ahead of the MMAs)
+            load_tile(t, cur);
             const int cs = t % NCV;
             if (t >= NCV && !wait_warp(&cv_empty[cs], ((t / NCV) - 1) & 1)) { ok = false; break; }
             uint8_t* ka_hi = sCV + cs * Cfg::CV_STAGE;
@@ -507,10 +540,6 @@ __global__ void __launch_bounds__(LlaTcCfg<D>::THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&cv_full[cs]);
-#pragma unroll
-            for (int h = 0; h < NB; ++h)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) cur[h][e] = nxt[h][e];
         }
         if (!ok) fail();
     }
