@@ -467,7 +467,10 @@ plx_status plx_decode_combine(const void* partials, int groups, int num_splits, 
  * (the intercept at k = q_i of the weighted ridge fit of v on k - q_i).
  * Conjugate gradients start from rho = 0.  Each row runs at most max_iters
  * steps and stops once |r|^2 <= tol^2 |mu|^2 (tol = 0 runs every step), or
- * when p . Ap <= 0.  All arithmetic is fp32 on the CUDA cores.
+ * when p . Ap <= 0.  The arithmetic is fp32 on the CUDA cores, except the
+ * CG steps after the first of the kept-weights path with N % 4 == 0 (see
+ * plx_lla_kept_weights_workspace_size), which run on the tensor cores with
+ * every product split in tf32 (fp32 accumulation).
  *
  *   q, k, v  : fp32 [B][H][N][d], 16-byte aligned.
  *   out      : fp32 [B][H][N][d] output, 16-byte aligned.
@@ -477,7 +480,7 @@ plx_status plx_decode_combine(const void* partials, int groups, int num_splits, 
  *   workspace: device scratch of plx_lla_workspace_size(B, H, N, d) bytes,
  *              256-byte aligned, no initialisation; with at least
  *              plx_lla_kept_weights_workspace_size(B, H, N, d) bytes the
- *              softmax weights are kept across the CG steps (same results).
+ *              softmax weights are kept across the CG steps (see there).
  *   B, H, N >= 1, B * H <= 65535; d a multiple of 32 in [32, 256];
  *   lambda >= 0 (finite); max_iters >= 0; tol >= 0 (finite).
  *   lambda = 0 needs every row's Sigma_KK to be non-singular (a prefix of at
@@ -498,11 +501,17 @@ size_t plx_lla_workspace_size(int B, int H, int N, int d);
  * Workspace bytes with which plx_lla_f32 keeps the CG steps' softmax weights
  * w_ij = exp(s_ij - lse_i) from the first step instead of recomputing them in
  * every step (they do not depend on the iterate): plx_lla_workspace_size plus
- * B*H*N*N*4 bytes, for d in {64, 128} (for other d the same as
- * plx_lla_workspace_size).  A call given at least this many bytes takes that
- * path; its results are those of the recomputing path, bit for bit.  The
- * extra space grows as N^2 (1.07 GB at B = 4, H = 16, N = 2048; 275 GB at
- * N = 32768), so it is for short contexts.
+ * B*H*N*N*4 bytes (rounded up to 256), for d in {64, 128} (for other d the
+ * same as plx_lla_workspace_size).  A call given at least this many bytes
+ * takes that path; the first step (CUDA cores, fp32) stores the weights, and
+ *   - N % 4 == 0: the later steps read them by TMA and run on the tensor
+ *     cores with every product split in tf32 (x = hi + lo, hi.hi + hi.lo +
+ *     lo.hi, fp32 sums): results within fp32 rounding of the recomputing
+ *     path's, not bit for bit;
+ *   - N % 4 != 0: the later steps read them on the CUDA cores: the
+ *     recomputing path's results, bit for bit.
+ * The extra space grows as N^2 (1.07 GB at B = 4, H = 16, N = 2048; 275 GB
+ * at N = 32768), so it is for short contexts.
  */
 size_t plx_lla_kept_weights_workspace_size(int B, int H, int N, int d);
 

@@ -432,8 +432,10 @@ def plx_lla_f32(q, k, v, *, lam, max_iters, tol=0.0, scale=None, workspace=None,
     row, a row stopping once |r| <= tol |mu|).  Returns ``(out, rho, lse,
     steps)``; rho (the solved probe) and steps (int32 per row) are None when
     not requested.  ``keep_weights`` allocates the larger workspace with which
-    the CG steps keep their softmax weights (same results; B H N^2 fp32 more);
-    a caller-given ``workspace`` of that size has the same effect."""
+    the CG steps keep their softmax weights (B H N^2 fp32 more; for N % 4 == 0
+    and d in {64, 128} the steps after the first then run on the tensor cores
+    in split tf32, within fp32 rounding of the recomputing path); a
+    caller-given ``workspace`` of that size has the same effect."""
     B, H, N, d = q.shape
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v)):

@@ -25,7 +25,9 @@
 //   4. plx_lla_out_kernel: o from Parallax's output formula with rho := x,
 //      in centred form.
 // The pages warn that the solve is unstable in low precision; every step
-// here is fp32.
+// here is fp32.  With the weights kept (d = 64, 128, N % 4 == 0), the steps
+// after the first run on the tensor cores instead (lla_tc.cuh), each product
+// split in tf32 to stay at fp32-level rounding.
 #pragma once
 #include "bwd_f32.cuh"   // warp_sum
 #include "status.cuh"
