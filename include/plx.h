@@ -59,7 +59,7 @@ typedef enum {
     PLX_ERR_MISALIGNED = 3,  /* pointer not 16-byte aligned (lse: 4-byte) */
     PLX_ERR_CUDA = 4,        /* a CUDA call or kernel launch failed */
     PLX_ERR_TIMEOUT = 5,     /* a device-side wait gave up (see plx_last_device_error) */
-    PLX_ERR_WORKSPACE = 6,   /* decode workspace missing or too small */
+    PLX_ERR_WORKSPACE = 6,   /* workspace missing or too small (any entry point that takes one) */
     PLX_ERR_RANGE = 7,       /* plx_fwd produced a non-finite output (see plx_last_device_error) */
     PLX_ERR_BOUNDS = 8       /* the debug build (PLX_DEBUG) caught an index outside its buffer and skipped
                                 the access (see plx_last_device_error) */

@@ -27,10 +27,12 @@
 //        p into TMEM, then per tile read R from TMEM (releasing it for the
 //        next tile's GEMM), add the previous tile's U_tile to the row's sum,
 //        read the row's 32 weights from shared memory, form G and split it
-//        into TMEM; at the end the CG update of the row from the sum;
+//        into TMEM; at the end the CG update of the row from the sum, its
+//        rows of p, x and r moved by 1-D bulk copies through the freed ring
+//        buffers;
 //   4    weight producer: one TMA load per tile of the [BH][N][N] weights
 //        (box 32 keys x 128 rows, 128-byte swizzle), a 4-stage ring;
-//   5    MMA issuer (lane 0);
+//   5    MMA issuer (one elected lane; one asm block per GEMM of a tile);
 //   6-7  converters: read the key tile from global memory, split it and
 //        store K_hi, K_lo twice, as [32 keys][d] (B of R = P K^T) and as
 //        [d][32 keys] (B of U += G K), both K-major with 128-byte swizzle;

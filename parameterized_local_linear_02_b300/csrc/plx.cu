@@ -788,7 +788,7 @@ const char* plx_strerror(plx_status status) {
         case PLX_ERR_MISALIGNED: return "misaligned pointer";
         case PLX_ERR_CUDA: return "CUDA error";
         case PLX_ERR_TIMEOUT: return "device-side wait timed out";
-        case PLX_ERR_WORKSPACE: return "decode workspace missing or too small";
+        case PLX_ERR_WORKSPACE: return "workspace missing or too small";
         case PLX_ERR_RANGE: return "non-finite output (inputs outside the supported range)";
         case PLX_ERR_BOUNDS: return "index outside its buffer (debug build)";
         default: return "unknown status";
