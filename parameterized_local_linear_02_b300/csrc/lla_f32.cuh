@@ -29,6 +29,7 @@
 // after the first run on the tensor cores instead (lla_tc.cuh), each product
 // split in tf32 to stay at fp32-level rounding.
 #pragma once
+#include <type_traits>
 #include "bwd_f32.cuh"   // warp_sum
 #include "status.cuh"
 
@@ -797,7 +798,12 @@ struct LlaOutCfg {
     static_assert(D == 64 || D == 128, "the block output pass is built for d in {64, 128}");
 };
 
-template <int D>
+// KEPT: p.wts holds the weights the first CG step kept (those of every row that
+// took a step); a block whose rows all took one reads them instead of forming
+// S = scale q K^T.  The first step formed them with this kernel's arithmetic
+// (the same products in the same order, then exp(s - lse)), so the output is
+// the same bit for bit; a block with a row that took no step forms S.
+template <int D, bool KEPT = false>
 __global__ void __launch_bounds__(256) plx_lla_out_gemm_kernel(const LlaParams p, const float* v, float* out,
                                                                float* lse_out) {
     using Cfg = LlaOutCfg<D>;
@@ -822,9 +828,14 @@ __global__ void __launch_bounds__(256) plx_lla_out_gemm_kernel(const LlaParams p
     const float* K = p.k + bh * p.N * D;
     const float* V = v + bh * p.N * D;
 
+    // the kept weights serve this block if every row of it took a CG step
+    int no_step = 0;
+    if (KEPT && tid < BM && ib + tid < p.N) no_step = p.steps[bh * p.N + ib + tid] == 0;
+    const bool use_w = KEPT && !__syncthreads_or(no_step);
     if (tid < BM) s_lse[tid] = ib + tid < p.N ? p.lse[bh * p.N + ib + tid] : 0.f;
     for (int idx = tid; idx < 2 * BM * (D / 4); idx += Cfg::THREADS) {
         const int r = idx / (D / 4), c = idx % (D / 4);
+        if (use_w && r < BM) continue;                   // q rows: the weights are kept
         const int i = ib + (r & (BM - 1));
         float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < p.N) {
@@ -907,36 +918,57 @@ __global__ void __launch_bounds__(256) plx_lla_out_gemm_kernel(const LlaParams p
         const float* vt = vstage + (t & 1) * BK * LD;
         const int j0 = t * BK;
         const int nk = min(BK, kmax + 1 - j0);
+        // the kept weights of this tile (use_w), loaded ahead of phase 1's FMAs
+        float wk[2][4];
+        if (use_w) {
+            const size_t wrow0 = (bh * p.N + ib + rg) * static_cast<size_t>(p.N);
+            const size_t wrow1 = wrow0 + 32 * static_cast<size_t>(p.N);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int kk = kg + 8 * jj, j = j0 + kk;
+                wk[0][jj] = (kk < nk && in0 && j <= ib + rg) ? p.wts[wrow0 + j] : 0.f;
+                wk[1][jj] = (kk < nk && in1 && j <= ib + rg + 32) ? p.wts[wrow1 + j] : 0.f;
+            }
+        }
+        // phase 1: acc[m][jj], m = 0, 1: s of rows rg, rg + 32; m = 2, 3: rho.k of
+        // the same rows (with the kept weights only m = 2, 3)
         float acc[4][4];
 #pragma unroll
         for (int m = 0; m < 4; ++m)
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) acc[m][jj] = 0.f;
+        auto phase1 = [&](auto m0c) {
+            constexpr int M0 = decltype(m0c)::value;
 #pragma unroll 4
-        for (int c = 0; c < D; c += 4) {
-            float4 a[4], b[4];
+            for (int c = 0; c < D; c += 4) {
+                float4 a[4], b[4];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) a[m] = *reinterpret_cast<const float4*>(QP + (rg + 32 * m) * LD + c);
+                for (int m = M0; m < 4; ++m) a[m] = *reinterpret_cast<const float4*>(QP + (rg + 32 * m) * LD + c);
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) b[jj] = *reinterpret_cast<const float4*>(kt + (kg + 8 * jj) * LD + c);
+                for (int jj = 0; jj < 4; ++jj) b[jj] = *reinterpret_cast<const float4*>(kt + (kg + 8 * jj) * LD + c);
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+                for (int m = M0; m < 4; ++m)
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    acc[m][jj] = fmaf(a[m].x, b[jj].x, acc[m][jj]);
-                    acc[m][jj] = fmaf(a[m].y, b[jj].y, acc[m][jj]);
-                    acc[m][jj] = fmaf(a[m].z, b[jj].z, acc[m][jj]);
-                    acc[m][jj] = fmaf(a[m].w, b[jj].w, acc[m][jj]);
-                }
-        }
+                    for (int jj = 0; jj < 4; ++jj) {
+                        acc[m][jj] = fmaf(a[m].x, b[jj].x, acc[m][jj]);
+                        acc[m][jj] = fmaf(a[m].y, b[jj].y, acc[m][jj]);
+                        acc[m][jj] = fmaf(a[m].z, b[jj].z, acc[m][jj]);
+                        acc[m][jj] = fmaf(a[m].w, b[jj].w, acc[m][jj]);
+                    }
+            }
+        };
+        if (use_w)
+            phase1(std::integral_constant<int, 2>{});
+        else
+            phase1(std::integral_constant<int, 0>{});
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             const int kk = kg + 8 * jj, j = j0 + kk;
             // keys past the tile's rows read unfilled shared memory: their r' is not
             // formed at all (0 x NaN would still be NaN)
             const bool v0 = kk < nk && in0 && j <= ib + rg, v1 = kk < nk && in1 && j <= ib + rg + 32;
-            const float w0 = v0 ? expf(acc[0][jj] - lse0) : 0.f;
-            const float w1 = v1 ? expf(acc[1][jj] - lse1) : 0.f;
+            const float w0 = use_w ? wk[0][jj] : (v0 ? expf(acc[0][jj] - lse0) : 0.f);
+            const float w1 = use_w ? wk[1][jj] : (v1 ? expf(acc[1][jj] - lse1) : 0.f);
             const float rc0 = v0 ? acc[2][jj] - kx0 : 0.f, rc1 = v1 ? acc[3][jj] - kx1 : 0.f;
             L0 += w0;
             L1 += w1;

@@ -100,6 +100,8 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_lla_cg_tc_kernel<64>, plx::LlaTcCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<128>, plx::LlaOutCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<64>, plx::LlaOutCfg<64>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<128, true>, plx::LlaOutCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<64, true>, plx::LlaOutCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_kbar_gemm_kernel<128>, plx::LlaKbarCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_kbar_gemm_kernel<64>, plx::LlaKbarCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_proj_tc_kernel<128>, ProjCfg<128>::SMEM);
@@ -501,7 +503,10 @@ void launch_lla(const float* q, const float* k, const float* v, float* out, floa
     if constexpr (DPL == 2 || DPL == 4) {
         using O = plx::LlaOutCfg<DPL * 32>;
         dim3 ogrid((N + O::BM - 1) / O::BM, static_cast<unsigned>(BH));
-        plx::plx_lla_out_gemm_kernel<DPL * 32><<<ogrid, O::THREADS, O::SMEM, s>>>(lp, v, out, lse);
+        if (w.wts)       // the weights the first step kept serve the blocks whose rows all took a step
+            plx::plx_lla_out_gemm_kernel<DPL * 32, true><<<ogrid, O::THREADS, O::SMEM, s>>>(lp, v, out, lse);
+        else
+            plx::plx_lla_out_gemm_kernel<DPL * 32><<<ogrid, O::THREADS, O::SMEM, s>>>(lp, v, out, lse);
     } else {
         plx::plx_lla_out_kernel<DPL><<<grid, plx::LLA_WARPS * 32, 0, s>>>(lp, v, out, lse);
     }
