@@ -503,13 +503,16 @@ size_t plx_lla_workspace_size(int B, int H, int N, int d);
  * every step (they do not depend on the iterate): plx_lla_workspace_size plus
  * B*H*N*N*4 bytes (rounded up to 256), for d in {64, 128} (for other d the
  * same as plx_lla_workspace_size).  A call given at least this many bytes
- * takes that path; the first step (CUDA cores, fp32) stores the weights, and
+ * takes that path: the kbar pass stores the scores s_ij, the first step
+ * (CUDA cores, fp32) turns them into the weights, the output pass reads them
+ * (for blocks of rows that all took a step), and
  *   - N % 4 == 0: the later steps read them by TMA and run on the tensor
  *     cores with every product split in tf32 (x = hi + lo, hi.hi + hi.lo +
  *     lo.hi, fp32 sums): results within fp32 rounding of the recomputing
  *     path's, not bit for bit;
  *   - N % 4 != 0: the later steps read them on the CUDA cores: the
- *     recomputing path's results, bit for bit.
+ *     recomputing path's results, bit for bit (the scores and weights are
+ *     formed with the recomputing path's products, in the same order).
  * The extra space grows as N^2 (1.07 GB at B = 4, H = 16, N = 2048; 275 GB
  * at N = 32768), so it is for short contexts.
  */

@@ -51,7 +51,8 @@ struct LlaParams {
     float lambda;
     float tol2;          // tol^2
     // [BH][N][N] fp32: the CG steps' softmax weights w_ij = exp(s_ij - lse_i),
-    // j <= i, kept from the first step (nullptr: every step recomputes them)
+    // j <= i, kept from the first step, which forms them from the scores the
+    // kbar pass stored there (nullptr: every step recomputes them)
     float* wts;
 };
 
@@ -372,10 +373,12 @@ struct LlaGemmCfg {
 };
 
 // WMODE 0: the step computes the weights w_ij from s_ij = scale q_i.k_j and
-// lse_i; 1: it also stores them (those of active rows) in p.wts; 2: it reads
-// them from p.wts and computes only p.k_j, half of phase 1.  The weights do
-// not depend on the iterate, and the stored values are the computed ones, so
-// the three modes give the same bits.
+// lse_i; 3 (the first step with the weights kept): it reads the scores s_ij
+// the kbar pass stored in p.wts, forms the weights and stores them over the
+// scores (active rows), and computes only p.k_j, half of phase 1; 2 (the
+// later steps): it reads the weights.  The weights do not depend on the
+// iterate, and the kbar pass forms s_ij with the same products in the same
+// order, so the three modes give the same bits.
 template <int D, int WMODE = 0>
 __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p) {
     using Cfg = LlaGemmCfg<D>;
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
     for (int idx = tid; idx < 2 * BM * (D / 4); idx += Cfg::THREADS) {
         const int r = idx / (D / 4), c = idx % (D / 4);
         const int i = ib + (r & (BM - 1));
-        if (WMODE == 2 && r < BM) continue;              // q rows: the weights are stored
+        if (WMODE >= 2 && r < BM) continue;              // q rows: the weights (or scores) are stored
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < p.N) {
             const size_t off = (bh * p.N + i) * D + c * 4;
@@ -497,12 +500,12 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
         const float* kt = stage + (t & 1) * BK * LD;
         const int j0 = t * BK;
         const int nk = min(BK, kmax + 1 - j0);
-        // rows rg, rg + 32 of the block and their weight rows (WMODE 1, 2)
+        // rows rg, rg + 32 of the block and their weight rows (WMODE 2, 3)
         const size_t wrow0 = (bh * p.N + ib + rg) * static_cast<size_t>(p.N);
         const size_t wrow1 = wrow0 + 32 * static_cast<size_t>(p.N);
         float wv[2][4];
-        if constexpr (WMODE == 2) {
-            // the stored weights of this tile, loaded ahead of phase 1's FMAs
+        if constexpr (WMODE >= 2) {
+            // the stored weights (or scores) of this tile, loaded ahead of phase 1's FMAs
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 const int kk = kg + 8 * jj, j = j0 + kk;
@@ -511,8 +514,8 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
             }
         }
         // phase 1: acc[m][jj], m = 0, 1: s of rows rg, rg+32; m = 2, 3: p.k of the same rows
-        // (WMODE 2: only m = 2, 3)
-        constexpr int M0 = WMODE == 2 ? 2 : 0;
+        // (WMODE 2, 3: only m = 2, 3)
+        constexpr int M0 = WMODE >= 2 ? 2 : 0;
         float acc[4][4];
 #pragma unroll
         for (int m = 0; m < 4; ++m)
@@ -545,13 +548,14 @@ __global__ void __launch_bounds__(256) plx_lla_cg_gemm_kernel(const LlaParams p)
             if constexpr (WMODE == 2) {
                 w0 = wv[0][jj];
                 w1 = wv[1][jj];
+            } else if constexpr (WMODE == 3) {
+                w0 = live0 ? expf(wv[0][jj] - lse0) : 0.f;
+                w1 = live1 ? expf(wv[1][jj] - lse1) : 0.f;
+                if (live0) p.wts[wrow0 + j] = w0;
+                if (live1) p.wts[wrow1 + j] = w1;
             } else {
                 w0 = live0 ? expf(acc[0][jj] - lse0) : 0.f;
                 w1 = live1 ? expf(acc[1][jj] - lse1) : 0.f;
-                if constexpr (WMODE == 1) {
-                    if (live0) p.wts[wrow0 + j] = w0;
-                    if (live1) p.wts[wrow1 + j] = w1;
-                }
             }
             const float g0 = live0 ? w0 * (acc[2][jj] - kp0) : 0.f;
             const float g1 = live1 ? w1 * (acc[3][jj] - kp1) : 0.f;
@@ -1069,7 +1073,9 @@ struct LlaKbarCfg {
     static_assert(D == 64 || D == 128, "the block kbar pass is built for d in {64, 128}");
 };
 
-template <int D>
+// KEEP: also store each causal pair's score s_ij = scale q_i . k_j in p.wts
+// (the first CG step turns those of its active rows into the weights).
+template <int D, bool KEEP = false>
 __global__ void __launch_bounds__(256) plx_lla_kbar_gemm_kernel(const LlaParams p, float* kbar, float* lse) {
     using Cfg = LlaKbarCfg<D>;
     constexpr int BM = Cfg::BM, BK = Cfg::BK, LD = Cfg::LD, DG = Cfg::DG, GLD = Cfg::GLD;
@@ -1177,6 +1183,11 @@ __global__ void __launch_bounds__(256) plx_lla_kbar_gemm_kernel(const LlaParams 
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             const int kk = kg + 8 * jj, j = j0 + kk;
+            if constexpr (KEEP) {
+                if (kk < nk && in0 && j <= ib + rg) p.wts[(bh * p.N + ib + rg) * static_cast<size_t>(p.N) + j] = acc[0][jj];
+                if (kk < nk && in1 && j <= ib + rg + 32)
+                    p.wts[(bh * p.N + ib + rg + 32) * static_cast<size_t>(p.N) + j] = acc[1][jj];
+            }
             if (!(kk < nk && in0 && j <= ib + rg)) acc[0][jj] = -INFINITY;
             if (!(kk < nk && in1 && j <= ib + rg + 32)) acc[1][jj] = -INFINITY;
             t0 = fmaxf(t0, acc[0][jj]);

@@ -92,10 +92,12 @@ const DeviceInfo* device_info() {
     e = e ? e : set_smem(plx::plx_bwd_tc_kernel<64, false, plx::BWD_DKV>, BwdTcCfg<64, false, plx::BWD_DKV>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<128>, plx::LlaGemmCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<64>, plx::LlaGemmCfg<64>::SMEM);
-    e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<128, 1>, plx::LlaGemmCfg<128>::SMEM);
-    e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<64, 1>, plx::LlaGemmCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<128, 2>, plx::LlaGemmCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<64, 2>, plx::LlaGemmCfg<64>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<128, 3>, plx::LlaGemmCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_cg_gemm_kernel<64, 3>, plx::LlaGemmCfg<64>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_kbar_gemm_kernel<128, true>, plx::LlaKbarCfg<128>::SMEM);
+    e = e ? e : set_smem(plx::plx_lla_kbar_gemm_kernel<64, true>, plx::LlaKbarCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_cg_tc_kernel<128>, plx::LlaTcCfg<128>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_cg_tc_kernel<64>, plx::LlaTcCfg<64>::SMEM);
     e = e ? e : set_smem(plx::plx_lla_out_gemm_kernel<128>, plx::LlaOutCfg<128>::SMEM);
@@ -469,7 +471,10 @@ void launch_lla(const float* q, const float* k, const float* v, float* out, floa
         // d = 64, 128: kbar and lse in the block form of the CG step
         using Kc = plx::LlaKbarCfg<DPL * 32>;
         dim3 kgrid((N + Kc::BM - 1) / Kc::BM, static_cast<unsigned>(BH));
-        plx::plx_lla_kbar_gemm_kernel<DPL * 32><<<kgrid, Kc::THREADS, Kc::SMEM, s>>>(lp, w.kbar, w.lse);
+        if (w.wts)       // it keeps the scores for the first CG step
+            plx::plx_lla_kbar_gemm_kernel<DPL * 32, true><<<kgrid, Kc::THREADS, Kc::SMEM, s>>>(lp, w.kbar, w.lse);
+        else
+            plx::plx_lla_kbar_gemm_kernel<DPL * 32><<<kgrid, Kc::THREADS, Kc::SMEM, s>>>(lp, w.kbar, w.lse);
     } else {
         plx::FwdF32Params f{q, k, k, nullptr, w.kbar, w.lse, N, scale};
         launch_f32<DPL, false>(f, BH, s);
@@ -488,8 +493,8 @@ void launch_lla(const float* q, const float* k, const float* v, float* out, floa
         for (int it = 0; it < max_iters; ++it) {
             if (!w.wts)
                 plx::plx_lla_cg_gemm_kernel<DPL * 32, 0><<<ggrid, G::THREADS, G::SMEM, s>>>(lp);
-            else if (it == 0)      // the first step keeps the weights it computes
-                plx::plx_lla_cg_gemm_kernel<DPL * 32, 1><<<ggrid, G::THREADS, G::SMEM, s>>>(lp);
+            else if (it == 0)      // the first step turns the kept scores into the weights
+                plx::plx_lla_cg_gemm_kernel<DPL * 32, 3><<<ggrid, G::THREADS, G::SMEM, s>>>(lp);
             else if (tc)
                 plx::plx_lla_cg_tc_kernel<DPL * 32>
                     <<<static_cast<unsigned>(n_blk * BH), T::THREADS, T::SMEM, s>>>(mw, lp, n_blk);
